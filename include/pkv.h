@@ -1,0 +1,166 @@
+/*
+ * pkv.h -- C ABI of the GB300 paged-KV attention step (libpkv.so).
+ *
+ * One step of a unified prefill/decode scheduler: every request in the step advances
+ * by q_len tokens (1 for a decode, a causal chunk for a chunked prefill) on top of the
+ * context_len tokens it already has in a paged KV cache.  This is the problem as
+ * niuwancheng.cn "11. chunked prefill and unified scheduling" states it (section "token
+ * budget per step": each request records how many tokens are computed and how many it
+ * advances this step), with 16-token pages addressed through a block table
+ * (lshu.cn/news/11576 §2.2 "written by page index", §2.3 "16 tokens per block").
+ *
+ * Call order within a step (hotelren.com/news/6181127 §3.1: append the new K/V, then
+ * score against all S+t cached keys): pkv_kv_append, then pkv_paged_attention_step.
+ *
+ * Conventions for every entry point
+ *  - Pointers named d_* or documented "device" are CUDA device pointers; all other
+ *    pointers are host pointers.  The caller owns every buffer; the library allocates
+ *    nothing and keeps no per-call state.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Work is enqueued asynchronously; only pkv_read_device_error synchronises.
+ *  - Return value: PKV_OK (0) or a negative pkv_status.  On an error detected on the
+ *    host nothing is launched.  Inconsistent device data (a page id outside the pool, a
+ *    position past the block-table row, q_offsets that disagree with total_q_tokens)
+ *    never traps: the kernel ORs a bit into *dev_err_flag (when non-NULL), skips the
+ *    offending token / tile and completes; read the flag with pkv_read_device_error.
+ *
+ * Tensor layouts (row-major, innermost last)
+ *   q, out      [total_q_tokens][num_q_heads][head_dim]      dtype
+ *   k_new,v_new [total_q_tokens][num_kv_heads][head_dim]     dtype
+ *   k_cache,
+ *   v_cache     [num_pages][num_kv_heads][16][head_dim]      dtype
+ *               (one contiguous 16 x head_dim block per page and KV head)
+ *   block_table [num_reqs][max_pages_per_req] int32 physical page ids
+ *   Token t of the step belongs to request r when q_offsets[r] <= t < q_offsets[r+1];
+ *   its position is context_lens[r] + (t - q_offsets[r]); it lives in page
+ *   block_table[r][pos / 16], slot pos % 16 (global slot id page * 16 + pos % 16).
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_PAGE_SIZE 16
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef enum { PKV_BF16 = 0, PKV_FP16 = 1 } pkv_dtype;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,     /* null pointer, negative size, page_size != 16, ... */
+    PKV_ERR_UNSUPPORTED = -2,     /* head_dim not 64/128, Hq % Hkv != 0, group > 8, dtype */
+    PKV_ERR_CAPACITY = -3,        /* max_context_len + max_q_len beyond the block table */
+    PKV_ERR_WORKSPACE = -4,       /* workspace NULL or smaller than required */
+    PKV_ERR_CUDA = -5,            /* a CUDA runtime call or launch failed */
+    PKV_ERR_DEVICE = -6           /* pkv_read_device_error found a non-zero flag */
+} pkv_status;
+
+/* Bits OR-ed into *dev_err_flag by the kernels. */
+#define PKV_DEVERR_PAGE_RANGE 1   /* page id outside [0, num_pages) */
+#define PKV_DEVERR_TABLE_RANGE 2  /* position past max_pages_per_req * 16 */
+#define PKV_DEVERR_TOKENS 4       /* q_offsets[num_reqs] != total_q_tokens, or lengths
+                                     above the host-declared maxima */
+#define PKV_DEVERR_TIMEOUT 8      /* a bounded wait on an asynchronous copy gave up */
+
+/*
+ * Description of one step.  Host integers size the launches; the four arrays are device
+ * pointers the kernels read.  The host integers must bound the device data:
+ *   total_q_tokens == q_offsets[num_reqs], max_q_len >= every q_lens[r],
+ *   max_context_len >= every context_lens[r],
+ *   ceil((max_context_len + max_q_len) / 16) <= max_pages_per_req is NOT required
+ *   (tables may be sized per request) but every request's own
+ *   ceil((context_lens[r] + q_lens[r]) / 16) must fit in max_pages_per_req.
+ */
+typedef struct {
+    int32_t num_reqs;            /* requests in the step (>= 0) */
+    int32_t num_q_heads;         /* Hq */
+    int32_t num_kv_heads;        /* Hkv, Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8} */
+    int32_t head_dim;            /* D in {64, 128} */
+    int32_t page_size;           /* must be 16 */
+    int32_t num_pages;           /* pages in each pool */
+    int32_t max_pages_per_req;   /* block_table row stride */
+    int32_t total_q_tokens;      /* T = sum of q_lens */
+    int32_t max_q_len;
+    int32_t max_context_len;
+    int32_t dtype;               /* pkv_dtype; one dtype for q, k, v, out */
+    const int32_t* q_lens;       /* device [num_reqs] */
+    const int32_t* q_offsets;    /* device [num_reqs + 1], exclusive prefix sum of q_lens */
+    const int32_t* context_lens; /* device [num_reqs], tokens cached BEFORE this step */
+    const int32_t* block_table;  /* device [num_reqs * max_pages_per_req] */
+} pkv_step_desc;
+
+/*
+ * pkv_kv_append -- write this step's new K/V rows into their pages.
+ * Defined by lshu.cn/news/11576 §2.2 (K/V written by page index into a pre-allocated
+ * pool of fixed pages) and hotelren.com/news/6181127 §3.1 (the new K and V are appended,
+ * the cache grows from S+t-1 to S+t).
+ *   k_new, v_new       device [T][Hkv][D]
+ *   k_cache, v_cache   device [num_pages][Hkv][16][D], updated in place (only the
+ *                      slots of this step's tokens are written; bit-exact copies)
+ *   slot_mapping_out   device int64 [T] or NULL: receives page * 16 + pos % 16
+ *   dev_err_flag       device int32 or NULL (see PKV_DEVERR_*)
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.  T == 0 is a no-op returning PKV_OK.
+ */
+PKV_API int pkv_kv_append(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                  void* k_cache, void* v_cache, int64_t* slot_mapping_out,
+                  int32_t* dev_err_flag, void* stream);
+
+/*
+ * pkv_attention_workspace_bytes -- device workspace the attention step needs for this
+ * description (split-KV partial results and the device-built work list).  Depends only
+ * on the host integers of *desc and on the current device's SM count.  Returns 0 for
+ * an invalid description.
+ */
+PKV_API size_t pkv_attention_workspace_bytes(const pkv_step_desc* desc);
+
+/*
+ * pkv_paged_attention_step -- causal softmax attention of every new query row over all
+ * keys of its request up to and including its own position, K/V read from the pages.
+ * Defined by hotelren.com/news/6181127 §1.1 (position i depends on 0..i), §2.1 (scores
+ * masked to -inf above the diagonal, row softmax, times V), §3.1 (a decode row scores
+ * all S+t cached keys), §5.1 skeleton softmax(q K^T) V with the scale made explicit;
+ * niuwancheng.cn "11. chunked prefill..." (a chunk reads the earlier chunks' K/V like a
+ * decode, same result as one-shot).
+ *   q             device [T][Hq][D]
+ *   k_cache,
+ *   v_cache       device pools (after this step's pkv_kv_append)
+ *   out           device [T][Hq][D], written in full (fp32 accumulation, rounded to
+ *                 nearest-even at the end)
+ *   scale         multiplies q.k before the softmax (1/sqrt(D) for standard attention)
+ *   workspace     device, >= pkv_attention_workspace_bytes(desc) bytes, 256-byte aligned;
+ *                 contents need no initialisation and are clobbered
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ */
+PKV_API int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const void* k_cache,
+                             const void* v_cache, void* out, float scale, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_err_flag, void* stream);
+
+/*
+ * pkv_read_device_error -- synchronise `stream`, copy *dev_err_flag (device) to
+ * *host_value and return PKV_OK when it is zero, PKV_ERR_DEVICE when not, PKV_ERR_CUDA
+ * when the copy fails.  The only synchronising entry point.
+ */
+PKV_API int pkv_read_device_error(const int32_t* dev_err_flag, int32_t* host_value, void* stream);
+
+/* Human-readable name of a pkv_status value (static storage). */
+PKV_API const char* pkv_status_string(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+PKV_API int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -33,6 +33,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_PAGE_TOKENS 16 /* lshu.cn/news/11576 §2.3: 16 tokens per block */
@@ -112,7 +113,7 @@ int64_t oracle_kv_bytes_per_token(int64_t layers, int64_t n_kv_heads, int64_t d_
 /* For each (row, head):  s_j = scale * <q, k_j>  (j = 0..pos)             */
 /*                        m = max_j s_j,  w_j = exp(s_j - m),  Z = sum w_j */
 /*                        out = sum_j (w_j / Z) v_j                         */
-/* Returns 0, or -1 on a bad argument (nothing written).                    */
+/* Returns 0, -1 on a bad argument (nothing written), -3 when out of memory. */
 /* ---------------------------------------------------------------------- */
 int oracle_attention_rows(int dtype, const uint16_t* q, const int32_t* pos, int32_t n_rows,
                           const uint16_t* k, const uint16_t* v, int32_t n_kv, int32_t Hq,
@@ -124,10 +125,25 @@ int oracle_attention_rows(int dtype, const uint16_t* q, const int32_t* pos, int3
         if (pos[i] < 0 || pos[i] >= n_kv) return -1;
     const int32_t group = Hq / Hkv;
     const int64_t units = (int64_t)n_rows * Hq;
+    const int64_t kv_elems = (int64_t)n_kv * Hkv * D;
+
+    /* widen K and V once (exact), then work in double only */
+    double* kd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
+    double* vd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
+    if (!kd || !vd) {
+        free(kd);
+        free(vd);
+        return -3;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < kv_elems; ++e) {
+        kd[e] = widen(dtype, k[e]);
+        vd[e] = widen(dtype, v[e]);
+    }
 
 #pragma omp parallel
     {
-        double* qd = (double*)__builtin_alloca(sizeof(double) * (size_t)D);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t u = 0; u < units; ++u) {
             const int32_t i = (int32_t)(u / Hq);
@@ -136,32 +152,35 @@ int oracle_attention_rows(int dtype, const uint16_t* q, const int32_t* pos, int3
             const int32_t p = pos[i];
             for (int32_t d = 0; d < D; ++d) qd[d] = widen(dtype, q[((int64_t)i * Hq + h) * D + d]);
 
-            /* pass 1: the row maximum of the scores */
+            /* pass 1: the row maximum of the scores s_j = scale * <q, k_j>, j = 0..p */
             double m = -INFINITY;
             for (int32_t j = 0; j <= p; ++j) {
-                const uint16_t* kj = k + ((int64_t)j * Hkv + g) * D;
+                const double* kj = kd + ((int64_t)j * Hkv + g) * D;
                 double s = 0.0;
-                for (int32_t d = 0; d < D; ++d) s += qd[d] * widen(dtype, kj[d]);
+                for (int32_t d = 0; d < D; ++d) s += qd[d] * kj[d];
                 s *= scale;
                 if (s > m) m = s;
             }
-            /* pass 2: weights, normaliser and weighted sum of V */
+            /* pass 2: weights w_j = exp(s_j - m), normaliser Z, weighted sum of V */
             double* o = out + ((int64_t)i * Hq + h) * D;
             for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
             double Z = 0.0;
             for (int32_t j = 0; j <= p; ++j) {
-                const uint16_t* kj = k + ((int64_t)j * Hkv + g) * D;
-                const uint16_t* vj = v + ((int64_t)j * Hkv + g) * D;
+                const double* kj = kd + ((int64_t)j * Hkv + g) * D;
+                const double* vj = vd + ((int64_t)j * Hkv + g) * D;
                 double s = 0.0;
-                for (int32_t d = 0; d < D; ++d) s += qd[d] * widen(dtype, kj[d]);
+                for (int32_t d = 0; d < D; ++d) s += qd[d] * kj[d];
                 s *= scale;
                 const double w = exp(s - m);
                 Z += w;
-                for (int32_t d = 0; d < D; ++d) o[d] += w * widen(dtype, vj[d]);
+                for (int32_t d = 0; d < D; ++d) o[d] += w * vj[d];
             }
             for (int32_t d = 0; d < D; ++d) o[d] /= Z;
         }
+        free(qd);
     }
+    free(kd);
+    free(vd);
     return 0;
 }
 

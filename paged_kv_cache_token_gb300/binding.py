@@ -1,0 +1,152 @@
+"""ctypes binding of libpkv.so -- argument marshalling only.
+
+Every function here has the name of the C entry point it calls (without the ``pkv_``
+prefix) and forwards raw device pointers taken from torch tensors together with the
+caller's current CUDA stream.  All arithmetic runs in the library's CUDA kernels; there
+is no fallback of any kind: if the shared library is missing or fails to load, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+OK = 0
+STATUS = {0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED",
+          -3: "PKV_ERR_CAPACITY", -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_CUDA",
+          -6: "PKV_ERR_DEVICE"}
+DEVERR_PAGE_RANGE, DEVERR_TABLE_RANGE, DEVERR_TOKENS, DEVERR_TIMEOUT = 1, 2, 4, 8
+BF16, FP16 = 0, 1
+DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16}
+
+EXPORTED = ("pkv_kv_append", "pkv_attention_workspace_bytes", "pkv_paged_attention_step",
+            "pkv_read_device_error", "pkv_status_string", "pkv_version")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__("%s returned %s (%d)" % (fn, STATUS.get(status, "?"), status))
+        self.status = status
+
+
+class StepDesc(ctypes.Structure):
+    """Mirror of ``pkv_step_desc`` (include/pkv.h)."""
+    _fields_ = [
+        ("num_reqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("max_pages_per_req", ctypes.c_int32), ("total_q_tokens", ctypes.c_int32),
+        ("max_q_len", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("q_lens", ctypes.c_void_p), ("q_offsets", ctypes.c_void_p),
+        ("context_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libpkv.so (raises OSError if it is absent: build it with build.build())."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise OSError("libpkv.so not found at %s; run paged_kv_cache_token_gb300.build.build()"
+                      % p)
+    lib = ctypes.CDLL(p)
+    V, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.pkv_kv_append.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V, V]
+    lib.pkv_kv_append.restype = ctypes.c_int
+    lib.pkv_attention_workspace_bytes.argtypes = [ctypes.POINTER(StepDesc)]
+    lib.pkv_attention_workspace_bytes.restype = sz
+    lib.pkv_paged_attention_step.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V,
+                                             ctypes.c_float, V, sz, V, V]
+    lib.pkv_paged_attention_step.restype = ctypes.c_int
+    lib.pkv_read_device_error.argtypes = [V, ctypes.POINTER(ctypes.c_int32), V]
+    lib.pkv_read_device_error.restype = ctypes.c_int
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_version.argtypes = []
+    lib.pkv_version.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def make_desc(*, num_reqs, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages_per_req,
+              total_q_tokens, max_q_len, max_context_len, dtype, q_lens=None, q_offsets=None,
+              context_lens=None, block_table=None, page_size=16) -> StepDesc:
+    """Fill a StepDesc; the four arrays are int32 CUDA tensors (or raw addresses)."""
+    def addr(x):
+        if x is None:
+            return None
+        return x.data_ptr() if isinstance(x, torch.Tensor) else int(x)
+    code = DTYPE_CODE.get(dtype, dtype)
+    return StepDesc(num_reqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                    max_pages_per_req, total_q_tokens, max_q_len, max_context_len, code,
+                    addr(q_lens), addr(q_offsets), addr(context_lens), addr(block_table))
+
+
+def version() -> int:
+    return load().pkv_version()
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()
+
+
+def kv_append(desc: StepDesc, k_new, v_new, k_cache, v_cache, slot_mapping=None, err=None,
+              stream=None, check: bool = True) -> int:
+    rc = load().pkv_kv_append(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                              _ptr(v_cache), _ptr(slot_mapping), _ptr(err), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_kv_append", rc)
+    return rc
+
+
+def attention_workspace_bytes(desc: StepDesc) -> int:
+    return int(load().pkv_attention_workspace_bytes(ctypes.byref(desc)))
+
+
+def paged_attention_step(desc: StepDesc, q, k_cache, v_cache, out, scale: float, workspace,
+                         err=None, stream=None, check: bool = True,
+                         workspace_bytes: Optional[int] = None) -> int:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None \
+        else workspace_bytes
+    rc = load().pkv_paged_attention_step(ctypes.byref(desc), _ptr(q), _ptr(k_cache),
+                                         _ptr(v_cache), _ptr(out), float(scale), _ptr(workspace),
+                                         nbytes, _ptr(err), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_paged_attention_step", rc)
+    return rc
+
+
+def read_device_error(err: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the flag value (0 = no device-detected error)."""
+    val = ctypes.c_int32(0)
+    rc = load().pkv_read_device_error(_ptr(err), ctypes.byref(val), _stream(stream))
+    if rc not in (OK, -6):
+        raise PkvError("pkv_read_device_error", rc)
+    return int(val.value)

@@ -1,0 +1,183 @@
+// C ABI of libpkv.so: argument checks on the host, then kernel launches on the caller's
+// stream.  Declarations and the contract of every entry point are in include/pkv.h.
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+
+#include "launch.h"
+#include "pkv.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int num_sms_current_device() {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by both calls.  Returns PKV_OK or the first problem found.
+int check_desc(const pkv_step_desc* d) {
+    if (!d) return PKV_ERR_INVALID_ARG;
+    if (d->page_size != PKV_PAGE_SIZE) return PKV_ERR_INVALID_ARG;
+    if (d->num_reqs < 0 || d->total_q_tokens < 0 || d->max_q_len < 0 ||
+        d->max_context_len < 0 || d->num_pages <= 0 || d->max_pages_per_req <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (d->num_q_heads <= 0 || d->num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+    if (d->dtype != PKV_BF16 && d->dtype != PKV_FP16) return PKV_ERR_UNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (d->num_q_heads % d->num_kv_heads) return PKV_ERR_UNSUPPORTED;
+    const int g = d->num_q_heads / d->num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return PKV_ERR_UNSUPPORTED;
+    if (d->num_reqs == 0 && d->total_q_tokens != 0) return PKV_ERR_INVALID_ARG;
+    if (d->total_q_tokens > 0 && d->max_q_len == 0) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(d->max_q_len) > d->total_q_tokens) return PKV_ERR_INVALID_ARG;
+    // a request of max_q_len tokens cannot fit a block-table row at all
+    if (static_cast<int64_t>(d->max_q_len) > static_cast<int64_t>(d->max_pages_per_req) * 16)
+        return PKV_ERR_CAPACITY;
+    // positions are int32 on the device
+    if (static_cast<int64_t>(d->max_context_len) + d->max_q_len >= INT_MAX / 2)
+        return PKV_ERR_CAPACITY;
+    if (static_cast<int64_t>(d->num_pages) * d->num_kv_heads * 16 * d->head_dim >
+        (int64_t(1) << 40))
+        return PKV_ERR_INVALID_ARG;
+    if (d->num_reqs > 0 &&
+        (!d->q_lens || !d->q_offsets || !d->context_lens || !d->block_table))
+        return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+// Requests with at least this many new tokens take the tensor-core prefill path.
+// INT_MAX keeps every row on the streaming path.
+int prefill_min_q() { return INT_MAX; }
+
+pkv::WorkspaceLayout layout_for(const pkv_step_desc* d, int num_sms) {
+    return pkv::workspace_layout(d->num_reqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
+                                 d->total_q_tokens, d->max_q_len, num_sms, prefill_min_q());
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_CAPACITY: return "PKV_ERR_CAPACITY";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_DEVICE: return "PKV_ERR_DEVICE";
+        default: return "PKV_UNKNOWN_STATUS";
+    }
+}
+
+int pkv_kv_append(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                  void* k_cache, void* v_cache, int64_t* slot_mapping_out,
+                  int32_t* dev_err_flag, void* stream) {
+    const int rc = check_desc(desc);
+    if (rc != PKV_OK) return rc;
+    if (desc->total_q_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PKV_ERR_INVALID_ARG;
+    if (slot_mapping_out && (reinterpret_cast<uintptr_t>(slot_mapping_out) & 7u))
+        return PKV_ERR_INVALID_ARG;
+    pkv::AppendArgs a{};
+    a.num_reqs = desc->num_reqs;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.head_dim = desc->head_dim;
+    a.num_pages = desc->num_pages;
+    a.max_pages = desc->max_pages_per_req;
+    a.total_q_tokens = desc->total_q_tokens;
+    a.q_lens = desc->q_lens;
+    a.q_offsets = desc->q_offsets;
+    a.context_lens = desc->context_lens;
+    a.block_table = desc->block_table;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.slot_mapping = slot_mapping_out;
+    a.err = dev_err_flag;
+    return pkv::launch_kv_append(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t pkv_attention_workspace_bytes(const pkv_step_desc* desc) {
+    if (check_desc(desc) != PKV_OK) return 0;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return 0;
+    return layout_for(desc, sms).total;
+}
+
+int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const void* k_cache,
+                             const void* v_cache, void* out, float scale, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_err_flag, void* stream) {
+    int rc = check_desc(desc);
+    if (rc != PKV_OK) return rc;
+    if (desc->total_q_tokens == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    const pkv::WorkspaceLayout lay = layout_for(desc, sms);
+    if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_WORKSPACE;
+
+    pkv::StepArgs a{};
+    a.num_reqs = desc->num_reqs;
+    a.num_q_heads = desc->num_q_heads;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.head_dim = desc->head_dim;
+    a.num_pages = desc->num_pages;
+    a.max_pages = desc->max_pages_per_req;
+    a.total_q_tokens = desc->total_q_tokens;
+    a.max_q_len = desc->max_q_len;
+    a.max_context_len = desc->max_context_len;
+    a.dtype = desc->dtype;
+    a.num_sms = sms;
+    a.q_lens = desc->q_lens;
+    a.q_offsets = desc->q_offsets;
+    a.context_lens = desc->context_lens;
+    a.block_table = desc->block_table;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.out = out;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.ws = static_cast<uint8_t*>(workspace);
+    a.lay = lay;
+    a.prefill_min_q = prefill_min_q();
+    a.err = dev_err_flag;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = pkv::launch_plan(a, s)) != PKV_OK) return rc;
+    if ((rc = pkv::launch_decode(a, s)) != PKV_OK) return rc;
+    if (a.prefill_min_q < INT_MAX && (rc = pkv::launch_prefill(a, s)) != PKV_OK) return rc;
+    return PKV_OK;
+}
+
+int pkv_read_device_error(const int32_t* dev_err_flag, int32_t* host_value, void* stream) {
+    if (!dev_err_flag || !host_value) return PKV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host_value, dev_err_flag, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    return *host_value == 0 ? PKV_OK : PKV_ERR_DEVICE;
+}
+
+}  // extern "C"

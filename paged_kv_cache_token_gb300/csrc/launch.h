@@ -1,0 +1,67 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct AppendArgs {
+    int num_reqs, num_kv_heads, head_dim, num_pages, max_pages, total_q_tokens;
+    const int32_t* q_lens;
+    const int32_t* q_offsets;
+    const int32_t* context_lens;
+    const int32_t* block_table;
+    const void* k_new;
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
+    int64_t* slot_mapping;
+    int32_t* err;
+};
+
+// Workspace layout for one attention step, all offsets 256-byte aligned.
+//   ctrl      int32[64]           [0] decode work counter, [1] decode items,
+//                                 [2] split items (those with partials), [3] pages per split
+//                                 [8] prefill tile counter, [9] prefill tiles
+//   req_info  int4[num_reqs]      {first item, splits, q_len, first prefill tile}
+//   items     int4[max_items]     decode items {request, row in request, kv head, split}
+//   tiles     int4[max_tiles]     prefill tiles {request, q tile, q head, 0}
+//   part_ml   float2[max_split_items * G]      (running max in log2 units, sum)
+//   part_o    float[max_split_items * G * D]   un-normalised partial outputs
+struct WorkspaceLayout {
+    size_t ctrl, req_info, items, tiles, part_ml, part_o, total;
+    int max_items, max_tiles, max_split_items, max_splits;
+};
+
+struct StepArgs {
+    int num_reqs, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages;
+    int total_q_tokens, max_q_len, max_context_len, dtype;
+    int num_sms;
+    const int32_t* q_lens;
+    const int32_t* q_offsets;
+    const int32_t* context_lens;
+    const int32_t* block_table;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    void* out;
+    float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+    uint8_t* ws;
+    WorkspaceLayout lay;
+    int prefill_min_q;  // requests with q_len >= this go to the tensor-core prefill path
+    int32_t* err;
+};
+
+WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int total_q_tokens, int max_q_len, int num_sms,
+                                 int prefill_min_q);
+
+int launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+int launch_plan(const StepArgs& a, cudaStream_t stream);
+int launch_decode(const StepArgs& a, cudaStream_t stream);
+int launch_combine(const StepArgs& a, cudaStream_t stream);
+int launch_prefill(const StepArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,14 @@
+// Tensor-core prefill path (q_len > 1 rows): not enabled yet; every row takes the
+// streaming path until this kernel lands.
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+int launch_prefill(const StepArgs& a, cudaStream_t stream) {
+    (void)a;
+    (void)stream;
+    return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

@@ -1,0 +1,137 @@
+"""Device-side driver for a sequence of steps: page pools, per-step metadata upload and
+the two C-ABI calls (append, then attention), all through :mod:`binding`.
+
+This is host plumbing around the library (allocation, copies, stream), the same thing a
+serving engine does around its attention backend.  It holds no attention arithmetic.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding
+from .scheduler import StepPlan
+
+SENTINEL = 0xFFFF  # NaN in both bf16 and fp16: slots never written stay recognisable
+TORCH_DTYPE = {binding.BF16: torch.bfloat16, binding.FP16: torch.float16}
+
+
+def bits_to_tensor(bits: np.ndarray, dtype_code: int, device="cuda", pin=False) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(TORCH_DTYPE[dtype_code])
+    if device == "cpu":
+        return t.pin_memory() if pin else t
+    return t.to(device, non_blocking=False)
+
+
+def tensor_to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@dataclass
+class DeviceStep:
+    """Device copies of one step's metadata plus the matching StepDesc."""
+    plan: StepPlan
+    desc: binding.StepDesc
+    tensors: tuple
+
+
+class PagedKV:
+    """Two page pools [num_pages, Hkv, 16, D] on one device plus an error flag."""
+
+    def __init__(self, num_pages: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 dtype_code: int, device="cuda", fill_sentinel: bool = True):
+        self.num_pages, self.hq, self.hkv, self.d = num_pages, num_q_heads, num_kv_heads, head_dim
+        self.dtype_code = dtype_code
+        self.dtype = TORCH_DTYPE[dtype_code]
+        self.device = torch.device(device)
+        shape = (num_pages, num_kv_heads, 16, head_dim)
+        self.k_cache = torch.empty(shape, dtype=self.dtype, device=self.device)
+        self.v_cache = torch.empty(shape, dtype=self.dtype, device=self.device)
+        if fill_sentinel:
+            self.k_cache.view(torch.int16).fill_(-1)
+            self.v_cache.view(torch.int16).fill_(-1)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._ws = None
+
+    # ------------------------------------------------------------------ metadata
+    def upload(self, plan: StepPlan, stream=None) -> DeviceStep:
+        dev = self.device
+        ql = torch.from_numpy(plan.q_lens).to(dev)
+        qo = torch.from_numpy(plan.q_offsets).to(dev)
+        cl = torch.from_numpy(plan.context_lens).to(dev)
+        bt = torch.from_numpy(np.ascontiguousarray(plan.block_table)).to(dev)
+        desc = binding.make_desc(num_reqs=plan.num_reqs, num_q_heads=self.hq,
+                                 num_kv_heads=self.hkv, head_dim=self.d,
+                                 num_pages=self.num_pages, max_pages_per_req=plan.max_pages,
+                                 total_q_tokens=plan.total_q_tokens, max_q_len=plan.max_q_len,
+                                 max_context_len=plan.max_context_len, dtype=self.dtype_code,
+                                 q_lens=ql, q_offsets=qo, context_lens=cl, block_table=bt)
+        return DeviceStep(plan, desc, (ql, qo, cl, bt))
+
+    def workspace(self, desc) -> torch.Tensor:
+        need = max(256, binding.attention_workspace_bytes(desc))
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    # ------------------------------------------------------------------ calls
+    def append(self, ds: DeviceStep, k_new: torch.Tensor, v_new: torch.Tensor,
+               slot_mapping: Optional[torch.Tensor] = None, stream=None) -> None:
+        binding.kv_append(ds.desc, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
+                          self.err, stream)
+
+    def attention(self, ds: DeviceStep, q: torch.Tensor, scale: float,
+                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty((ds.plan.total_q_tokens, self.hq, self.d), dtype=self.dtype,
+                              device=self.device)
+        ws = self.workspace(ds.desc)
+        binding.paged_attention_step(ds.desc, q, self.k_cache, self.v_cache, out, scale, ws,
+                                     self.err, stream)
+        return out
+
+    def read_error(self) -> int:
+        return binding.read_device_error(self.err)
+
+
+# ---------------------------------------------------------------------- workload glue
+def step_host_inputs(workload, plan: StepPlan):
+    """(q, k_new, v_new) bit arrays for a step, gathered from the workload's sequences."""
+    qs, ks, vs = [], [], []
+    for rid, c, n in zip(plan.rids, plan.context_lens.tolist(), plan.q_lens.tolist()):
+        req = workload.requests[rid]
+        k, v = workload.kv(rid)
+        ks.append(k[c:c + n])
+        vs.append(v[c:c + n])
+        if c >= req.history:
+            qs.append(workload.q(rid)[c - req.history:c - req.history + n])
+        else:  # loading cached history: no queries
+            qs.append(np.zeros((n, workload.num_q_heads, workload.head_dim), np.uint16))
+    cat = lambda xs, h: (np.concatenate(xs) if xs else
+                         np.zeros((0, h, workload.head_dim), np.uint16))
+    return cat(qs, workload.num_q_heads), cat(ks, workload.num_kv_heads), \
+        cat(vs, workload.num_kv_heads)
+
+
+def paged_kv_for(workload, device="cuda", fill_sentinel=True) -> PagedKV:
+    return PagedKV(workload.num_pages, workload.num_q_heads, workload.num_kv_heads,
+                   workload.head_dim, workload.dtype, device, fill_sentinel)
+
+
+def load_history(kv: PagedKV, workload, plan: Optional[StepPlan]) -> None:
+    """Append every request's cached history (no attention)."""
+    if plan is None:
+        return
+    _, k, v = step_host_inputs(workload, plan)
+    ds = kv.upload(plan)
+    kv.append(ds, bits_to_tensor(k, workload.dtype), bits_to_tensor(v, workload.dtype))
+
+
+def run_step(kv: PagedKV, workload, plan: StepPlan) -> torch.Tensor:
+    q, k, v = step_host_inputs(workload, plan)
+    ds = kv.upload(plan)
+    kv.append(ds, bits_to_tensor(k, workload.dtype), bits_to_tensor(v, workload.dtype))
+    return kv.attention(ds, bits_to_tensor(q, workload.dtype), workload.scale)

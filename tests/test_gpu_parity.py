@@ -1,0 +1,235 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded
+inputs.  kv_append, page contents and slot ids must be bit-exact; attention outputs must be
+within max-abs 2e-2 and mean-abs 2e-3 of the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_token_gb300 import binding, build, runner
+from paged_kv_cache_token_gb300 import workloads as W
+from paged_kv_cache_token_gb300.scheduler import PagePool, Scheduler, make_plan, scheduler_for
+
+from gpu_common import assert_close, gpu_as_f64, oracle_rows, pool_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.load()
+
+
+def custom(index, hq, hkv, d, dtype, specs, budget=1 << 30, chunk_cap=None, extra_pages=8,
+           interleave=False):
+    reqs = [W.RequestSpec(i, *s) for i, s in enumerate(specs)]
+    need = sum(-(-r.total // 16) for r in reqs) + extra_pages
+    g = torch.Generator().manual_seed(9000 + index)
+    order = torch.randperm(need, generator=g).numpy().astype(np.int32)
+    return W.Workload(index, "custom", hq, hkv, d, dtype, reqs, order, need, budget=budget,
+                      chunk_cap=chunk_cap, interleave_history=interleave)
+
+
+def run_all(w, check_rows=None, every_step=True):
+    """Run a workload's history load and every step; compare each step with the oracle."""
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    worst = (0.0, 0.0)
+    outs = []
+    for i, plan in enumerate(s.all_steps()):
+        out = runner.run_step(kv, w, plan)
+        if every_step or i == 0:
+            rows = None if check_rows is None else check_rows(plan)
+            ref = oracle_rows(w, plan, rows)
+            got = gpu_as_f64(out) if rows is None else gpu_as_f64(out[torch.as_tensor(rows)])
+            assert kv.read_error() == 0
+            mx, mean = assert_close(got, ref, "%s step %d" % (w.name, i))
+            worst = (max(worst[0], mx), max(worst[1], mean))
+        outs.append(out)
+    assert kv.read_error() == 0
+    return worst, outs, kv
+
+
+# ------------------------------------------------------------------------------ kv_append
+def test_append_tiny_bit_exact():
+    w = W.tiny()
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    shape = (w.num_pages, w.num_kv_heads, 16, w.head_dim)
+    ref_k = np.full(shape, 0xFFFF, np.uint16)
+    ref_v = ref_k.copy()
+    for plan in s.all_steps():
+        _, k, v = runner.step_host_inputs(w, plan)
+        ds = kv.upload(plan)
+        slots = torch.full((plan.total_q_tokens,), -7, dtype=torch.int64, device="cuda")
+        kv.append(ds, runner.bits_to_tensor(k, w.dtype), runner.bits_to_tensor(v, w.dtype), slots)
+        ref_k, ref_v, ref_slots = oracle.kv_append(plan.q_lens, plan.context_lens,
+                                                   plan.block_table, w.num_pages, k, v, ref_k,
+                                                   ref_v)
+        gk, gv = pool_bits(kv)
+        assert np.array_equal(gk, ref_k) and np.array_equal(gv, ref_v)
+        assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    assert kv.read_error() == 0
+
+
+@pytest.mark.parametrize("d,hkv,dtype", [(64, 2, 0), (128, 8, 0), (128, 3, 1), (64, 1, 1)])
+def test_append_page_boundaries_bit_exact(d, hkv, dtype):
+    rng = np.random.default_rng(d + hkv)
+    ctx = [0, 15, 16, 31, 32, 1023, 1024, 5, 0]
+    ql = [1, 1, 16, 17, 33, 1, 16, 0, 64]
+    need = [-(-(c + q) // 16) for c, q in zip(ctx, ql)]
+    npages = sum(need) + 5
+    order = rng.permutation(npages).astype(np.int32)
+    tables, used = [], 0
+    for n in need:
+        tables.append(order[used:used + n].tolist())
+        used += n
+    plan = make_plan(list(range(len(ctx))), ql, ctx, tables)
+    T = plan.total_q_tokens
+    k = rng.integers(0, 0xFFFF, size=(T, hkv, d), dtype=np.uint16)
+    v = rng.integers(0, 0xFFFF, size=(T, hkv, d), dtype=np.uint16)
+    kv = runner.PagedKV(npages, hkv, hkv, d, dtype)
+    ds = kv.upload(plan)
+    slots = torch.empty((T,), dtype=torch.int64, device="cuda")
+    kv.append(ds, runner.bits_to_tensor(k, dtype), runner.bits_to_tensor(v, dtype), slots)
+    sent = np.full((npages, hkv, 16, d), 0xFFFF, np.uint16)
+    rk, rv, rs = oracle.kv_append(plan.q_lens, plan.context_lens, plan.block_table, npages, k, v,
+                                  sent, sent)
+    gk, gv = pool_bits(kv)
+    assert np.array_equal(gk, rk) and np.array_equal(gv, rv)
+    assert np.array_equal(slots.cpu().numpy(), rs)
+    assert kv.read_error() == 0
+
+
+def test_append_bad_page_sets_flag_and_skips():
+    plan = make_plan([0, 1], [3, 2], [0, 0], [[0], [7]])   # page 7 outside a 4-page pool
+    kv = runner.PagedKV(4, 1, 1, 64, 0)
+    ds = kv.upload(plan)
+    k = torch.zeros((5, 1, 64), dtype=torch.bfloat16, device="cuda")
+    kv.append(ds, k, k)
+    assert kv.read_error() & binding.DEVERR_PAGE_RANGE
+    gk, _ = pool_bits(kv)
+    assert np.all(gk[0, 0, :3] == 0) and np.all(gk[0, 0, 3:] == 0xFFFF)
+    assert np.all(gk[1:] == 0xFFFF)
+
+
+# ------------------------------------------------------------------------------ attention
+def test_tiny_all_steps():
+    run_all(W.tiny())
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(4, 2, 64, 0), (32, 8, 128, 0), (8, 8, 128, 1),
+                                            (16, 2, 128, 1), (8, 1, 64, 0), (6, 3, 64, 1)])
+def test_decode_batches(hq, hkv, d, dtype):
+    ctx = [0, 1, 15, 16, 17, 100, 255, 256, 1000, 3000]  # one key, page edges, multi-split
+    w = custom(100 + hq + d, hq, hkv, d, dtype, [(c, 0, 2) for c in ctx])
+    run_all(w)
+
+
+def test_decode_literal_skeleton_scale_one():
+    # hotelren.com/news/6181127 §5.1 writes softmax(q @ K_all.T) with no scale: scale = 1.0
+    w = custom(200, 4, 2, 64, 0, [(40, 0, 1), (3, 0, 1)])
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    q, k, v = runner.step_host_inputs(w, plan)
+    ds = kv.upload(plan)
+    kv.append(ds, runner.bits_to_tensor(k, 0), runner.bits_to_tensor(v, 0))
+    out = kv.attention(ds, runner.bits_to_tensor(q, 0), 1.0)
+    w.scale_override = 1.0
+    ref = np.concatenate([oracle.attention_rows(0, w.q(r)[:1], np.array([c], np.int32),
+                                                w.kv(r)[0][:c + 1], w.kv(r)[1][:c + 1], 1.0)
+                          for r, c in zip(plan.rids, plan.context_lens.tolist())])
+    assert_close(gpu_as_f64(out), ref, "scale 1")
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(4, 2, 64, 0), (32, 8, 128, 0), (8, 8, 128, 1)])
+def test_prefill_chunks_small(hq, hkv, d, dtype):
+    # prompts around the 128-row tile and 16-token page edges, chunked by a small budget
+    specs = [(0, 1, 1), (0, 2, 0), (0, 127, 1), (0, 128, 0), (0, 129, 2), (0, 300, 1),
+             (20, 33, 0)]
+    run_all(custom(300 + hq + d, hq, hkv, d, dtype, specs, budget=160, chunk_cap=96))
+
+
+def test_block_table_permutation_bitwise_identical():
+    base = custom(400, 32, 8, 128, 0, [(c, 0, 1) for c in (50, 700, 2100, 16)])
+    outs = []
+    for seed in (1, 2):
+        w = custom(400, 32, 8, 128, 0, [(c, 0, 1) for c in (50, 700, 2100, 16)])
+        g = torch.Generator().manual_seed(seed)
+        w.page_order = torch.randperm(base.num_pages, generator=g).numpy().astype(np.int32)
+        _, o, _ = run_all(w, every_step=False)
+        outs.append(runner.tensor_to_bits(o[0]))
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_attention_bad_page_sets_flag():
+    w = custom(500, 4, 2, 64, 0, [(20, 0, 1)])
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    plan.block_table[0, 0] = w.num_pages + 3
+    q, k, v = runner.step_host_inputs(w, plan)
+    ds = kv.upload(plan)
+    kv.attention(ds, runner.bits_to_tensor(q, 0), w.scale)
+    assert kv.read_error() & binding.DEVERR_PAGE_RANGE
+
+
+# ------------------------------------------------------------------------------ full configs
+def test_config_decode_only_full():
+    """64 requests, ctx U[512, 4096], 32/8 heads, d=128, bf16, 70k-page permuted pool:
+    every output row against the oracle."""
+    worst, _, _ = run_all(W.decode_only())
+    print("decode-only worst max/mean abs", worst)
+
+
+def test_config_mha_skew_all_64_steps():
+    worst, _, _ = run_all(W.mha_skew())
+    print("mha-skew worst max/mean abs", worst)
+
+
+def _sample_rows(plan, n=24, seed=0):
+    T = plan.total_q_tokens
+    rng = np.random.default_rng(seed + T)
+    pick = set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    pick |= {0, T - 1}
+    # every request's first and last row (decodes, chunk edges)
+    for j in range(plan.num_reqs):
+        if plan.q_lens[j]:
+            pick |= {int(plan.q_offsets[j]), int(plan.q_offsets[j + 1]) - 1}
+    return sorted(pick)
+
+
+def test_config_prefill_one_shot_and_chunked():
+    one = W.prefill()
+    w1, o1, _ = run_all(one, check_rows=lambda p: _sample_rows(p, 48))
+    ch = W.prefill(chunk=2048)
+    w2, o2, _ = run_all(ch, check_rows=lambda p: _sample_rows(p, 24))
+    chunked = torch.cat(o2)
+    diff = (chunked.float() - o1[0].float()).abs().max().item()
+    print("prefill one-shot", w1, "chunked", w2, "gpu chunked-vs-one-shot max diff", diff)
+    assert diff <= 2 * 2e-2
+
+
+def test_config_mixed_chunked_matches_oracle_and_one_shot():
+    w = W.mixed()
+    worst, outs, _ = run_all(w, check_rows=lambda p: _sample_rows(p, 16))
+    print("mixed worst", worst)
+    # the prompt's chunked rows against a one-shot run of the same prompt
+    prompt = w.requests[-1]
+    npages = (prompt.prompt + 15) // 16 + 8
+    order = torch.randperm(npages, generator=torch.Generator().manual_seed(11)).numpy()
+    one = W.Workload(w.index, "one-shot", 32, 8, 128, 0, [W.RequestSpec(0, 0, prompt.prompt, 0)],
+                     order.astype(np.int32), npages, budget=prompt.prompt)
+    one._cache[("kv", 0)] = w.kv(prompt.rid)
+    one._cache[("q", 0)] = w.q(prompt.rid)
+    _, o1, _ = run_all(one, check_rows=lambda p: _sample_rows(p, 16))
+    chunked = torch.cat([o[-int(len_):] for o, len_ in
+                         zip(outs, [2018] * 14 + [1748])])
+    diff = (chunked.float() - o1[0].float()).abs().max().item()
+    print("mixed: gpu chunked-vs-one-shot max diff", diff)
+    assert diff <= 2 * 2e-2
