@@ -1,0 +1,447 @@
+"""Benchmark of the paged-KV attention step on GB300.
+
+Default workload (the headline metric): decode-only step with Llama-3-8B attention shapes --
+64 requests, cached contexts uniform in [512, 4096], 32 query / 8 KV heads, head dim 128,
+bf16, 16-token pages scattered over a 70,000-page pool.  One step = kv_append of the 64 new
+tokens + paged_attention_step (plan, decode stream, split combine).  The metric is KV GB/s:
+algorithmic bytes of the step (K/V read by attention, Q read, output write, append read +
+write, block-table reads) divided by the step time.  The secondary object "prefill_chunk"
+times the tensor-core-bound workload: one-shot causal prefill of 8,192 tokens (32/8 heads,
+d=128) and the same prompt as 4 x 2,048-token chunks, in TFLOP/s of causal attention FLOPs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 the script runs under torch.distributed.run, one rank per GPU; every rank runs
+its own copy of the workload (requests are independent, no collective on the data path),
+timing is max over ranks and ``value`` counts the bytes of all ranks (weak scaling).
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_token_gb300 import workloads as W  # noqa: E402
+from paged_kv_cache_token_gb300.scheduler import scheduler_for  # noqa: E402
+
+METRIC = "paged-attn decode KV GB/s and prefill-chunk TFLOPS, % of GB300 peak"
+L2_BYTES = 129 * 2 ** 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------------------ accounting
+def step_bytes(w, plan):
+    """Algorithmic bytes of one step: every byte the definition has to touch once."""
+    esz = 2
+    hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+    T = plan.total_q_tokens
+    kv_tokens = int((plan.context_lens.astype(np.int64) + plan.q_lens).sum())
+    attn_kv = kv_tokens * hkv * d * esz * 2           # K and V read once per KV head
+    q_out = T * hq * d * esz * 2                       # Q read, output written
+    append = T * hkv * d * esz * 2 * 2                 # K_new, V_new read and written
+    pages = int(((plan.context_lens + plan.q_lens + 15) // 16).sum())
+    meta = pages * 4 + plan.num_reqs * 12
+    return dict(attention=attn_kv + q_out + meta, append=append,
+                step=attn_kv + q_out + meta + append, kv=attn_kv)
+
+
+def causal_flops(w, plan):
+    """4 * D * Hq * (number of (query, key) pairs with key <= query)."""
+    pairs = 0
+    for c, n in zip(plan.context_lens.tolist(), plan.q_lens.tolist()):
+        pairs += n * c + n * (n + 1) // 2
+    return 4 * w.head_dim * w.num_q_heads * pairs
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+        else:
+            self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unavailable"]}
+        # samples under load: the upper half of the run is the timed kernels
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ our arm
+def lib_event():
+    """A timing event whose CUDA handle exists (torch creates it on first record), so the
+    library can record it on its own stream."""
+    e = torch.cuda.Event(enable_timing=True)
+    e.record()
+    return e
+
+
+def build_decode_state(device, pool_pages=70000):
+    from paged_kv_cache_token_gb300 import runner
+    w = W.decode_only(num_pages=pool_pages)
+    s = scheduler_for(w)
+    hist = s.history_plan()
+    plan = s.next_step()
+    kv = runner.paged_kv_for(w, device=device, fill_sentinel=False)
+    runner.load_history(kv, w, hist)
+    q, k, v = runner.step_host_inputs(w, plan)
+    return w, plan, kv, (q, k, v)
+
+
+def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
+    from paged_kv_cache_token_gb300 import binding, runner
+    w, plan, kv, (qh, kh, vh) = build_decode_state(device, pool_pages)
+    dt = w.dtype
+    q = runner.bits_to_tensor(qh, dt, device)
+    k_new = runner.bits_to_tensor(kh, dt, device)
+    v_new = runner.bits_to_tensor(vh, dt, device)
+    ds = kv.upload(plan)
+    out = torch.empty((plan.total_q_tokens, w.num_q_heads, w.head_dim), dtype=kv.dtype,
+                      device=device)
+    ws = kv.workspace(ds.desc)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        binding.kv_append(ds.desc, k_new, v_new, kv.k_cache, kv.v_cache, None, kv.err, stream)
+        binding.paged_attention_step(ds.desc, q, kv.k_cache, kv.v_cache, out, w.scale, ws,
+                                     kv.err, stream)
+
+    for _ in range(max(3, warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    assert kv.read_error() == 0
+
+    kstart = [lib_event() for _ in range(steps)]
+    kstop = [lib_event() for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    with clocks:
+        # repeat the timed region so the clock sampler sees >= ~1 s of load
+        reps = 0
+        wall0 = time.time()
+        while True:
+            t0.record(stream)
+            for i in range(steps):
+                binding.set_kernel_events(0, kstart[i], kstop[i])
+                one_step()
+            binding.set_kernel_events(0, None, None)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            reps += 1
+            if time.time() - wall0 > 1.0 or reps >= 50:
+                break
+    dist_ctx.barrier()
+    ms_total = t0.elapsed_time(t1)          # last repetition: exactly `steps` steps
+    ms_kernel = float(np.mean([a.elapsed_time(b) for a, b in zip(kstart, kstop)]))
+    ms_step = dist_ctx.max(ms_total / steps)
+    assert kv.read_error() == 0
+    acct = step_bytes(w, plan)
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    pin = lambda a: runner.bits_to_tensor(a, dt, "cpu", pin=True)
+    hq_, hk_, hv_ = pin(qh), pin(kh), pin(vh)
+    meta_h = [torch.from_numpy(x).pin_memory() for x in
+              (plan.q_lens, plan.q_offsets, plan.context_lens, plan.block_table)]
+    meta_d = list(ds.tensors)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in [hq_, hk_, hv_] + meta_h)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        q.copy_(hq_, non_blocking=True)
+        k_new.copy_(hk_, non_blocking=True)
+        v_new.copy_(hv_, non_blocking=True)
+        for hsrc, ddst in zip(meta_h, meta_d):
+            ddst.copy_(hsrc, non_blocking=True)
+        one_step()
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    ms_e2e = dist_ctx.max(e0.elapsed_time(e1) / steps)
+    return dict(w=w, plan=plan, acct=acct, ms_step=ms_step, ms_kernel=ms_kernel, ms_e2e=ms_e2e,
+                h2d=h2d, d2h=d2h, clocks=clocks.summary(), launches=4 * steps)
+
+
+def time_prefill(device, reps=3):
+    """Attention-kernel time of the 8K one-shot prefill and of the 4 x 2048 chunks."""
+    from paged_kv_cache_token_gb300 import binding, runner
+    res = {}
+    for label, chunk in (("one_shot_8192", None), ("chunks_4x2048", 2048)):
+        w = W.prefill(chunk=chunk)
+        s = scheduler_for(w)
+        kv = runner.paged_kv_for(w, device=device, fill_sentinel=False)
+        plans = s.all_steps()
+        flops = sum(causal_flops(w, p) for p in plans)
+        total_ms = 0.0
+        main_ms = 0.0
+        for p in plans:
+            qh, kh, vh = runner.step_host_inputs(w, p)
+            ds = kv.upload(p)
+            q = runner.bits_to_tensor(qh, w.dtype, device)
+            kv.append(ds, runner.bits_to_tensor(kh, w.dtype, device),
+                      runner.bits_to_tensor(vh, w.dtype, device))
+            out = torch.empty((p.total_q_tokens, w.num_q_heads, w.head_dim), dtype=kv.dtype,
+                              device=device)
+            kv.attention(ds, q, w.scale, out)          # warm-up
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ka, kb = lib_event(), lib_event()
+            t = []
+            tk = []
+            for _ in range(reps):
+                binding.set_kernel_events(0, ka, kb)
+                binding.set_kernel_events(1, ka, kb)
+                a.record()
+                kv.attention(ds, q, w.scale, out)
+                b.record()
+                torch.cuda.synchronize()
+                binding.set_kernel_events(0, None, None)
+                binding.set_kernel_events(1, None, None)
+                t.append(a.elapsed_time(b))
+                tk.append(ka.elapsed_time(kb))
+            total_ms += float(np.median(t))
+            main_ms += float(np.median(tk))
+        assert kv.read_error() == 0
+        res[label] = dict(ms=total_ms, tflops=flops / total_ms / 1e9, flops=flops,
+                          main_kernel_ms=main_ms)
+        del kv
+        torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------------ oracle arm
+def oracle_decode_sample(n_req, min_seconds=0.0):
+    """Time the fp64 oracle on the first n_req decode rows of the decode workload (all 32
+    heads each), repeating the pass until at least ``min_seconds`` of CPU work."""
+    import oracle
+    w = W.decode_only()
+    s = scheduler_for(w)
+    s.history_plan()
+    plan = s.next_step()
+    sel = list(range(n_req))
+    data = [(w.q(r)[:1], w.kv(r)) for r in sel]
+    kv_tokens = int(sum(int(plan.context_lens[j]) + 1 for j in sel))
+    nbytes = kv_tokens * w.num_kv_heads * w.head_dim * 2 * 2 + n_req * w.num_q_heads * \
+        w.head_dim * 2 * 2
+    passes, t0 = 0, time.time()
+    while True:
+        for j, r in enumerate(sel):
+            c = int(plan.context_lens[j])
+            k, v = data[j][1]
+            oracle.attention_rows(w.dtype, data[j][0], np.array([c], np.int32), k[:c + 1],
+                                  v[:c + 1], w.scale)
+        passes += 1
+        if time.time() - t0 >= min_seconds:
+            break
+    secs = time.time() - t0
+    return secs, nbytes * passes, oracle.num_threads(), passes
+
+
+# ------------------------------------------------------------------------------ dist glue
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x):
+        if not self.pg:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def run_reference(args, dist_ctx):
+    if dist_ctx.rank != 0:
+        return
+    n_req = 16  # a quarter of the 64 decode rows per step
+    for _ in range(args.warmup):
+        oracle_decode_sample(2)
+    total_s, total_b, cores = 0.0, 0, 1
+    for _ in range(args.steps):
+        s, b, cores, _ = oracle_decode_sample(n_req)
+        total_s += s
+        total_b += b
+    value = total_b / total_s / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "decode-only, 32q/8kv heads, d=128, bf16 inputs, ctx "
+                                   "U[512,4096], 64 requests (oracle sample: 16 rows/step)",
+                       "parallelism": "host cores (OpenMP)"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "first 16 of 64 decode rows per step, all 32 heads"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-pages", type=int, default=70000,
+                    help="page-pool size (the step touches the same bytes at any size; a "
+                         "smaller pool keeps profiler captures small)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    dist_ctx = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist_ctx)
+            return
+        from paged_kv_cache_token_gb300 import binding, build
+        build.build()
+        binding.load()
+        device = torch.device("cuda", dist_ctx.local if dist_ctx.world > 1 else 0)
+        torch.cuda.set_device(device)
+        hbm, bf16, bf16_sus, peak_src = peaks()
+        r = time_decode(device, args.steps, args.warmup, dist_ctx, args.pool_pages)
+        acct = r["acct"]
+        value = acct["step"] * dist_ctx.world / (r["ms_step"] * 1e-3) / 1e9
+        kernel_bytes = acct["attention"]
+        achieved = kernel_bytes / (r["ms_kernel"] * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist_ctx.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "decode-only step: 64 requests, cached ctx U[512,4096], 32 q /"
+                                   " 8 kv heads, d_head 128, bf16, 16-token pages over a "
+                                   "%d-page permuted pool (kv_append + paged_attention_step)"
+                                   % args.pool_pages,
+                       "kv_bytes_per_step": acct["kv"], "step_bytes": acct["step"],
+                       "l2": "inputs larger than L2: %.0f MB K/V read per step vs 129 MB L2"
+                             % (acct["kv"] / 1e6),
+                       "parallelism": "independent replica per GPU" if dist_ctx.world > 1
+                       else "1 GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_source": peak_src + " hbm_gbs",
+                         "kernel": "decode_kernel", "bytes_per_launch": kernel_bytes,
+                         "ms_per_launch": r["ms_kernel"], "traffic": None},
+            "e2e": {"value": acct["step"] * dist_ctx.world / (r["ms_e2e"] * 1e-3) / 1e9,
+                    "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["ms_e2e"]},
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+        }
+        if not args.no_prefill and dist_ctx.rank == 0:
+            pf = time_prefill(device)
+            one = pf["one_shot_8192"]
+            line["prefill_chunk"] = {
+                "workload": "causal prefill S=8192, 32 q / 8 kv heads, d 128, bf16, pages; "
+                            "one shot and 4 x 2048 chunks",
+                "one_shot_tflops": one["tflops"], "chunked_tflops": pf["chunks_4x2048"]["tflops"],
+                "one_shot_ms": one["ms"], "chunked_ms": pf["chunks_4x2048"]["ms"],
+                "flops": one["flops"], "peak_tflops": bf16, "frac": one["tflops"] / bf16,
+                "peak_source": peak_src + " bf16_tflops (burst)"}
+        if not args.no_cpu_baseline and dist_ctx.rank == 0:
+            secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
+            line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": "fp64 oracle on the whole decode step (64 rows x 32 "
+                                              "heads), repeated %d times: %.1f s" % (passes, secs)}
+        if dist_ctx.rank == 0:
+            print(json.dumps(line))
+    finally:
+        dist_ctx.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -153,6 +153,16 @@ PKV_API int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, c
  */
 PKV_API int pkv_read_device_error(const int32_t* dev_err_flag, int32_t* host_value, void* stream);
 
+/*
+ * pkv_set_kernel_events -- optional timing hook for benchmarks.  While set, each
+ * pkv_paged_attention_step call on this host thread records `start` on its stream just
+ * before the main kernel of the chosen path and `stop` just after it (which = 0: the
+ * decode-stream kernel, which = 1: the tensor-core prefill kernel); a path that does not
+ * launch in a call records nothing.  Events are cudaEvent_t passed as void*; NULL clears.
+ * Returns PKV_OK, or PKV_ERR_INVALID_ARG for an unknown `which`.
+ */
+PKV_API int pkv_set_kernel_events(int which, void* start, void* stop);
+
 /* Human-readable name of a pkv_status value (static storage). */
 PKV_API const char* pkv_status_string(int status);
 

@@ -26,7 +26,8 @@ BF16, FP16 = 0, 1
 DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16}
 
 EXPORTED = ("pkv_kv_append", "pkv_attention_workspace_bytes", "pkv_paged_attention_step",
-            "pkv_read_device_error", "pkv_status_string", "pkv_version")
+            "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
+            "pkv_version")
 
 
 class PkvError(RuntimeError):
@@ -74,6 +75,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_read_device_error.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_set_kernel_events.argtypes = [ctypes.c_int, V, V]
+    lib.pkv_set_kernel_events.restype = ctypes.c_int
     lib.pkv_version.argtypes = []
     lib.pkv_version.restype = ctypes.c_int
     if path is None:
@@ -141,6 +144,16 @@ def paged_attention_step(desc: StepDesc, q, k_cache, v_cache, out, scale: float,
     if check and rc != OK:
         raise PkvError("pkv_paged_attention_step", rc)
     return rc
+
+
+def set_kernel_events(which: int, start=None, stop=None) -> None:
+    """Record torch.cuda.Event ``start``/``stop`` around the main kernel of path ``which``
+    (0 decode stream, 1 tensor-core prefill) in later attention calls; None clears."""
+    s = ctypes.c_void_p(start.cuda_event) if start is not None else None
+    e = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
+    rc = load().pkv_set_kernel_events(which, s, e)
+    if rc != OK:
+        raise PkvError("pkv_set_kernel_events", rc)
 
 
 def read_device_error(err: torch.Tensor, stream=None) -> int:

@@ -61,6 +61,8 @@ int check_desc(const pkv_step_desc* d) {
 // INT_MAX keeps every row on the streaming path.
 int prefill_min_q() { return INT_MAX; }
 
+thread_local cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
+
 pkv::WorkspaceLayout layout_for(const pkv_step_desc* d, int num_sms) {
     return pkv::workspace_layout(d->num_reqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
                                  d->total_q_tokens, d->max_q_len, num_sms, prefill_min_q());
@@ -165,8 +167,17 @@ int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const voi
     a.err = dev_err_flag;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((rc = pkv::launch_plan(a, s)) != PKV_OK) return rc;
-    if ((rc = pkv::launch_decode(a, s)) != PKV_OK) return rc;
-    if (a.prefill_min_q < INT_MAX && (rc = pkv::launch_prefill(a, s)) != PKV_OK) return rc;
+    if ((rc = pkv::launch_decode(a, s, g_events[0][0], g_events[0][1])) != PKV_OK) return rc;
+    if (a.prefill_min_q < INT_MAX &&
+        (rc = pkv::launch_prefill(a, s, g_events[1][0], g_events[1][1])) != PKV_OK)
+        return rc;
+    return PKV_OK;
+}
+
+int pkv_set_kernel_events(int which, void* start, void* stop) {
+    if (which != 0 && which != 1) return PKV_ERR_INVALID_ARG;
+    g_events[which][0] = static_cast<cudaEvent_t>(start);
+    g_events[which][1] = static_cast<cudaEvent_t>(stop);
     return PKV_OK;
 }
 

@@ -638,7 +638,8 @@ int launch_plan(const StepArgs& a, cudaStream_t stream) {
 }
 
 template <typename T, int D, int G>
-static int launch_decode_t(const StepArgs& a, cudaStream_t stream) {
+static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev0,
+                           cudaEvent_t ev1) {
     using S = DecodeSmem<T, D, G>;
     static int blocks_per_sm = 0;  // benign race: every thread computes the same value
     if (blocks_per_sm == 0) {
@@ -653,29 +654,31 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream) {
         blocks_per_sm = std::max(1, n);
     }
     const int grid = blocks_per_sm * a.num_sms;
+    if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return PKV_ERR_CUDA;
     decode_kernel<T, D, G><<<grid, kDecThreads, S::kBytes, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return PKV_ERR_CUDA;
     combine_kernel<T, D, G><<<std::max(1, a.num_reqs * a.num_kv_heads), 128, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 template <typename T, int D>
-static int dispatch_group(const StepArgs& a, cudaStream_t s) {
+static int dispatch_group(const StepArgs& a, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
     switch (a.num_q_heads / a.num_kv_heads) {
-        case 1: return launch_decode_t<T, D, 1>(a, s);
-        case 2: return launch_decode_t<T, D, 2>(a, s);
-        case 4: return launch_decode_t<T, D, 4>(a, s);
-        case 8: return launch_decode_t<T, D, 8>(a, s);
+        case 1: return launch_decode_t<T, D, 1>(a, s, e0, e1);
+        case 2: return launch_decode_t<T, D, 2>(a, s, e0, e1);
+        case 4: return launch_decode_t<T, D, 4>(a, s, e0, e1);
+        case 8: return launch_decode_t<T, D, 8>(a, s, e0, e1);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }
 
-int launch_decode(const StepArgs& a, cudaStream_t stream) {
+int launch_decode(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
     if (a.dtype == PKV_BF16)
-        return a.head_dim == 128 ? dispatch_group<__nv_bfloat16, 128>(a, stream)
-                                 : dispatch_group<__nv_bfloat16, 64>(a, stream);
-    return a.head_dim == 128 ? dispatch_group<__half, 128>(a, stream)
-                             : dispatch_group<__half, 64>(a, stream);
+        return a.head_dim == 128 ? dispatch_group<__nv_bfloat16, 128>(a, stream, e0, e1)
+                                 : dispatch_group<__nv_bfloat16, 64>(a, stream, e0, e1);
+    return a.head_dim == 128 ? dispatch_group<__half, 128>(a, stream, e0, e1)
+                             : dispatch_group<__half, 64>(a, stream, e0, e1);
 }
 
 }  // namespace pkv

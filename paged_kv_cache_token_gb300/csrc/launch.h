@@ -60,8 +60,10 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
 
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 int launch_plan(const StepArgs& a, cudaStream_t stream);
-int launch_decode(const StepArgs& a, cudaStream_t stream);
-int launch_combine(const StepArgs& a, cudaStream_t stream);
-int launch_prefill(const StepArgs& a, cudaStream_t stream);
+// ev_start / ev_stop (may be null) are recorded around the main kernel only.
+int launch_decode(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
+                  cudaEvent_t ev_stop);
+int launch_prefill(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
+                   cudaEvent_t ev_stop);
 
 }  // namespace pkv

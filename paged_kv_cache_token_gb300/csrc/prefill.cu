@@ -5,9 +5,11 @@
 
 namespace pkv {
 
-int launch_prefill(const StepArgs& a, cudaStream_t stream) {
+int launch_prefill(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
     (void)a;
     (void)stream;
+    (void)e0;
+    (void)e1;
     return PKV_ERR_UNSUPPORTED;
 }
 
