@@ -147,6 +147,33 @@ PKV_API int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, c
                              size_t workspace_bytes, int32_t* dev_err_flag, void* stream);
 
 /*
+ * pkv_paged_attention_step_static_ws -- the same attention step as
+ * pkv_paged_attention_step, for callers that cannot allocate device memory when they call
+ * it.  Examples are code that runs from a plugin or callback that must not synchronise the
+ * device (cudaMalloc and cudaFree can synchronise it), and runtimes that hand out all
+ * device memory once at start-up and allow no allocation afterwards.  This entry point
+ * allocates nothing: its scratch (the work list and split-KV partial results) lives in a
+ * fixed array compiled into the library, PKV_STATIC_WORKSPACE_BYTES (16 MiB) on every GPU
+ * that loads the library, held until the process exits.  The pages have no counterpart to
+ * this call; it only changes where the scratch memory comes from.
+ *   Arguments and results are those of pkv_paged_attention_step without the workspace.
+ *   A step whose pkv_attention_workspace_bytes exceeds PKV_STATIC_WORKSPACE_BYTES is
+ *   rejected with PKV_ERR_WORKSPACE before anything is launched.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any
+ *   stream capture.  Later calls on the device reuse the address.
+ *   Every call on a device shares the one array, which keeps the previous call's
+ *   contents (the step initialises what it needs, nothing has to start at zero).  Calls
+ *   that overlap on the GPU -- on different streams, or from several host threads without
+ *   ordering -- race on the array: issue them in order on one stream.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
+PKV_API int pkv_paged_attention_step_static_ws(const pkv_step_desc* desc, const void* q,
+                                               const void* k_cache, const void* v_cache,
+                                               void* out, float scale, int32_t* dev_err_flag,
+                                               void* stream);
+
+/*
  * pkv_read_device_error -- synchronise `stream`, copy *dev_err_flag (device) to
  * *host_value and return PKV_OK when it is zero, PKV_ERR_DEVICE when not, PKV_ERR_CUDA
  * when the copy fails.  The only synchronising entry point.

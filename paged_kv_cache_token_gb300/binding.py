@@ -146,6 +146,25 @@ def paged_attention_step(desc: StepDesc, q, k_cache, v_cache, out, scale: float,
     return rc
 
 
+STATIC_WORKSPACE_BYTES = 16 << 20
+
+
+def paged_attention_step_static_ws(desc: StepDesc, q, k_cache, v_cache, out, scale: float,
+                                   err=None, stream=None, check: bool = True) -> int:
+    """The attention step with the library's built-in scratch array instead of a caller
+    workspace (for callers that cannot allocate device memory at call time)."""
+    lib = load()
+    fn = lib.pkv_paged_attention_step_static_ws
+    fn.argtypes = [ctypes.POINTER(StepDesc), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    rc = fn(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), float(scale),
+            _ptr(err), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_paged_attention_step_static_ws", rc)
+    return rc
+
+
 def set_kernel_events(which: int, start=None, stop=None) -> None:
     """Record torch.cuda.Event ``start``/``stop`` around the main kernel of path ``which``
     (0 decode stream, 1 tensor-core prefill) in later attention calls; None clears."""
