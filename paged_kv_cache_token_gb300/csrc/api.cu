@@ -57,9 +57,9 @@ int check_desc(const pkv_step_desc* d) {
     return PKV_OK;
 }
 
-// Requests with at least this many new tokens take the tensor-core prefill path.
-// INT_MAX keeps every row on the streaming path.
-int prefill_min_q() { return INT_MAX; }
+// Requests with at least this many new tokens take the tensor-core prefill path (128-row
+// query tiles); shorter multi-token requests run row by row on the streaming path.
+int prefill_min_q() { return 16; }
 
 thread_local cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
 
