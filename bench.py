@@ -376,6 +376,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill"], default=None,
+                    help="time only the prefill workload (one-shot 8K and 4 x 2K) and print "
+                         "its JSON object; used for focused profiler captures")
     ap.add_argument("--pool-pages", type=int, default=70000,
                     help="page-pool size (the step touches the same bytes at any size; a "
                          "smaller pool keeps profiler captures small)")
@@ -392,6 +395,11 @@ def main():
         device = torch.device("cuda", dist_ctx.local if dist_ctx.world > 1 else 0)
         torch.cuda.set_device(device)
         hbm, bf16, bf16_sus, peak_src = peaks()
+        if args.only == "prefill":
+            if dist_ctx.rank == 0:
+                pf = time_prefill(device)
+                print(json.dumps({"prefill_chunk": pf, "peak_tflops": bf16}))
+            return
         r = time_decode(device, args.steps, args.warmup, dist_ctx, args.pool_pages)
         acct = r["acct"]
         value = acct["step"] * dist_ctx.world / (r["ms_step"] * 1e-3) / 1e9

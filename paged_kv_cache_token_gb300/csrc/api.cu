@@ -164,11 +164,12 @@ int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const voi
     a.ws = static_cast<uint8_t*>(workspace);
     a.lay = lay;
     a.prefill_min_q = prefill_min_q();
+    a.heads_per_tile = pkv::prefill_heads_per_tile(desc->num_q_heads, desc->num_kv_heads);
     a.err = dev_err_flag;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((rc = pkv::launch_plan(a, s)) != PKV_OK) return rc;
     if ((rc = pkv::launch_decode(a, s, g_events[0][0], g_events[0][1])) != PKV_OK) return rc;
-    if (a.prefill_min_q < INT_MAX &&
+    if (lay.max_tiles > 0 &&
         (rc = pkv::launch_prefill(a, s, g_events[1][0], g_events[1][1])) != PKV_OK)
         return rc;
     return PKV_OK;

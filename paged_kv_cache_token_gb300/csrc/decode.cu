@@ -15,6 +15,7 @@
 // online softmax keeps (running max, running sum, un-normalised output) per query head.
 // The four warps merge in shared memory; a request split over several items leaves
 // partial results that the combine kernel reduces with the same rescaling.
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
                 if (pass == 0 && q == 1) n = Hkv * cdiv(pages, sp);
                 if (pass == 1 && q > 1 && q < a.prefill_min_q) n = Hkv * q;
                 if (pass == 2 && q >= a.prefill_min_q && q > 1)
-                    n = cdiv(q, 128) * a.num_q_heads;
+                    n = cdiv(q, 128) * (a.num_q_heads / a.heads_per_tile);
             }
             int total;
             const int ex = block_exclusive_scan(n, &total, s_warp);
@@ -180,9 +181,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
                     items[in.x + i] = make_int4(r, i / Hkv, i % Hkv, 0);
             } else if (q > 1) {
                 const int nt = cdiv(q, 128);
-                for (int i = lane; i < nt * a.num_q_heads; i += 32)
-                    tiles[in.w + i] = make_int4(r, nt - 1 - i / a.num_q_heads,
-                                                i % a.num_q_heads, 0);
+                const int slots = a.num_q_heads / a.heads_per_tile;
+                for (int i = lane; i < nt * slots; i += 32)
+                    tiles[in.w + i] = make_int4(r, nt - 1 - i / slots, i % slots, 0);
             }
         }
     }
@@ -610,7 +611,6 @@ __global__ void __launch_bounds__(128) combine_kernel(StepArgs a) {
 WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int total_q_tokens, int max_q_len, int num_sms,
                                  int prefill_min_q) {
-    (void)max_q_len;
     WorkspaceLayout L{};
     const int G = num_q_heads / num_kv_heads;
     const int pairs = std::max(1, num_reqs * num_kv_heads);
@@ -619,7 +619,14 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
     L.max_splits = max_splits;
     L.max_split_items = num_reqs * num_kv_heads * max_splits;
     L.max_items = L.max_split_items + total_q_tokens * num_kv_heads;
-    L.max_tiles = prefill_min_q < INT_MAX ? (total_q_tokens / 128 + num_reqs) * num_q_heads : 0;
+    // prefill tiles: none unless some request can reach prefill_min_q tokens; then at most
+    // T/128 full tiles plus one partial tile per prefilling request
+    const int prefill_reqs = max_q_len >= prefill_min_q
+                                 ? std::min(num_reqs, total_q_tokens / std::max(1, prefill_min_q))
+                                 : 0;
+    L.max_tiles = prefill_reqs ? (total_q_tokens / 128 + prefill_reqs) *
+                                     (num_q_heads / prefill_heads_per_tile(num_q_heads, num_kv_heads))
+                               : 0;
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     size_t off = 0;
     L.ctrl = off; off = up(off + 64 * sizeof(int32_t));

@@ -1,6 +1,7 @@
 // Internal launch interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -51,12 +52,17 @@ struct StepArgs {
     uint8_t* ws;
     WorkspaceLayout lay;
     int prefill_min_q;  // requests with q_len >= this go to the tensor-core prefill path
+    int heads_per_tile; // query heads per prefill tile (2 when a KV group has an even size)
     int32_t* err;
 };
 
 WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int total_q_tokens, int max_q_len, int num_sms,
                                  int prefill_min_q);
+// query heads one prefill tile covers for this head configuration
+inline int prefill_heads_per_tile(int num_q_heads, int num_kv_heads) {
+    return ((num_q_heads / num_kv_heads) % 2 == 0) ? 2 : 1;
+}
 
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 int launch_plan(const StepArgs& a, cudaStream_t stream);
@@ -65,5 +71,10 @@ int launch_decode(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                   cudaEvent_t ev_stop);
 int launch_prefill(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                    cudaEvent_t ev_stop);
+int launch_prefill_pair(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
+                        cudaEvent_t ev_stop);
+// Q ([T][Hq][D], 128-row boxes) and K/V pool (16-row page boxes) tensor maps, 128-byte
+// swizzle, 64-element-wide boxes.
+bool make_prefill_maps(const StepArgs& a, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv);
 
 }  // namespace pkv

@@ -16,7 +16,9 @@
 //              by more than 2^8), writes P = 2^(s - m) as 16-bit values into shared memory
 //              in the 128-byte-swizzled K-major layout, normalises O at the end;
 //   warp 4     producer: TMA loads of the Q tile (3-D map over [T][Hq][D]) and of each
-//              page's 16 x D block of K and V (2-D map over the pool rows), 2 stages;
+//              page's 16 x D block of K and V (2-D map over the pool rows); K has a 3-stage
+//              ring freed as soon as its scores are computed, V a 2-stage ring freed after
+//              P V, and keys are requested a tile ahead of values;
 //   warp 5     MMA: S_j = Q K_j^T into one of two TMEM buffers, then O += P_{j-1} V_{j-1},
 //              so the tensor core computes the next scores while softmax works.
 // Keys past the request's last key in the final tile have their V rows zeroed in shared
@@ -37,7 +39,8 @@ namespace {
 
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per KV tile (8 pages)
-constexpr int kStagesKV = 2;
+constexpr int kStagesK = 3;       // K ring: released as soon as its S = Q K^T completes
+constexpr int kStagesV = 2;       // V ring: released after its O += P V
 constexpr int kThreads = 192;     // 4 softmax warps + producer + MMA
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows > 2^8
@@ -47,17 +50,19 @@ struct PrefillSmem {
     static constexpr int kHalves = D / 64;               // 128-byte column blocks
     static constexpr int kHalfBytes = kBM * 128;          // 128 rows x 128 bytes
     static constexpr int kQ = kBM * D * 2;
-    static constexpr int kKV = kBN * D * 2;
+    static constexpr int kKV = kBN * D * 2;               // one K or V tile
     static constexpr int kP = kBM * kBN * 2;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQ;                       // stage s: K at kKOff + s*2*kKV
-    static constexpr int kPOff = kQ + kStagesKV * 2 * kKV;
+    static constexpr int kKOff = kQ;                       // K stage s at kKOff + s*kKV
+    static constexpr int kVOff = kKOff + kStagesK * kKV;   // V stage s at kVOff + s*kKV
+    static constexpr int kPOff = kVOff + kStagesV * kKV;
     static constexpr int kBarOff = kPOff + kP;
     static constexpr int kBars = 16;
     static constexpr int kMiscOff = kBarOff + kBars * 8;
     static constexpr int kBytes = kMiscOff + 64 + 1024;    // + alignment slack
     // keep one CTA per SM so the 512-column TMEM allocation never waits
     static constexpr int kLaunchBytes = kBytes > 120 * 1024 ? kBytes : 120 * 1024;
+    static_assert(kLaunchBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct TileInfo {
@@ -83,12 +88,14 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
     uint64_t* q_full = bars + 0;
-    uint64_t* kv_full = bars + 1;    // [kStagesKV]
-    uint64_t* kv_empty = bars + 3;   // [kStagesKV]
-    uint64_t* s_full = bars + 5;     // [2]
-    uint64_t* p_full = bars + 7;
-    uint64_t* o_done = bars + 8;
-    uint64_t* drain = bars + 9;
+    uint64_t* k_full = bars + 1;     // [kStagesK]
+    uint64_t* k_empty = bars + 4;    // [kStagesK]
+    uint64_t* v_full = bars + 7;     // [kStagesV]
+    uint64_t* v_empty = bars + 9;    // [kStagesV]
+    uint64_t* s_full = bars + 11;    // [2]
+    uint64_t* p_full = bars + 13;
+    uint64_t* o_done = bars + 14;
+    uint64_t* drain = bars + 15;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
     int* abort_flag = reinterpret_cast<int*>(smem + S::kMiscOff + 4);
 
@@ -114,9 +121,13 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kStagesKV; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < kStagesK; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kStagesV; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
@@ -139,11 +150,13 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
 
     uint8_t* sQ = smem + S::kQOff;
     uint8_t* sP = smem + S::kPOff;
-    auto sK = [&](int s) { return smem + S::kKOff + s * 2 * S::kKV; };
-    auto sV = [&](int s) { return smem + S::kKOff + s * 2 * S::kKV + S::kKV; };
+    auto sK = [&](int j) { return smem + S::kKOff + (j % kStagesK) * S::kKV; };  // tile j
+    auto sV = [&](int j) { return smem + S::kVOff + (j % kStagesV) * S::kKV; };
 
     if (warp == 4) {
         // ================================================================ producer
+        // whole warp: lanes fetch 32 block-table entries at a time, lane 0 issues TMA.
+        // Order K_0, then for every j: K_{j+1}, V_j -- keys run a tile ahead of values.
         if (lane == 0) {
             tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_k);
@@ -152,38 +165,60 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             for (int c = 0; c < S::kHalves; ++c)
                 tc::tma_load_3d(sQ + c * S::kHalfBytes, &tm_q, c * 64, ti.h,
                                 ti.q_off + ti.qt * kBM, q_full);
-            const int32_t* bt = a.block_table + static_cast<int64_t>(ti.r) * a.max_pages;
-            for (int j = 0; j < ti.n_kv; ++j) {
-                const int s = j % kStagesKV;
-                if (j >= kStagesKV && !mbar_wait(&kv_empty[s], ((j / kStagesKV) - 1) & 1)) {
-                    set_error(a.err, PKV_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
-                    break;
-                }
-                const int p0 = j * (kBN / kPage);
-                const int np = min(kBN / kPage, ti.npages_seq - p0);
-                mbar_arrive_expect_tx(&kv_full[s], np * kPage * D * 2 * 2);
-                for (int p = 0; p < np; ++p) {
-                    const int lp = p0 + p;
-                    int phys = 0;
-                    if (lp < a.max_pages) {
-                        phys = __ldg(bt + lp);
-                        if (phys < 0 || phys >= a.num_pages) {
+        }
+        const int32_t* bt = a.block_table + static_cast<int64_t>(ti.r) * a.max_pages;
+        int win_base = -1, win = 0;
+        auto page_of = [&](int lp) -> int {  // warp-wide; physical page of logical page lp
+            const int base = lp & ~31;
+            if (base != win_base) {
+                win_base = base;
+                const int l = base + lane;
+                win = 0;
+                if (l < ti.npages_seq) {
+                    if (l < a.max_pages) {
+                        win = __ldg(bt + l);
+                        if (win < 0 || win >= a.num_pages) {
                             set_error(a.err, PKV_DEVERR_PAGE_RANGE);
-                            phys = 0;
+                            win = 0;
                         }
                     } else {
                         set_error(a.err, PKV_DEVERR_TABLE_RANGE);
                     }
-                    const int row0 = (phys * a.num_kv_heads + ti.g) * kPage;
-                    for (int c = 0; c < S::kHalves; ++c) {
-                        tc::tma_load_2d(sK(s) + c * S::kHalfBytes + p * kPage * 128, &tm_k, c * 64,
-                                        row0, &kv_full[s]);
-                        tc::tma_load_2d(sV(s) + c * S::kHalfBytes + p * kPage * 128, &tm_v, c * 64,
-                                        row0, &kv_full[s]);
-                    }
                 }
             }
+            return __shfl_sync(kFull, win, lp & 31);
+        };
+        bool ok = true;
+        auto issue = [&](int j, bool is_v) {
+            const int nst = is_v ? kStagesV : kStagesK;
+            uint64_t* full = is_v ? &v_full[j % kStagesV] : &k_full[j % kStagesK];
+            uint64_t* empty = is_v ? &v_empty[j % kStagesV] : &k_empty[j % kStagesK];
+            if (j >= nst && lane == 0 && !mbar_wait(empty, ((j / nst) - 1) & 1)) ok = false;
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok) return;
+            const int p0 = j * (kBN / kPage);
+            const int np = min(kBN / kPage, ti.npages_seq - p0);
+            uint8_t* dst = is_v ? sV(j) : sK(j);
+            const void* map = is_v ? static_cast<const void*>(&tm_v) : static_cast<const void*>(&tm_k);
+            if (lane == 0) mbar_arrive_expect_tx(full, np * kPage * D * 2);
+            for (int p = 0; p < np; ++p) {
+                const int phys = page_of(p0 + p);
+                if (lane == 0) {
+                    const int row0 = (phys * a.num_kv_heads + ti.g) * kPage;
+                    for (int c = 0; c < S::kHalves; ++c)
+                        tc::tma_load_2d(dst + c * S::kHalfBytes + p * kPage * 128, map, c * 64,
+                                        row0, full);
+                }
+            }
+        };
+        if (ti.n_kv > 0) issue(0, false);
+        for (int j = 0; ok && j < ti.n_kv; ++j) {
+            if (j + 1 < ti.n_kv) issue(j + 1, false);
+            if (ok) issue(j, true);
+        }
+        if (!ok && lane == 0) {
+            set_error(a.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
         }
     } else if (warp == 5) {
         // ================================================================ MMA issuer
@@ -192,7 +227,7 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             const uint32_t p_addr = smem_u32(sP);
             bool ok = mbar_wait(q_full, 0);
             auto issue_pv = [&](int jj) {  // O (+)= P_jj V_jj
-                const uint32_t v_addr = smem_u32(sV(jj % kStagesKV));
+                const uint32_t v_addr = smem_u32(sV(jj));
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     const uint64_t ad = tc::smem_desc_sw128(
@@ -201,13 +236,15 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                     tc::mma_f16_ss(tm_o, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::commit(o_done);
-                tc::commit(&kv_empty[jj % kStagesKV]);
+                tc::commit(&v_empty[jj % kStagesV]);
+            };
+            auto wait_v = [&](int jj) {
+                return mbar_wait(&v_full[jj % kStagesV], (jj / kStagesV) & 1);
             };
             for (int j = 0; ok && j < ti.n_kv; ++j) {
-                const int s = j % kStagesKV;
-                if (!mbar_wait(&kv_full[s], (j / kStagesKV) & 1)) { ok = false; break; }
+                if (!mbar_wait(&k_full[j % kStagesK], (j / kStagesK) & 1)) { ok = false; break; }
                 tc::fence_after_sync();
-                const uint32_t k_addr = smem_u32(sK(s));
+                const uint32_t k_addr = smem_u32(sK(j));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * S::kHalfBytes + (kk & 3) * 32;
@@ -216,14 +253,15 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                     tc::mma_f16_ss(tm_s(j), ad, bd, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&s_full[j & 1]);
+                tc::commit(&k_empty[j % kStagesK]);
                 if (j >= 1) {
-                    if (!mbar_wait(p_full, (j - 1) & 1)) { ok = false; break; }
+                    if (!wait_v(j - 1) || !mbar_wait(p_full, (j - 1) & 1)) { ok = false; break; }
                     tc::fence_after_sync();
                     issue_pv(j - 1);
                 }
             }
             if (ok && ti.n_kv > 0) {
-                if (mbar_wait(p_full, (ti.n_kv - 1) & 1)) {
+                if (wait_v(ti.n_kv - 1) && mbar_wait(p_full, (ti.n_kv - 1) & 1)) {
                     tc::fence_after_sync();
                     issue_pv(ti.n_kv - 1);
                 } else {
@@ -267,11 +305,27 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                 }
             }
             const float m_new = fmaxf(m, tmax);
+            const bool need = (j == 0) || (m_new > m + kRescaleThreshold);
+            const float alpha = (j > 0 && need) ? tc::ex2(m - m_new) : 1.f;
+            if (need) m = m_new;
+            // P = 2^(x - m) packed to 16-bit pairs before waiting for the previous P V, so
+            // the exponentials overlap with the tensor core
+            uint32_t pk[64];
+            float lsum = 0.f;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float p0 = tc::ex2(__uint_as_float(sr[cb][2 * u]) - m);
+                    const float p1 = tc::ex2(__uint_as_float(sr[cb][2 * u + 1]) - m);
+                    lsum += p0 + p1;
+                    pk[cb * 16 + u] = Cv::pack(p0, p1);
+                }
+            }
+            l = l * alpha + lsum;
             if (j > 0 && !mbar_wait(o_done, (j - 1) & 1)) { ok = false; break; }
             __syncwarp();
-            const bool need = (j == 0) || (m_new > m + kRescaleThreshold);
-            if (j > 0 && __any_sync(kFull, need)) {
-                const float alpha = need ? tc::ex2(m - m_new) : 1.f;
+            if (j > 0 && __any_sync(kFull, alpha != 1.f)) {  // rescale my O row
                 tc::fence_after_sync();
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
@@ -284,32 +338,19 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                     tc::tmem_st32(tm_o + lane_off + cb * 32, orow);
                 }
                 tc::tmem_wait_st();
-                if (need) l *= alpha;
             }
-            if (need) m = m_new;
-            // P = 2^(x - m) as 16-bit values, row i of the 128-byte-swizzled K-major tile
+            // row i of the 128-byte-swizzled K-major P tile
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float p0 = tc::ex2(__uint_as_float(sr[cb][q8 * 8 + 2 * u]) - m);
-                        const float p1 = tc::ex2(__uint_as_float(sr[cb][q8 * 8 + 2 * u + 1]) - m);
-                        l += p0 + p1;
-                        pk[u] = Cv::pack(p0, p1);
-                    }
-                    const int chunk = cb * 4 + q8;            // 16-byte chunk along the keys
-                    const int half = chunk >> 3, c = chunk & 7;
-                    uint8_t* dst = sP + half * S::kHalfBytes + i * 128 + ((c ^ (i & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
+            for (int chunk = 0; chunk < 16; ++chunk) {      // 16-byte chunks along the keys
+                const int half = chunk >> 3, c = chunk & 7;
+                uint8_t* dst = sP + half * S::kHalfBytes + i * 128 + ((c ^ (i & 7)) << 4);
+                *reinterpret_cast<uint4*>(dst) =
+                    make_uint4(pk[chunk * 4], pk[chunk * 4 + 1], pk[chunk * 4 + 2], pk[chunk * 4 + 3]);
             }
             // final tile: V rows past the last key are zeroed (P is 0 there, V may be NaN)
             if (j == ti.n_kv - 1 && kbase + i >= ti.kv_len &&
-                mbar_wait(&kv_full[j % kStagesKV], (j / kStagesKV) & 1)) {
-                uint8_t* vrow = sV(j % kStagesKV);
+                mbar_wait(&v_full[j % kStagesV], (j / kStagesV) & 1)) {
+                uint8_t* vrow = sV(j);
 #pragma unroll
                 for (int c = 0; c < S::kHalves; ++c) {
                     uint4* dst = reinterpret_cast<uint4*>(vrow + c * S::kHalfBytes + i * 128);
@@ -361,10 +402,12 @@ prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
     }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------------------------
 // host side: tensor maps and launch
 // ------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* p = nullptr;
@@ -378,7 +421,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_maps(const StepArgs& a, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+bool make_prefill_maps(const StepArgs& a, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
     auto enc = encode_fn();
     if (!enc) return false;
     const CUtensorMapDataType dt =
@@ -413,6 +456,8 @@ bool make_maps(const StepArgs& a, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap*
     return true;
 }
 
+namespace {
+
 template <typename T, int D>
 int launch_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
     using S = PrefillSmem<D>;
@@ -424,7 +469,7 @@ int launch_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t
         configured = true;
     }
     alignas(64) CUtensorMap mq, mk, mv;
-    if (!make_maps(a, &mq, &mk, &mv)) return PKV_ERR_CUDA;
+    if (!make_prefill_maps(a, &mq, &mk, &mv)) return PKV_ERR_CUDA;
     if (a.lay.max_tiles <= 0) return PKV_OK;
     if (e0 && cudaEventRecord(e0, stream) != cudaSuccess) return PKV_ERR_CUDA;
     prefill_kernel<T, D><<<a.lay.max_tiles, kThreads, S::kLaunchBytes, stream>>>(a, mq, mk, mv);
@@ -436,6 +481,7 @@ int launch_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t
 }  // namespace
 
 int launch_prefill(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
+    if (a.heads_per_tile == 2) return launch_prefill_pair(a, stream, e0, e1);
     if (a.dtype == PKV_BF16)
         return a.head_dim == 128 ? launch_t<__nv_bfloat16, 128>(a, stream, e0, e1)
                                  : launch_t<__nv_bfloat16, 64>(a, stream, e0, e1);

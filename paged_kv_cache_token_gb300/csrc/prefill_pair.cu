@@ -1,0 +1,414 @@
+// Prefill-chunk attention for two query heads of one KV group per CTA (grouped-query
+// attention with an even group size, hotelren.com/news/6181127 §6.3).
+//
+// Same mathematics as prefill.cu -- causal softmax attention of a 128-row query tile
+// against every key of its request read from the pages (hotelren.com §1.1, §2.1;
+// niuwancheng.cn "11. chunked prefill and unified scheduling") -- organised so the tensor
+// core stays busy:
+//   * both heads consume one K/V stream: each 128-key tile (8 pages) is loaded once for
+//     2 x 128 query rows, halving L2->SM traffic per FLOP;
+//   * three producer warps issue the page boxes in parallel (a tiled TMA instruction
+//     keeps its issuing thread busy for ~190 cycles, so one issuer cannot feed the MMA);
+//   * P = 2^(s - m) is written as packed 16-bit pairs into tensor memory over the scores it
+//     came from and read from there by the P V MMA, so shared memory holds only Q, K, V;
+//   * the MMA warp alternates the heads -- S0, S1, P0 V, S0', P1 V, S1', ... -- while the
+//     two softmax warpgroups work on the other head's scores;
+//   * a head's scores S_j complete only after its previous P V (one thread issues every
+//     MMA and tcgen05.commit tracks all of them), so the softmax may rescale O right away.
+// Softmax makes two passes over the score row in tensor memory (max, then exponentials) to
+// stay within the register budget of 384 threads.
+#include <cuda.h>
+
+#include <climits>
+#include <type_traits>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kStagesK = 3;
+constexpr int kStagesV = 2;
+constexpr int kProducers = 3;
+constexpr int kWarpMma = 8;
+constexpr int kWarpProd0 = 9;
+constexpr int kThreads = 32 * (kWarpProd0 + kProducers);  // 384
+constexpr int kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct PairSmem {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kHalfBytes = kBM * 128;
+    static constexpr int kQ = kBM * D * 2;                 // one head's Q tile
+    static constexpr int kKV = kBN * D * 2;
+    static constexpr int kQOff = 0;                        // head h at kQOff + h * kQ
+    static constexpr int kKOff = 2 * kQ;
+    static constexpr int kVOff = kKOff + kStagesK * kKV;
+    static constexpr int kBarOff = kVOff + kStagesV * kKV;
+    static constexpr int kBars = 24;
+    static constexpr int kMiscOff = kBarOff + kBars * 8;
+    static constexpr int kBytes = kMiscOff + 64 + 1024;
+    static constexpr int kLaunchBytes = kBytes > 120 * 1024 ? kBytes : 120 * 1024;
+    static_assert(kLaunchBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v) {
+    using S = PairSmem<D>;
+    using Cv = F16<T>;
+    constexpr int kAB = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+    constexpr uint32_t kIdescS = tc::idesc_f16(kAB, 0, kBM, kBN);
+    constexpr uint32_t kIdescO = tc::idesc_f16(kAB, 1, kBM, D);
+
+    const int32_t* ctrl = reinterpret_cast<const int32_t*>(a.ws + a.lay.ctrl);
+    if (static_cast<int>(blockIdx.x) >= ctrl[9]) return;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+    uint64_t* q_full = bars + 0;
+    uint64_t* k_full = bars + 1;    // [3]
+    uint64_t* k_empty = bars + 4;   // [3]
+    uint64_t* v_full = bars + 7;    // [2]
+    uint64_t* v_empty = bars + 9;   // [2]
+    uint64_t* s_full = bars + 11;   // [2] per head
+    uint64_t* p_full = bars + 13;   // [2] per head
+    uint64_t* o_final = bars + 15;
+    uint64_t* drain = bars + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- tile: request r, query tile qt, head pair hp -> heads 2hp, 2hp+1 (one KV group)
+    const int4 tl = reinterpret_cast<const int4*>(a.ws + a.lay.tiles)[blockIdx.x];
+    const int r = tl.x, qt = tl.y, h0 = 2 * tl.z;
+    const int g = h0 / (a.num_q_heads / a.num_kv_heads);
+    const int ctx = a.context_lens[r];
+    const int q_off = a.q_offsets[r];
+    const int rows_valid = min(kBM, a.q_lens[r] - qt * kBM);
+    const int first_pos = ctx + qt * kBM;
+    const int kv_len = first_pos + rows_valid;
+    const int n_kv = cdiv(kv_len, kBN);
+    const int npages_seq = cdiv(kv_len, kPage);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kStagesK; ++s) {
+            mbar_init(&k_full[s], kProducers);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kStagesV; ++s) {
+            mbar_init(&v_full[s], kProducers);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&p_full[h], 128);
+        }
+        mbar_init(o_final, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    auto tm_s = [&](int h) { return tmem + static_cast<uint32_t>(h * kBN); };     // S_h / P_h
+    auto tm_o = [&](int h) { return tmem + static_cast<uint32_t>(2 * kBN + h * 128); };
+    auto sQ = [&](int h) { return smem + S::kQOff + h * S::kQ; };
+    auto sK = [&](int j) { return smem + S::kKOff + (j % kStagesK) * S::kKV; };
+    auto sV = [&](int j) { return smem + S::kVOff + (j % kStagesV) * S::kKV; };
+
+    if (warp >= kWarpProd0) {
+        // ================================================================ producers
+        const int pi = warp - kWarpProd0;
+        if (pi == 0 && lane == 0) {
+            tc::prefetch_tmap(&tm_q);
+            tc::prefetch_tmap(&tm_k);
+            tc::prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(q_full, 2 * S::kQ);
+            for (int h = 0; h < 2; ++h)
+                for (int c = 0; c < S::kHalves; ++c)
+                    tc::tma_load_3d(sQ(h) + c * S::kHalfBytes, &tm_q, c * 64, h0 + h,
+                                    q_off + qt * kBM, q_full);
+        }
+        const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.max_pages;
+        int win_base = -1, win = 0;
+        auto page_of = [&](int lp) -> int {  // warp-wide
+            const int base = lp & ~31;
+            if (base != win_base) {
+                win_base = base;
+                const int l = base + lane;
+                win = 0;
+                if (l < npages_seq) {
+                    if (l < a.max_pages) {
+                        win = __ldg(bt + l);
+                        if (win < 0 || win >= a.num_pages) {
+                            set_error(a.err, PKV_DEVERR_PAGE_RANGE);
+                            win = 0;
+                        }
+                    } else {
+                        set_error(a.err, PKV_DEVERR_TABLE_RANGE);
+                    }
+                }
+            }
+            return __shfl_sync(kFull, win, lp & 31);
+        };
+        bool ok = true;
+        auto issue = [&](int j, bool is_v) {
+            const int nst = is_v ? kStagesV : kStagesK;
+            uint64_t* full = is_v ? &v_full[j % kStagesV] : &k_full[j % kStagesK];
+            uint64_t* empty = is_v ? &v_empty[j % kStagesV] : &k_empty[j % kStagesK];
+            if (j >= nst && lane == 0 && !mbar_wait(empty, ((j / nst) - 1) & 1)) ok = false;
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok) return;
+            const int p0 = j * (kBN / kPage);
+            const int np = min(kBN / kPage, npages_seq - p0);
+            const int mine = np > pi ? (np - pi + kProducers - 1) / kProducers : 0;
+            uint8_t* dst = is_v ? sV(j) : sK(j);
+            const void* map = is_v ? static_cast<const void*>(&tm_v) : static_cast<const void*>(&tm_k);
+            if (lane == 0) mbar_arrive_expect_tx(full, mine * kPage * D * 2);
+            for (int p = 0; p < np; ++p) {
+                const int phys = page_of(p0 + p);
+                if (lane == 0 && p % kProducers == pi) {
+                    const int row0 = (phys * a.num_kv_heads + g) * kPage;
+                    for (int c = 0; c < S::kHalves; ++c)
+                        tc::tma_load_2d(dst + c * S::kHalfBytes + p * kPage * 128, map, c * 64,
+                                        row0, full);
+                }
+            }
+        };
+        if (n_kv > 0) issue(0, false);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            if (j + 1 < n_kv) issue(j + 1, false);
+            if (ok) issue(j, true);
+        }
+        if (!ok && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
+    } else if (warp == kWarpMma) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(q_full, 0);
+            auto issue_s = [&](int h, int j) {
+                const uint32_t q_addr = smem_u32(sQ(h)), k_addr = smem_u32(sK(j));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * S::kHalfBytes + (kk & 3) * 32;
+                    tc::mma_f16_ss(tm_s(h), tc::smem_desc_sw128(q_addr + off, 16, 1024),
+                                   tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS,
+                                   kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&s_full[h]);
+            };
+            auto issue_pv = [&](int h, int j) {
+                const uint32_t v_addr = smem_u32(sV(j));
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    tc::mma_f16_ts(tm_o(h), tm_s(h) + kk * 8,
+                                   tc::smem_desc_sw128(v_addr + kk * 2048, S::kHalfBytes, 1024),
+                                   kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+            };
+            auto wait_k = [&](int j) {
+                return mbar_wait(&k_full[j % kStagesK], (j / kStagesK) & 1);
+            };
+            if (ok && n_kv > 0 && (ok = wait_k(0))) {
+                tc::fence_after_sync();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc::commit(&k_empty[0]);
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (!mbar_wait(&v_full[j % kStagesV], (j / kStagesV) & 1) ||
+                    !mbar_wait(&p_full[0], j & 1)) { ok = false; break; }
+                tc::fence_after_sync();
+                issue_pv(0, j);
+                const bool more = j + 1 < n_kv;
+                if (more) {
+                    if (!wait_k(j + 1)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    issue_s(0, j + 1);
+                }
+                if (!mbar_wait(&p_full[1], j & 1)) { ok = false; break; }
+                tc::fence_after_sync();
+                issue_pv(1, j);
+                tc::commit(&v_empty[j % kStagesV]);
+                if (more) {
+                    issue_s(1, j + 1);
+                    tc::commit(&k_empty[(j + 1) % kStagesK]);
+                }
+            }
+            if (!ok) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            tc::commit(o_final);
+            tc::commit(drain);
+            mbar_wait(drain, 0);
+        }
+    } else {
+        // ================================================================ softmax (head h)
+        const int h = warp >> 2;
+        const int i = threadIdx.x & 127;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const int pos = first_pos + i;
+        const float sl2 = a.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!mbar_wait(&s_full[h], j & 1)) { ok = false; break; }
+            __syncwarp();
+            tc::fence_after_sync();
+            const int kbase = j * kBN;
+            const bool diag = kbase + kBN - 1 > first_pos;
+            // pass 1: row maximum of the raw scores
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t sr[32];
+                tc::tmem_ld32(tm_s(h) + lane_off + cb * 32, sr);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float x = __uint_as_float(sr[e]);
+                    if (diag && kbase + cb * 32 + e > pos) x = -INFINITY;
+                    mx[e & 3] = fmaxf(mx[e & 3], x);
+                }
+            }
+            const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+            const float m_new = fmaxf(m, tmax);
+            const bool need = (j == 0) || (m_new > m + kRescaleThreshold);
+            const float alpha = (j > 0 && need) ? tc::ex2(m - m_new) : 1.f;
+            if (need) m = m_new;
+            if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
+                // O_h is stable: its last P V completed before these scores did
+#pragma unroll
+                for (int cb = 0; cb < D / 32; ++cb) {
+                    uint32_t orow[32];
+                    tc::tmem_ld32(tm_o(h) + lane_off + cb * 32, orow);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
+                    tc::tmem_st32(tm_o(h) + lane_off + cb * 32, orow);
+                }
+            }
+            // pass 2: P = 2^(s * scale_log2 - m), packed pairs written over the scores
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t sr[32];
+                tc::tmem_ld32(tm_s(h) + lane_off + cb * 32, sr);
+                tc::tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int c0 = kbase + cb * 32 + 2 * u;
+                    float p0 = tc::ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, -m));
+                    float p1 = tc::ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, -m));
+                    if (diag && c0 > pos) p0 = 0.f;
+                    if (diag && c0 + 1 > pos) p1 = 0.f;
+                    ls[u & 3] += p0 + p1;
+                    pk[u] = Cv::pack(p0, p1);
+                }
+                tc::tmem_st16(tm_s(h) + lane_off + cb * 16, pk);
+            }
+            tc::tmem_wait_st();
+            l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            // final tile: V rows past the last key are zeroed (P is 0 there; stale pool
+            // data may be NaN and 0 * NaN would poison the product)
+            if (h == 0 && j == n_kv - 1 && kbase + i >= kv_len &&
+                mbar_wait(&v_full[j % kStagesV], (j / kStagesV) & 1)) {
+                uint8_t* vrow = sV(j);
+#pragma unroll
+                for (int c = 0; c < S::kHalves; ++c) {
+                    uint4* dst = reinterpret_cast<uint4*>(vrow + c * S::kHalfBytes + i * 128);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0, 0, 0, 0);
+                }
+                tc::fence_proxy_async_smem();
+            }
+            tc::fence_before_sync();
+            mbar_arrive(&p_full[h]);
+        }
+        // ---- epilogue: O / l -> 16-bit, row i of head h0 + h
+        if (ok && n_kv > 0 && mbar_wait(o_final, 0)) {
+            __syncwarp();
+            tc::fence_after_sync();
+            const float inv_l = 1.f / l;
+            T* orow = static_cast<T*>(a.out) +
+                      (static_cast<int64_t>(q_off + qt * kBM + i) * a.num_q_heads + h0 + h) * D;
+#pragma unroll
+            for (int cb = 0; cb < D / 32; ++cb) {
+                uint32_t o32[32];
+                __syncwarp();
+                tc::tmem_ld32(tm_o(h) + lane_off + cb * 32, o32);
+                tc::tmem_wait_ld();
+                if (i < rows_valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = Cv::pack(__uint_as_float(o32[u * 8 + 2 * e]) * inv_l,
+                                            __uint_as_float(o32[u * 8 + 2 * e + 1]) * inv_l);
+                        dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        } else if (n_kv > 0) {
+            set_error(a.err, PKV_DEVERR_TIMEOUT);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <typename T, int D>
+int launch_pair_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
+    using S = PairSmem<D>;
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(prefill_pair_kernel<T, D>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 S::kLaunchBytes) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured = true;
+    }
+    alignas(64) CUtensorMap mq, mk, mv;
+    if (!make_prefill_maps(a, &mq, &mk, &mv)) return PKV_ERR_CUDA;
+    if (a.lay.max_tiles <= 0) return PKV_OK;
+    if (e0 && cudaEventRecord(e0, stream) != cudaSuccess) return PKV_ERR_CUDA;
+    prefill_pair_kernel<T, D><<<a.lay.max_tiles, kThreads, S::kLaunchBytes, stream>>>(a, mq, mk,
+                                                                                       mv);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (e1 && cudaEventRecord(e1, stream) != cudaSuccess) return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+}  // namespace
+
+int launch_prefill_pair(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
+    if (a.dtype == PKV_BF16)
+        return a.head_dim == 128 ? launch_pair_t<__nv_bfloat16, 128>(a, stream, e0, e1)
+                                 : launch_pair_t<__nv_bfloat16, 64>(a, stream, e0, e1);
+    return a.head_dim == 128 ? launch_pair_t<__half, 128>(a, stream, e0, e1)
+                             : launch_pair_t<__half, 64>(a, stream, e0, e1);
+}
+
+}  // namespace pkv
