@@ -90,6 +90,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// Whole-warp wait: lane 0 polls, the other lanes stay parked in the warp barrier instead of
+// spinning on the mbarrier; every lane returns lane 0's result, converged.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+    __syncwarp();
+    return __shfl_sync(kFull, ok, 0) != 0;
+}
 
 // ---------------------------------------------------------------- bulk async copy (TMA, 1-D)
 // Global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte aligned) that

@@ -202,23 +202,28 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
         // ================================================================ MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait(q_full, 0);
+            // descriptors of every tile base; a k-step adds its byte offset >> 4 to the
+            // 14-bit start-address field (all addresses stay below 256 KiB)
+            const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(sQ(0)), 16, 1024);
+            const uint64_t dq1 = tc::smem_desc_sw128(smem_u32(sQ(1)), 16, 1024);
+            const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(sK(0)), 16, 1024);
+            const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(sV(0)), S::kHalfBytes, 1024);
+            constexpr uint64_t kKStep = (S::kKV) >> 4;          // stage stride in 16 B units
             auto issue_s = [&](int h, int j) {
-                const uint32_t q_addr = smem_u32(sQ(h)), k_addr = smem_u32(sK(j));
+                const uint64_t dq = h ? dq1 : dq0;
+                const uint64_t dk = dk0 + static_cast<uint64_t>(j % kStagesK) * kKStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * S::kHalfBytes + (kk & 3) * 32;
-                    tc::mma_f16_ss(tm_s(h), tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                                   tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS,
-                                   kk > 0 ? 1u : 0u);
+                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * S::kHalfBytes + (kk & 3) * 32) >> 4);
+                    tc::mma_f16_ss(tm_s(h), dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&s_full[h]);
             };
             auto issue_pv = [&](int h, int j) {
-                const uint32_t v_addr = smem_u32(sV(j));
+                const uint64_t dv = dv0 + static_cast<uint64_t>(j % kStagesV) * kKStep;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    tc::mma_f16_ts(tm_o(h), tm_s(h) + kk * 8,
-                                   tc::smem_desc_sw128(v_addr + kk * 2048, S::kHalfBytes, 1024),
+                    tc::mma_f16_ts(tm_o(h), tm_s(h) + kk * 8, dv + static_cast<uint64_t>(kk * 2048 >> 4),
                                    kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
             };
             auto wait_k = [&](int j) {
@@ -260,80 +265,105 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
         const int h = warp >> 2;
         const int i = threadIdx.x & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t my_s = tm_s(h) + lane_off, my_o = tm_o(h) + lane_off;
         const int pos = first_pos + i;
         const float sl2 = a.scale_log2;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            if (!mbar_wait(&s_full[h], j & 1)) { ok = false; break; }
-            __syncwarp();
+            if (!mbar_wait_warp(&s_full[h], j & 1)) { ok = false; break; }
             tc::fence_after_sync();
             const int kbase = j * kBN;
+            // keys at or past `lim` are masked for this row (only on the diagonal tiles)
             const bool diag = kbase + kBN - 1 > first_pos;
+            const int lim = diag ? pos + 1 - kbase : kBN;
             // pass 1: row maximum of the raw scores
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t sr[32];
-                tc::tmem_ld32(tm_s(h) + lane_off + cb * 32, sr);
+                tc::tmem_ld32(my_s + cb * 32, sr);
                 tc::tmem_wait_ld();
+                if (!diag) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float x = __uint_as_float(sr[e]);
-                    if (diag && kbase + cb * 32 + e > pos) x = -INFINITY;
-                    mx[e & 3] = fmaxf(mx[e & 3], x);
+                    for (int e = 0; e < 32; e += 4) {
+                        mx0 = fmaxf(mx0, __uint_as_float(sr[e]));
+                        mx1 = fmaxf(mx1, __uint_as_float(sr[e + 1]));
+                        mx2 = fmaxf(mx2, __uint_as_float(sr[e + 2]));
+                        mx3 = fmaxf(mx3, __uint_as_float(sr[e + 3]));
+                    }
+                } else {
+                    const int rem = lim - cb * 32;  // valid keys in this chunk
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float x = e < rem ? __uint_as_float(sr[e]) : -INFINITY;
+                        if ((e & 1) == 0) mx0 = fmaxf(mx0, x); else mx1 = fmaxf(mx1, x);
+                    }
                 }
             }
-            const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+            const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
             const float m_new = fmaxf(m, tmax);
             const bool need = (j == 0) || (m_new > m + kRescaleThreshold);
             const float alpha = (j > 0 && need) ? tc::ex2(m - m_new) : 1.f;
             if (need) m = m_new;
             if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
                 // O_h is stable: its last P V completed before these scores did
-#pragma unroll
+#pragma unroll 1
                 for (int cb = 0; cb < D / 32; ++cb) {
                     uint32_t orow[32];
-                    tc::tmem_ld32(tm_o(h) + lane_off + cb * 32, orow);
+                    tc::tmem_ld32(my_o + cb * 32, orow);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
-                    tc::tmem_st32(tm_o(h) + lane_off + cb * 32, orow);
+                    tc::tmem_st32(my_o + cb * 32, orow);
                 }
             }
             // pass 2: P = 2^(s * scale_log2 - m), packed pairs written over the scores
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+            float ls0 = 0.f, ls1 = 0.f;
+            const float nm = -m;
+#pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t sr[32];
-                tc::tmem_ld32(tm_s(h) + lane_off + cb * 32, sr);
+                tc::tmem_ld32(my_s + cb * 32, sr);
                 tc::tmem_wait_ld();
                 uint32_t pk[16];
+                if (!diag) {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int c0 = kbase + cb * 32 + 2 * u;
-                    float p0 = tc::ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, -m));
-                    float p1 = tc::ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, -m));
-                    if (diag && c0 > pos) p0 = 0.f;
-                    if (diag && c0 + 1 > pos) p1 = 0.f;
-                    ls[u & 3] += p0 + p1;
-                    pk[u] = Cv::pack(p0, p1);
+                    for (int u = 0; u < 16; ++u) {
+                        const float p0 = tc::ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, nm));
+                        const float p1 = tc::ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nm));
+                        if (u & 1) ls1 += p0 + p1; else ls0 += p0 + p1;
+                        pk[u] = Cv::pack(p0, p1);
+                    }
+                } else {
+                    const int rem = lim - cb * 32;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        float p0 = tc::ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, nm));
+                        float p1 = tc::ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nm));
+                        p0 = 2 * u < rem ? p0 : 0.f;
+                        p1 = 2 * u + 1 < rem ? p1 : 0.f;
+                        if (u & 1) ls1 += p0 + p1; else ls0 += p0 + p1;
+                        pk[u] = Cv::pack(p0, p1);
+                    }
                 }
-                tc::tmem_st16(tm_s(h) + lane_off + cb * 16, pk);
+                tc::tmem_st16(my_s + cb * 16, pk);
             }
             tc::tmem_wait_st();
-            l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            l = l * alpha + (ls0 + ls1);
             // final tile: V rows past the last key are zeroed (P is 0 there; stale pool
             // data may be NaN and 0 * NaN would poison the product)
-            if (h == 0 && j == n_kv - 1 && kbase + i >= kv_len &&
-                mbar_wait(&v_full[j % kStagesV], (j / kStagesV) & 1)) {
-                uint8_t* vrow = sV(j);
+            if (h == 0 && j == n_kv - 1 && kv_len - kbase < kBN) {
+                if (mbar_wait_warp(&v_full[j % kStagesV], (j / kStagesV) & 1) &&
+                    kbase + i >= kv_len) {
+                    uint8_t* vrow = sV(j);
 #pragma unroll
-                for (int c = 0; c < S::kHalves; ++c) {
-                    uint4* dst = reinterpret_cast<uint4*>(vrow + c * S::kHalfBytes + i * 128);
+                    for (int c = 0; c < S::kHalves; ++c) {
+                        uint4* dst = reinterpret_cast<uint4*>(vrow + c * S::kHalfBytes + i * 128);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0, 0, 0, 0);
+                        for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0, 0, 0, 0);
+                    }
                 }
                 tc::fence_proxy_async_smem();
             }
@@ -341,17 +371,15 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             mbar_arrive(&p_full[h]);
         }
         // ---- epilogue: O / l -> 16-bit, row i of head h0 + h
-        if (ok && n_kv > 0 && mbar_wait(o_final, 0)) {
-            __syncwarp();
+        if (ok && n_kv > 0 && mbar_wait_warp(o_final, 0)) {
             tc::fence_after_sync();
             const float inv_l = 1.f / l;
             T* orow = static_cast<T*>(a.out) +
                       (static_cast<int64_t>(q_off + qt * kBM + i) * a.num_q_heads + h0 + h) * D;
-#pragma unroll
+#pragma unroll 1
             for (int cb = 0; cb < D / 32; ++cb) {
                 uint32_t o32[32];
-                __syncwarp();
-                tc::tmem_ld32(tm_o(h) + lane_off + cb * 32, o32);
+                tc::tmem_ld32(my_o + cb * 32, o32);
                 tc::tmem_wait_ld();
                 if (i < rows_valid) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
@@ -365,6 +393,7 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                         dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
+                __syncwarp();
             }
         } else if (n_kv > 0) {
             set_error(a.err, PKV_DEVERR_TIMEOUT);
