@@ -7,8 +7,9 @@
 // core stays busy:
 //   * both heads consume one K/V stream: each 128-key tile (8 pages) is loaded once for
 //     2 x 128 query rows, halving L2->SM traffic per FLOP;
-//   * three producer warps issue the page boxes in parallel (a tiled TMA instruction
-//     keeps its issuing thread busy for ~190 cycles, so one issuer cannot feed the MMA);
+//   * six producer warps issue the page boxes in parallel, three for keys and three for
+//     values, each stream on its own ring (a tiled TMA instruction keeps its issuing
+//     thread busy for ~190 cycles, so one issuer cannot feed the MMA);
 //   * P = 2^(s - m) is written as packed 16-bit pairs into tensor memory over the scores it
 //     came from and read from there by the P V MMA, so shared memory holds only Q, K, V;
 //   * the MMA warp alternates the heads -- S0, S1, P0 V, S0', P1 V, S1', ... -- while the
@@ -16,7 +17,7 @@
 //   * a head's scores S_j complete only after its previous P V (one thread issues every
 //     MMA and tcgen05.commit tracks all of them), so the softmax may rescale O right away.
 // Softmax makes two passes over the score row in tensor memory (max, then exponentials) to
-// stay within the register budget of 384 threads.
+// stay within the register budget of 480 threads.
 #include <cuda.h>
 
 #include <climits>
@@ -34,10 +35,10 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kStagesK = 3;
 constexpr int kStagesV = 2;
-constexpr int kProducers = 3;
+constexpr int kProducers = 3;      // warps issuing K boxes; as many again issue V boxes
 constexpr int kWarpMma = 8;
-constexpr int kWarpProd0 = 9;
-constexpr int kThreads = 32 * (kWarpProd0 + kProducers);  // 384
+constexpr int kWarpProd0 = 9;      // warps 9..11 load K (and Q), 12..14 load V
+constexpr int kThreads = 32 * (kWarpProd0 + 2 * kProducers);  // 480
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -135,8 +136,9 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
 
     if (warp >= kWarpProd0) {
         // ================================================================ producers
-        const int pi = warp - kWarpProd0;
-        if (pi == 0 && lane == 0) {
+        const bool is_v = warp >= kWarpProd0 + kProducers;
+        const int pi = (warp - kWarpProd0) % kProducers;
+        if (!is_v && pi == 0 && lane == 0) {
             tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_k);
             tc::prefetch_tmap(&tm_v);
@@ -192,11 +194,7 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                 }
             }
         };
-        if (n_kv > 0) issue(0, false);
-        for (int j = 0; ok && j < n_kv; ++j) {
-            if (j + 1 < n_kv) issue(j + 1, false);
-            if (ok) issue(j, true);
-        }
+        for (int j = 0; ok && j < n_kv; ++j) issue(j, is_v);
         if (!ok && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
     } else if (warp == kWarpMma) {
         // ================================================================ MMA issuer
@@ -319,14 +317,14 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                     tc::tmem_st32(my_o + cb * 32, orow);
                 }
             }
-            // pass 2: P = 2^(s * scale_log2 - m), packed pairs written over the scores
+            // pass 2: P = 2^(s * scale_log2 - m), packed pairs written over the scores; the
+            // next chunk's scores load while this chunk's exponentials run
             float ls0 = 0.f, ls1 = 0.f;
             const float nm = -m;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t sr[32];
-                tc::tmem_ld32(my_s + cb * 32, sr);
-                tc::tmem_wait_ld();
+            uint32_t sa[32], sb[32];
+            tc::tmem_ld32(my_s, sa);
+            tc::tmem_wait_ld();
+            auto exps = [&](const uint32_t (&sr)[32], int cb) {
                 uint32_t pk[16];
                 if (!diag) {
 #pragma unroll
@@ -349,7 +347,17 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                     }
                 }
                 tc::tmem_st16(my_s + cb * 16, pk);
-            }
+            };
+            tc::tmem_ld32(my_s + 32, sb);
+            exps(sa, 0);
+            tc::tmem_wait_ld();
+            tc::tmem_ld32(my_s + 64, sa);
+            exps(sb, 1);
+            tc::tmem_wait_ld();
+            tc::tmem_ld32(my_s + 96, sb);
+            exps(sa, 2);
+            tc::tmem_wait_ld();
+            exps(sb, 3);
             tc::tmem_wait_st();
             l = l * alpha + (ls0 + ls1);
             // final tile: V rows past the last key are zeroed (P is 0 there; stale pool
