@@ -432,13 +432,20 @@ def main():
         if not args.no_prefill and dist_ctx.rank == 0:
             pf = time_prefill(device)
             one = pf["one_shot_8192"]
+            ch = pf["chunks_4x2048"]
+            kern_tflops = one["flops"] / one["main_kernel_ms"] / 1e9
             line["prefill_chunk"] = {
                 "workload": "causal prefill S=8192, 32 q / 8 kv heads, d 128, bf16, pages; "
                             "one shot and 4 x 2048 chunks",
-                "one_shot_tflops": one["tflops"], "chunked_tflops": pf["chunks_4x2048"]["tflops"],
-                "one_shot_ms": one["ms"], "chunked_ms": pf["chunks_4x2048"]["ms"],
+                "one_shot_tflops": one["tflops"], "chunked_tflops": ch["tflops"],
+                "one_shot_ms": one["ms"], "chunked_ms": ch["ms"],
                 "flops": one["flops"], "peak_tflops": bf16, "frac": one["tflops"] / bf16,
-                "peak_source": peak_src + " bf16_tflops (burst)"}
+                "peak_source": peak_src + " bf16_tflops (burst)",
+                "roofline": {"bound": "tensor", "kernel": "prefill_pair_kernel",
+                             "achieved": kern_tflops, "peak": bf16, "unit": "TFLOP/s",
+                             "frac": kern_tflops / bf16, "ms_per_launch": one["main_kernel_ms"],
+                             "flops_per_launch": one["flops"],
+                             "chunked_kernel_tflops": ch["flops"] / ch["main_kernel_ms"] / 1e9}}
         if not args.no_cpu_baseline and dist_ctx.rank == 0:
             secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
             line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores,

@@ -65,7 +65,8 @@ thread_local cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr
 
 pkv::WorkspaceLayout layout_for(const pkv_step_desc* d, int num_sms) {
     return pkv::workspace_layout(d->num_reqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
-                                 d->total_q_tokens, d->max_q_len, num_sms, prefill_min_q());
+                                 d->total_q_tokens, d->max_q_len, d->max_context_len, num_sms,
+                                 prefill_min_q());
 }
 
 }  // namespace
@@ -105,6 +106,7 @@ int pkv_kv_append(const pkv_step_desc* desc, const void* k_new, const void* v_ne
     a.num_pages = desc->num_pages;
     a.max_pages = desc->max_pages_per_req;
     a.total_q_tokens = desc->total_q_tokens;
+    a.max_q_len = desc->max_q_len;
     a.q_lens = desc->q_lens;
     a.q_offsets = desc->q_offsets;
     a.context_lens = desc->context_lens;

@@ -110,6 +110,16 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
         : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels of one step are launched so each may start while its predecessor drains.
+// pdl_wait: block until every preceding kernel in the stream has completed and its memory
+// is visible (a no-op for a launch without the attribute).  pdl_trigger: allow the next
+// kernel in the stream to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 

@@ -7,14 +7,17 @@
 // §6.3: with grouped-query attention several query heads share one KV head (here they are
 // processed together, so each K/V byte is read once per KV head, not once per query head).
 //
-// Work item = (request, row, KV head, split).  A split is a run of pages of one request;
-// a CTA of four warps takes one item at a time from a device work queue.  Each warp owns
-// every fourth page of the item and a private ring of 3 stages; a page's K block and V
-// block (16 x D each, contiguous in the pool) arrive through two 1-D bulk async copies on
-// one mbarrier.  Scores stay in base-2 units (q is pre-scaled by scale * log2 e) and an
-// online softmax keeps (running max, running sum, un-normalised output) per query head.
-// The four warps merge in shared memory; a request split over several items leaves
-// partial results that the combine kernel reduces with the same rescaling.
+// Rows of requests that advance by fewer than `prefill_min_q` tokens are decode rows; each
+// row i of such a request attends keys 0..ctx+i.  Work item = (decode row, KV head, split),
+// a split being an even share of the row's pages.  Every warp is an independent worker:
+// it takes items from a device queue, streams each page's K block and V block (16 x D
+// each, contiguous in the pool) through a private 3-stage shared-memory ring with 1-D bulk
+// async copies, and starts the next item's first pages while finishing the current one so
+// the copy pipeline never drains.  Scores stay in base-2 units (q is pre-scaled by
+// scale * log2 e); an online softmax keeps (running max, running sum, un-normalised output)
+// per query head.  A row with one split is normalised and written directly; otherwise each
+// split leaves its partial (m, l, O) in a fixed slot and the combine kernel reduces them:
+// m* = max m_s, l* = sum l_s 2^(m_s - m*), O = sum O_s 2^(m_s - m*) / l*.
 #include <algorithm>
 #include <climits>
 
@@ -29,176 +32,188 @@ constexpr int kPlanThreads = 1024;
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kStages = 3;
-constexpr int kMinSplitPages = 8;
-constexpr int kItemsPerSm = 8;  // target decode items per SM when choosing the split size
+constexpr int kMinSplitPages = 4;
+constexpr int kItemsPerWarp = 6;  // target decode items per resident warp
 
-__device__ __forceinline__ int4* ws_req_info(const StepArgs& a) {
-    return reinterpret_cast<int4*>(a.ws + a.lay.req_info);
-}
-__device__ __forceinline__ int4* ws_items(const StepArgs& a) {
-    return reinterpret_cast<int4*>(a.ws + a.lay.items);
-}
-__device__ __forceinline__ int4* ws_tiles(const StepArgs& a) {
-    return reinterpret_cast<int4*>(a.ws + a.lay.tiles);
-}
-__device__ __forceinline__ int32_t* ws_ctrl(const StepArgs& a) {
-    return reinterpret_cast<int32_t*>(a.ws + a.lay.ctrl);
+template <typename T>
+__device__ __forceinline__ T* ws_at(const StepArgs& a, size_t off) {
+    return reinterpret_cast<T*>(a.ws + off);
 }
 
-// Exclusive block-wide scan of one int per thread (blockDim.x == kPlanThreads).
-__device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = s_warp[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFull, w, o);
-            if (lane >= o) w += y;
-        }
-        s_warp[lane] = w;  // inclusive over warps
-    }
-    __syncthreads();
-    const int before = (warp ? s_warp[warp - 1] : 0) + x - v;
-    *total = s_warp[31];
-    __syncthreads();
-    return before;
+// Request r is valid for this step when its lengths agree with q_offsets and the host maxima.
+__device__ __forceinline__ bool request_ok(const StepArgs& a, int r, int q, int c) {
+    return q >= 0 && c >= 0 && q <= a.max_q_len && c <= a.max_context_len &&
+           a.q_offsets[r + 1] - a.q_offsets[r] == q;
 }
 
 }  // namespace
 
 // ------------------------------------------------------------------------------------
-// plan: validate per-request lengths, choose the split size, number the work.
-// One CTA.  Requests with q_len == 1 become split items (first, so their partial results
-// are indexed by item), rows of requests with 1 < q_len < prefill_min_q become one item
-// per (row, KV head), requests with q_len >= prefill_min_q become prefill tiles
-// (q tile of 128 rows, query head), longest first.
+// plan: validate lengths, choose the split size, number decode rows, decode items and
+// prefill tiles.  One CTA; per-request values of a chunk of 1024 requests live in shared
+// memory so each phase reads global memory at most once.
 // ------------------------------------------------------------------------------------
+namespace {
+// exclusive block-wide scan of three ints per thread at once
+struct Int3 { int x, y, z; };
+__device__ Int3 block_exclusive_scan3(Int3 v, Int3* total, Int3* s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    Int3 x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yx = __shfl_up_sync(kFull, x.x, o), yy = __shfl_up_sync(kFull, x.y, o),
+                  yz = __shfl_up_sync(kFull, x.z, o);
+        if (lane >= o) { x.x += yx; x.y += yy; x.z += yz; }
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        Int3 w = s_warp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yx = __shfl_up_sync(kFull, w.x, o), yy = __shfl_up_sync(kFull, w.y, o),
+                      yz = __shfl_up_sync(kFull, w.z, o);
+            if (lane >= o) { w.x += yx; w.y += yy; w.z += yz; }
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    const Int3 before = warp ? s_warp[warp - 1] : Int3{0, 0, 0};
+    *total = s_warp[31];
+    __syncthreads();
+    return Int3{before.x + x.x - v.x, before.y + x.y - v.y, before.z + x.z - v.z};
+}
+}  // namespace
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
     __shared__ unsigned long long s_sum;
-    __shared__ int s_max, s_split, s_bad;
-    __shared__ int s_warp[32];
-    const int tid = threadIdx.x;
-    int32_t* ctrl = ws_ctrl(a);
-    int4* info = ws_req_info(a);
+    __shared__ int s_bad, s_split;
+    __shared__ Int3 s_warp3[32];
+    __shared__ int s_q[kPlanThreads], s_c[kPlanThreads], s_t0[kPlanThreads];
+    __shared__ int s_row0[kPlanThreads], s_item0[kPlanThreads], s_tile0[kPlanThreads];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
+    int4* rows = ws_at<int4>(a, a.lay.rows);
+    int4* items = ws_at<int4>(a, a.lay.items);
+    int4* tiles = ws_at<int4>(a, a.lay.tiles);
+    const int Hkv = a.num_kv_heads;
+    const int slots = a.num_q_heads / a.heads_per_tile;
     if (tid == 0) {
         s_sum = 0;
-        s_max = 0;
         s_bad = (a.q_offsets[0] != 0 || a.q_offsets[a.num_reqs] != a.total_q_tokens);
     }
     __syncthreads();
-    const int Hkv = a.num_kv_heads;
+
+    // ---- pass A: validity and the decode page total (sets the split size)
     unsigned long long my_sum = 0;
-    int my_max = 0;
     for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
         const int q = a.q_lens[r], c = a.context_lens[r];
-        const bool ok = q >= 0 && c >= 0 && q <= a.max_q_len && c <= a.max_context_len &&
-                        a.q_offsets[r + 1] - a.q_offsets[r] == q;
-        if (!ok) { atomicOr(&s_bad, 1); continue; }
-        const int pages = cdiv(c + q, kPage);
-        if (pages > a.max_pages) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
-        if (q == 1) {
-            my_sum += pages;
-            my_max = max(my_max, pages);
-        }
+        if (!request_ok(a, r, q, c)) { atomicOr(&s_bad, 1); continue; }
+        if (cdiv(c + q, kPage) > a.max_pages) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
+        if (q >= 1 && q < a.prefill_min_q)
+            for (int i = 0; i < q; ++i) my_sum += cdiv(c + i + 1, kPage);
     }
-    atomicAdd(&s_sum, my_sum);
-    atomicMax(&s_max, my_max);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) my_sum += __shfl_xor_sync(kFull, my_sum, o);
+    if (lane == 0 && my_sum) atomicAdd(&s_sum, my_sum);
     __syncthreads();
     const bool bad = s_bad != 0;
     if (tid == 0) {
         if (bad) set_error(a.err, PKV_DEVERR_TOKENS);
-        const long long target = static_cast<long long>(kItemsPerSm) * a.num_sms;
-        long long sp = kMinSplitPages;
-        sp = max(sp, static_cast<long long>(cdiv(s_max, a.lay.max_splits)));
-        sp = max(sp, static_cast<long long>((s_sum * Hkv + target - 1) / target));
-        sp = (sp + kDecWarps - 1) / kDecWarps * kDecWarps;
-        s_split = static_cast<int>(min(sp, static_cast<long long>(INT_MAX / 2)));
+        const unsigned long long heads = s_sum * static_cast<unsigned long long>(Hkv);
+        const unsigned long long tgt = static_cast<unsigned long long>(a.lay.target_items);
+        const unsigned long long sp = (heads + tgt - 1) / tgt;
+        s_split = static_cast<int>(max(sp, static_cast<unsigned long long>(kMinSplitPages)));
     }
     __syncthreads();
     const int sp = s_split;
 
-    // three numbering passes: split items, row items, prefill tiles
-    int carry_split = 0, carry_items = 0, carry_tiles = 0;
-    for (int pass = 0; pass < 3; ++pass) {
-        int carry = pass == 2 ? 0 : carry_items;
-        for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
-            const int r = base + tid;
-            int n = 0, q = 0, pages = 0;
-            if (r < a.num_reqs && !bad) {
-                q = a.q_lens[r];
-                const int c = a.context_lens[r];
-                const bool ok = q >= 0 && c >= 0 && q <= a.max_q_len && c <= a.max_context_len &&
-                                a.q_offsets[r + 1] - a.q_offsets[r] == q;
-                if (!ok) q = 0;
-                pages = cdiv(c + q, kPage);
-                if (pass == 0 && q == 1) n = Hkv * cdiv(pages, sp);
-                if (pass == 1 && q > 1 && q < a.prefill_min_q) n = Hkv * q;
-                if (pass == 2 && q >= a.prefill_min_q && q > 1)
-                    n = cdiv(q, 128) * (a.num_q_heads / a.heads_per_tile);
+    // ---- per chunk: count, scan, then fill rows / items / tiles (warp per request)
+    Int3 carry{0, 0, 0};
+    bool overflow = false;
+    for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
+        const int r = base + tid;
+        int q = 0, c = 0;
+        Int3 n{0, 0, 0};  // decode rows, decode items, prefill tiles of request r
+        if (r < a.num_reqs && !bad) {
+            q = a.q_lens[r];
+            c = a.context_lens[r];
+            if (!request_ok(a, r, q, c)) q = 0;
+            if (q >= 1 && q < a.prefill_min_q) {
+                n.x = q;
+                for (int i = 0; i < q; ++i) n.y += Hkv * cdiv(cdiv(c + i + 1, kPage), sp);
             }
-            int total;
-            const int ex = block_exclusive_scan(n, &total, s_warp);
-            if (r < a.num_reqs) {
-                if (pass == 0) info[r] = make_int4(carry + ex, q == 1 ? cdiv(pages, sp) : 0, q, 0);
-                if (pass == 1 && n) info[r].x = carry + ex;
-                if (pass == 1 && q > 1) info[r].y = 1;
-                if (pass == 2 && n) info[r].w = carry + ex;
-            }
-            carry += total;
+            if (q > 1 && q >= a.prefill_min_q) n.z = cdiv(q, 128) * slots;
         }
-        if (pass == 0) carry_split = carry;
-        if (pass < 2) carry_items = carry; else carry_tiles = carry;
-    }
-    if (carry_items > a.lay.max_items || carry_tiles > a.lay.max_tiles ||
-        carry_split > a.lay.max_split_items) {  // cannot happen when the host maxima hold
-        if (tid == 0) set_error(a.err, PKV_DEVERR_TOKENS);
-        carry_items = carry_tiles = carry_split = 0;
-    }
-    __syncthreads();
-
-    // fill the item and tile lists: one warp per request, lanes over its items
-    const int lane = tid & 31, warp = tid >> 5;
-    int4* items = ws_items(a);
-    int4* tiles = ws_tiles(a);
-    if (carry_items || carry_tiles) {
-        for (int r = warp; r < a.num_reqs; r += kPlanThreads / 32) {
-            const int4 in = info[r];
-            const int q = in.z;
-            if (q == 1) {
-                const int ns = in.y;
-                for (int i = lane; i < Hkv * ns; i += 32)
-                    items[in.x + i] = make_int4(r, 0, i / ns, i % ns);
-            } else if (q > 1 && q < a.prefill_min_q) {
-                for (int i = lane; i < q * Hkv; i += 32)
-                    items[in.x + i] = make_int4(r, i / Hkv, i % Hkv, 0);
-            } else if (q > 1) {
-                const int nt = cdiv(q, 128);
-                const int slots = a.num_q_heads / a.heads_per_tile;
+        Int3 tot;
+        const Int3 ex = block_exclusive_scan3(n, &tot, s_warp3);
+        overflow = overflow || carry.x + tot.x > a.lay.max_rows ||
+                   carry.y + tot.y > a.lay.max_items || carry.z + tot.z > a.lay.max_tiles;
+        if (r < a.num_reqs) {
+            s_q[tid] = q;
+            s_c[tid] = c;
+            s_t0[tid] = r < a.num_reqs ? a.q_offsets[r] : 0;
+            s_row0[tid] = carry.x + ex.x;
+            s_item0[tid] = carry.y + ex.y;
+            s_tile0[tid] = carry.z + ex.z;
+        }
+        __syncthreads();
+        const int nreq = min(kPlanThreads, a.num_reqs - base);
+        for (int k = warp; !overflow && k < nreq; k += kPlanThreads / 32) {
+            const int rq = base + k, qk = s_q[k], ck = s_c[k];
+            if (qk >= 1 && qk < a.prefill_min_q) {
+                // rows of this request (qk <= 31): lane i = row i; warp scan of item counts
+                const int ns = lane < qk ? cdiv(cdiv(ck + lane + 1, kPage), sp) : 0;
+                int incl = Hkv * ns;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int first = s_item0[k] + incl - Hkv * ns;
+                if (lane < qk) {
+                    rows[s_row0[k] + lane] = make_int4(s_t0[k] + lane, first, ck + lane + 1, ns);
+                }
+                for (int i = 0; i < qk; ++i) {
+                    const int ns_i = __shfl_sync(kFull, ns, i);
+                    const int first_i = __shfl_sync(kFull, first, i);
+                    const int nkv = ck + i + 1, pages = cdiv(nkv, kPage);
+                    const int t = s_t0[k] + i;
+                    for (int e = lane; e < Hkv * ns_i; e += 32) {
+                        const int g = e / ns_i, s_ = e % ns_i;
+                        const int pb = static_cast<int>(static_cast<long long>(s_) * pages / ns_i);
+                        const int pe = static_cast<int>(static_cast<long long>(s_ + 1) * pages / ns_i);
+                        const int pos = first_i + e;  // = slot: splits of a (row, head) adjacent
+                        items[2 * pos] = make_int4(t, g | (s_ << 16), pb, pe - pb);
+                        items[2 * pos + 1] = make_int4(nkv, ns_i, rq, first_i + g * ns_i);
+                    }
+                }
+            } else if (qk > 1) {
+                const int nt = cdiv(qk, 128);
                 for (int i = lane; i < nt * slots; i += 32)
-                    tiles[in.w + i] = make_int4(r, nt - 1 - i / slots, i % slots, 0);
+                    tiles[s_tile0[k] + i] = make_int4(rq, nt - 1 - i / slots, i % slots, 0);
             }
         }
+        carry = Int3{carry.x + tot.x, carry.y + tot.y, carry.z + tot.z};
+        __syncthreads();
     }
+    // the plan ran alongside this step's kv_append; finish only after it (so a kernel that
+    // waits for the plan also sees the appended K/V), then let the attention kernels start
+    pdl_wait();
+    pdl_trigger();
     if (tid == 0) {
+        if (overflow) set_error(a.err, PKV_DEVERR_TOKENS);  // host maxima were wrong
         ctrl[0] = 0;
-        ctrl[1] = carry_items;
-        ctrl[2] = carry_split;
+        ctrl[1] = overflow ? 0 : carry.y;
+        ctrl[2] = overflow ? 0 : carry.x;
         ctrl[3] = sp;
         ctrl[8] = 0;
-        ctrl[9] = carry_tiles;
+        ctrl[9] = overflow ? 0 : carry.z;
     }
 }
 
 // ------------------------------------------------------------------------------------
-// decode: persistent CTAs pull items; see the file comment for the data flow.
+// decode: independent warps pull items; see the file comment for the data flow.
 // ------------------------------------------------------------------------------------
 template <typename T, int D, int G>
 struct DecodeSmem {
@@ -206,9 +221,15 @@ struct DecodeSmem {
     static constexpr int kStageBytes = 2 * kPageBytes;
     static constexpr int kRing = kDecWarps * kStages * kStageBytes;
     static constexpr int kPbuf = kDecWarps * kPage * G * 4;
-    static constexpr int kMerge = kDecWarps * G * (D + 2) * 4;
     static constexpr int kBars = kDecWarps * kStages * 8;
-    static constexpr int kBytes = kRing + kPbuf + kMerge + kBars + 16;
+    static constexpr int kBytes = kRing + kPbuf + kBars;
+};
+
+// One work item as a warp sees it.
+struct DecItem {
+    int idx;        // queue position; >= count when none
+    int t, g, s, pb, np;   // token of the row in the step, KV head, split, first page, pages
+    int nkv, ns, r, base;  // keys of the row, splits of the row, request, slot of split 0
 };
 
 template <typename T, int D, int G>
@@ -225,114 +246,169 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* ring = smem + warp * kStages * S::kStageBytes;
     float* pbuf = reinterpret_cast<float*>(smem + S::kRing) + warp * kPage * G;
-    float* merge = reinterpret_cast<float*>(smem + S::kRing + S::kPbuf);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing + S::kPbuf + S::kMerge) +
-                     warp * kStages;
-    int* s_item = reinterpret_cast<int*>(smem + S::kRing + S::kPbuf + S::kMerge + S::kBars);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing + S::kPbuf) + warp * kStages;
 
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
     __syncwarp();
+    pdl_wait();     // the plan (and through it this step's kv_append) has completed
+    pdl_trigger();  // the combine may be scheduled; it waits for this grid to finish
 
-    const int32_t* ctrl = ws_ctrl(a);
+    int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
     const int num_items = ctrl[1];
-    const int sp = ctrl[3];
-    const int4* items = ws_items(a);
-    const int4* info = ws_req_info(a);
-    float2* part_ml = reinterpret_cast<float2*>(a.ws + a.lay.part_ml);
-    float* part_o = reinterpret_cast<float*>(a.ws + a.lay.part_o);
+    const int4* items = ws_at<const int4>(a, a.lay.items);
+    float2* part_ml = ws_at<float2>(a, a.lay.part_ml);
+    float* part_o = ws_at<float>(a, a.lay.part_o);
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads;
+    const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
+    const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
     const int c8 = lane & 7, tg = lane >> 3;
     const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
     const int swz = (c8 >> 2) & 1;  // staggered chunk order: conflict-free 16-byte loads
     const int my_tok = tg * 4 + 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0);  // token of my reduced scores
 
-    uint32_t issued = 0, consumed = 0;  // per-warp ring counters (persist across items)
+    // ---- item metadata moves through a pipeline so no dependent load sits on the critical
+    //      path: queue index claimed 3 items ahead, record loaded 2 ahead, page ids and q 1
+    //      ahead; each load is consumed one item switch after it was issued.
+    auto resolve = [&](int idx, const int4& ra, const int4& rb) {
+        DecItem it;
+        it.idx = idx;
+        it.t = ra.x; it.g = ra.y & 0xffff; it.s = ra.y >> 16; it.pb = ra.z; it.np = ra.w;
+        it.nkv = rb.x; it.ns = rb.y; it.r = rb.z; it.base = rb.w;
+        if (idx >= num_items) it.np = 0;
+        return it;
+    };
+    auto load_record = [&](int idx, int4& ra, int4& rb) {
+        if (idx < num_items) {
+            ra = items[2 * idx];
+            rb = items[2 * idx + 1];
+        } else {
+            ra = make_int4(0, 0, 0, 0);
+            rb = make_int4(0, 1, 0, 0);
+        }
+    };
+    // lane l: physical id of page pb + w + l
+    auto load_window = [&](const DecItem& it, int w) {
+        int phys = 0;
+        const int i = w + lane;
+        if (i < it.np) {
+            const int lp = it.pb + i;
+            if (lp < a.max_pages) {
+                phys = __ldg(a.block_table + static_cast<int64_t>(it.r) * a.max_pages + lp);
+                if (phys < 0 || phys >= a.num_pages) {
+                    set_error(a.err, PKV_DEVERR_PAGE_RANGE);
+                    phys = 0;
+                }
+            } else {
+                set_error(a.err, PKV_DEVERR_TABLE_RANGE);
+            }
+        }
+        return phys;
+    };
+    // raw q of the G query heads of an item, my q.k dims (staggered chunk order)
+    auto load_q = [&](const DecItem& it, uint4 (&qr)[G][NCH]) {
+        if (it.np == 0) return;
+        const uint16_t* qbase = static_cast<const uint16_t*>(a.q) +
+                                (static_cast<int64_t>(it.t) * Hq + it.g * G) * D + c8 * QKD;
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int ci = 0; ci < NCH; ++ci)
+                qr[j][ci] = __ldg(reinterpret_cast<const uint4*>(qbase + j * D) +
+                                  (ci ^ (NCH == 2 ? swz : 0)));
+    };
+    auto claim = [&]() {  // lane 0 holds the claimed index; read it with __shfl_sync later
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(&ctrl[0], 1);
+        return idx;
+    };
+
+    // prime the pipeline
+    const int i0 = __shfl_sync(kFull, claim(), 0);
+    const int i1 = __shfl_sync(kFull, claim(), 0);
+    int4 ra, rb;
+    load_record(i0, ra, rb);
+    DecItem cur = resolve(i0, ra, rb);
+    load_record(i1, ra, rb);
+    DecItem nxt = resolve(i1, ra, rb);
+    int cur_win = load_window(cur, 0), cur_win_base = 0;
+    int nxt_win = load_window(nxt, 0);
+    // the next item's q is prefetched when the registers allow (not for 8 x 128-dim heads)
+    constexpr bool kPrefetchQ = G * NCH <= 8;
+    uint4 q_cur[G][NCH], q_nxt[kPrefetchQ ? G : 1][kPrefetchQ ? NCH : 1];
+    load_q(cur, q_cur);
+    if constexpr (kPrefetchQ) load_q(nxt, q_nxt);
+    int p2_idx = __shfl_sync(kFull, claim(), 0);
+    int4 p2a, p2b;
+    load_record(p2_idx, p2a, p2b);
+    int p3_lane0 = claim();
+    uint32_t issued = 0, consumed = 0;  // ring counters
     bool aborted = false;
-    if (threadIdx.x == 0) s_item[1] = 0;
+    int ic = 0;          // pages of `cur` issued so far
+    int in_nxt = 0;      // pages of `nxt` issued ahead (at most its first window)
+    // issue one page into the ring: `cur` first, then the head of `nxt` (whole warp)
+    auto issue_one = [&]() {
+        int win, lidx, g;
+        if (ic < cur.np) {
+            if (ic >= cur_win_base + 32) {
+                cur_win_base += 32;
+                cur_win = load_window(cur, cur_win_base);
+            }
+            win = cur_win;
+            lidx = ic - cur_win_base;
+            g = cur.g;
+            ++ic;
+        } else if (in_nxt < nxt.np && in_nxt < 32) {
+            win = nxt_win;
+            lidx = in_nxt;
+            g = nxt.g;
+            ++in_nxt;
+        } else {
+            return;
+        }
+        const int phys = __shfl_sync(kFull, win, lidx);
+        if (lane == 0) {
+            const int stage = issued % kStages;
+            uint8_t* dst = ring + stage * S::kStageBytes;
+            const int64_t off = (static_cast<int64_t>(phys) * Hkv + g) * (kPage * D);
+            mbar_arrive_expect_tx(&bars[stage], 2 * S::kPageBytes);
+            bulk_g2s(dst, kc + off, S::kPageBytes, &bars[stage]);
+            bulk_g2s(dst + S::kPageBytes, vc + off, S::kPageBytes, &bars[stage]);
+        }
+        ++issued;
+    };
+    for (int k = 0; k < kStages; ++k) issue_one();
 
-    for (;;) {
-        if (threadIdx.x == 0) s_item[0] = atomicAdd(const_cast<int32_t*>(ctrl), 1);
-        __syncthreads();
-        const int item = s_item[0];
-        if (item >= num_items || s_item[1]) break;  // s_item[1]: some warp gave up waiting
-        const int4 it = items[item];
-        const int r = it.x, row = it.y, g = it.z, split = it.w;
-        const int4 in = info[r];
-        const int nsplit = in.y;
-        const int ctx = a.context_lens[r];
-        const int t = a.q_offsets[r] + row;
-        const int nkv = ctx + row + 1;                // keys 0..pos inclusive
-        const int npages = cdiv(nkv, kPage);
-        // q_len == 1 requests are cut into splits of sp pages; a row of a longer request
-        // is one item over all of its pages
-        const int pb = split * sp;
-        const int pe = in.z == 1 ? min(npages, pb + sp) : npages;
-        const int n_mine = pe - pb > warp ? cdiv(pe - pb - warp, kDecWarps) : 0;
-        const int32_t* bt_row = a.block_table + static_cast<int64_t>(r) * a.max_pages;
-
+    // output row of (token t, KV head g): lanes write DPL dims of each of the G heads
+    auto store_row = [&](int t, int g, int j, const float (&res)[DPL]) {
+        uint16_t* out_row = static_cast<uint16_t*>(a.out) +
+                            (static_cast<int64_t>(t) * Hq + g * G + j) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+            *reinterpret_cast<uint2*>(out_row) =
+                make_uint2(Cv::pack(res[0], res[1]), Cv::pack(res[2], res[3]));
+        } else {
+            *reinterpret_cast<uint32_t*>(out_row) = Cv::pack(res[0], res[1]);
+        }
+    };
+    while (cur.np > 0 && !aborted) {
         // query heads g*G .. g*G+G-1, my q.k dims, pre-scaled into base-2 units
         float qf[G][QKD];
-        {
-            const uint16_t* qbase = static_cast<const uint16_t*>(a.q) +
-                                    (static_cast<int64_t>(t) * Hq + g * G) * D + c8 * QKD;
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
+        for (int j = 0; j < G; ++j) {
 #pragma unroll
-                for (int ci = 0; ci < NCH; ++ci) {
-                    const uint4 w = __ldg(reinterpret_cast<const uint4*>(qbase + j * D) + (ci ^ (NCH == 2 ? swz : 0)));
-                    const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+            for (int ci = 0; ci < NCH; ++ci) {
+                const uint32_t ws4[4] = {q_cur[j][ci].x, q_cur[j][ci].y, q_cur[j][ci].z,
+                                         q_cur[j][ci].w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = Cv::unpack(ws4[e]);
-                        qf[j][ci * 8 + 2 * e] = f.x * a.scale_log2;
-                        qf[j][ci * 8 + 2 * e + 1] = f.y * a.scale_log2;
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = Cv::unpack(ws4[e]);
+                    qf[j][ci * 8 + 2 * e] = f.x * a.scale_log2;
+                    qf[j][ci * 8 + 2 * e + 1] = f.y * a.scale_log2;
                 }
             }
         }
-
-        // physical page ids of my first 32 pages (lane i holds page i of this warp)
-        auto load_window = [&](int first) -> int {
-            const int i = first + lane;
-            int phys = 0;
-            if (i < n_mine) {
-                const int lp = pb + warp + i * kDecWarps;
-                if (lp < a.max_pages) {
-                    phys = __ldg(bt_row + lp);
-                    if (phys < 0 || phys >= a.num_pages) {
-                        set_error(a.err, PKV_DEVERR_PAGE_RANGE);
-                        phys = 0;
-                    }
-                } else {
-                    set_error(a.err, PKV_DEVERR_TABLE_RANGE);
-                }
-            }
-            return phys;
-        };
-        int window = load_window(0);
-        int window_base = 0;
-        const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
-        const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
-        auto issue = [&](int i) {  // whole warp calls; lane 0 issues
-            if (i >= window_base + 32) {
-                window_base += 32;
-                window = load_window(window_base);
-            }
-            const int phys = __shfl_sync(kFull, window, i - window_base);
-            if (lane == 0) {
-                const int stage = issued % kStages;
-                uint8_t* dst = ring + stage * S::kStageBytes;
-                const int64_t off = (static_cast<int64_t>(phys) * Hkv + g) * (kPage * D);
-                mbar_arrive_expect_tx(&bars[stage], 2 * S::kPageBytes);
-                bulk_g2s(dst, kc + off, S::kPageBytes, &bars[stage]);
-                bulk_g2s(dst + S::kPageBytes, vc + off, S::kPageBytes, &bars[stage]);
-            }
-            ++issued;
-        };
-
         float m[G], o[G][DPL], lsum[NV];
 #pragma unroll
         for (int j = 0; j < G; ++j) {
@@ -343,13 +419,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 #pragma unroll
         for (int i = 0; i < NV; ++i) lsum[i] = 0.f;
 
-        const int prologue = min(kStages, n_mine);
-        for (int i = 0; i < prologue; ++i) issue(i);
-
-        for (int i = 0; i < n_mine; ++i) {
+        for (int i = 0; i < cur.np; ++i) {
             const int stage = consumed % kStages;
-            const uint32_t parity = (consumed / kStages) & 1;
-            if (!mbar_wait(&bars[stage], parity)) {
+            if (!mbar_wait_warp(&bars[stage], (consumed / kStages) & 1)) {
                 if (lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
                 aborted = true;
                 break;
@@ -357,9 +429,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             ++consumed;
             const uint8_t* sK = ring + stage * S::kStageBytes;
             const uint8_t* sV = sK + S::kPageBytes;
-            const int lp = pb + warp + i * kDecWarps;
-            const int nvalid = min(kPage, nkv - lp * kPage);
-
+            const int nvalid = min(kPage, cur.nkv - (cur.pb + i) * kPage);
             // ---- scores: lane (tg, c8) does tokens tg*4..tg*4+3 over dims c8*QKD..+QKD
             float v[N0];
 #pragma unroll
@@ -487,18 +557,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 for (int tok = 0; tok < nvalid; ++tok) pv_token(tok);
             }
             __syncwarp();
-            if (i + kStages < n_mine) issue(i + kStages);
+            issue_one();  // refill the stage just freed
         }
-        if (aborted) {  // drain what this warp still has in flight, bounded
-            if (lane == 0) s_item[1] = 1;
-            while (consumed < issued) {
-                const int stage = consumed % kStages;
-                mbar_wait(&bars[stage], (consumed / kStages) & 1);
-                ++consumed;
-            }
-        }
+        if (aborted) break;
 
-        // ---- warp totals: sum lsum over the token lanes, gather every head
+        // ---- totals of this split: sum lsum over the token lanes, gather every head
         float lh[G];
 #pragma unroll
         for (int i2 = 0; i2 < NV; ++i2) {
@@ -515,112 +578,124 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 lh[NV + i2] = b0 ? x : other;
             }
         }
-        float* mw = merge + warp * G * (D + 2);
+        if (cur.ns == 1) {
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
+            for (int j = 0; j < G; ++j) {
+                float res[DPL];
+                const float inv = 1.f / lh[j];
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) mw[j * (D + 2) + lane * DPL + e] = o[j][e];
-            if (lane == 0) {
-                mw[j * (D + 2) + D] = m[j];
-                mw[j * (D + 2) + D + 1] = lh[j];
+                for (int e = 0; e < DPL; ++e) res[e] = o[j][e] * inv;
+                store_row(cur.t, cur.g, j, res);
+            }
+        } else {
+            // leave this split's partial for the combine kernel (plain stores: the next
+            // launch on the stream sees them)
+            const int64_t slot = static_cast<int64_t>(cur.base) + cur.s;
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                float* po = part_o + (slot * G + j) * D + lane * DPL;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) po[e] = o[j][e];
+                if (lane == 0) part_ml[slot * G + j] = make_float2(m[j], lh[j]);
             }
         }
-        __syncthreads();
 
-        // ---- merge the four warps; finish the row or leave a partial for the combine
-        for (int idx = threadIdx.x; idx < G * D; idx += kDecThreads) {
-            const int j = idx / D, d = idx % D;
-            float M = -1e30f;
+        // ---- advance the metadata pipeline; `nxt`'s first pages are already in flight
+        cur = nxt;
+        cur_win = nxt_win;
+        cur_win_base = 0;
+        if constexpr (kPrefetchQ) {
 #pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, merge[(w * G + j) * (D + 2) + D]);
-            float L = 0.f, O = 0.f;
+            for (int j = 0; j < G; ++j)
 #pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) {
-                const float* mr = merge + (w * G + j) * (D + 2);
-                const float sc = fast_exp2(mr[D] - M);
-                L = fmaf(mr[D + 1], sc, L);
-                O = fmaf(mr[d], sc, O);
-            }
-            if (nsplit <= 1) {
-                const float res = O / L;
-                uint16_t* op = static_cast<uint16_t*>(a.out) +
-                               (static_cast<int64_t>(t) * Hq + g * G + j) * D + d;
-                const uint32_t packed = Cv::pack(res, 0.f);
-                *op = static_cast<uint16_t>(packed & 0xffffu);
-            } else {
-                part_o[(static_cast<int64_t>(item) * G + j) * D + d] = O;
-                if (d == 0) part_ml[static_cast<int64_t>(item) * G + j] = make_float2(M, L);
-            }
+                for (int ci = 0; ci < NCH; ++ci) q_cur[j][ci] = q_nxt[j][ci];
+        } else {
+            load_q(cur, q_cur);
         }
-        __syncthreads();
+        ic = in_nxt;
+        in_nxt = 0;
+        nxt = resolve(p2_idx, p2a, p2b);
+        nxt_win = load_window(nxt, 0);
+        if constexpr (kPrefetchQ) load_q(nxt, q_nxt);
+        p2_idx = __shfl_sync(kFull, p3_lane0, 0);
+        load_record(p2_idx, p2a, p2b);
+        p3_lane0 = claim();
+        while (issued - consumed < static_cast<uint32_t>(kStages)) {
+            const uint32_t before = issued;
+            issue_one();
+            if (issued == before) break;
+        }
+    }
+    // drain copies still in flight (only after an abort), bounded
+    while (consumed < issued) {
+        mbar_wait_warp(&bars[consumed % kStages], (consumed / kStages) & 1);
+        ++consumed;
     }
 }
 
 // ------------------------------------------------------------------------------------
-// combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s for split requests.
-// One CTA per (request, KV head); requests with a single split were finished in place.
+// combine: one CTA per (decode row, KV head) with more than one split, one thread per
+// (query head, 4 dims); every split's loads are independent so they overlap:
+//   m* = max_s m_s,  l* = sum_s l_s 2^(m_s - m*),  out = sum_s O_s 2^(m_s - m*) / l*
 // ------------------------------------------------------------------------------------
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) combine_kernel(StepArgs a) {
+__global__ void __launch_bounds__(G * D / 4) combine_kernel(StepArgs a) {
     using Cv = F16<T>;
-    constexpr int kMaxSplitsSmem = 64;
-    __shared__ float s_w[G][kMaxSplitsSmem];
-    __shared__ float s_inv_l[G];
-    const int r = blockIdx.x / a.num_kv_heads, g = blockIdx.x % a.num_kv_heads;
-    const int4 in = ws_req_info(a)[r];
-    if (in.z != 1 || in.y <= 1) return;
-    const int ns = min(in.y, kMaxSplitsSmem);
-    const int item0 = in.x + g * in.y;
-    if (item0 + ns > ws_ctrl(a)[2]) return;  // the plan dropped the work (bad device data)
-    const float2* part_ml = reinterpret_cast<const float2*>(a.ws + a.lay.part_ml);
-    const float* part_o = reinterpret_cast<const float*>(a.ws + a.lay.part_o);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int j = warp; j < G; j += 4) {
-        float M = -1e30f;
-        for (int s = lane; s < ns; s += 32) M = fmaxf(M, part_ml[(int64_t)(item0 + s) * G + j].x);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float L = 0.f;
-        for (int s = lane; s < ns; s += 32) {
-            const float2 ml = part_ml[(int64_t)(item0 + s) * G + j];
-            const float w = fast_exp2(ml.x - M);
-            s_w[j][s] = w;
-            L = fmaf(ml.y, w, L);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
-        if (lane == 0) s_inv_l[j] = 1.f / L;
+    const int Hkv = a.num_kv_heads;
+    const int d = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
+    pdl_wait();  // the decode kernel has finished writing the partials
+    const int32_t* ctrl = ws_at<const int32_t>(a, a.lay.ctrl);
+    const int4 row = ws_at<const int4>(a, a.lay.rows)[d];  // {token, first slot, keys, splits}
+    if (d >= ctrl[2]) return;
+    const int ns = row.w;
+    if (ns <= 1) return;  // finished in place by the decode kernel
+    const int64_t base = row.y + static_cast<int64_t>(g) * ns;
+    const float2* part_ml = ws_at<const float2>(a, a.lay.part_ml);
+    const float* part_o = ws_at<const float>(a, a.lay.part_o);
+    const int j = threadIdx.x / (D / 4), dim = (threadIdx.x % (D / 4)) * 4;
+    // one pass with a running maximum: acc, L rescaled when a split raises it
+    float M = -1e30f, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s = 0; s < ns; ++s) {
+        const float2 ml = part_ml[(base + s) * G + j];
+        const float4 o = *reinterpret_cast<const float4*>(part_o + ((base + s) * G + j) * D + dim);
+        const float mn = fmaxf(M, ml.x);
+        const float c = fast_exp2(M - mn), w = fast_exp2(ml.x - mn);
+        M = mn;
+        L = fmaf(L, c, ml.y * w);
+        acc.x = fmaf(acc.x, c, o.x * w);
+        acc.y = fmaf(acc.y, c, o.y * w);
+        acc.z = fmaf(acc.z, c, o.z * w);
+        acc.w = fmaf(acc.w, c, o.w * w);
     }
-    __syncthreads();
-    const int t = a.q_offsets[r];
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int j = idx / D, d = idx % D;
-        float O = 0.f;
-        for (int s = 0; s < ns; ++s)
-            O = fmaf(part_o[((int64_t)(item0 + s) * G + j) * D + d], s_w[j][s], O);
-        const float res = O * s_inv_l[j];
-        uint16_t* op = static_cast<uint16_t*>(a.out) +
-                       (static_cast<int64_t>(t) * a.num_q_heads + g * G + j) * D + d;
-        *op = static_cast<uint16_t>(Cv::pack(res, 0.f) & 0xffffu);
-    }
+    const float inv = 1.f / L;
+    const int t = row.x;
+    uint16_t* out = static_cast<uint16_t*>(a.out) +
+                    (static_cast<int64_t>(t) * a.num_q_heads + g * G + j) * D + dim;
+    *reinterpret_cast<uint2*>(out) =
+        make_uint2(Cv::pack(acc.x * inv, acc.y * inv), Cv::pack(acc.z * inv, acc.w * inv));
 }
 
 // ------------------------------------------------------------------------------------
 // host launchers
 // ------------------------------------------------------------------------------------
 WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                 int total_q_tokens, int max_q_len, int num_sms,
-                                 int prefill_min_q) {
+                                 int total_q_tokens, int max_q_len, int max_context_len,
+                                 int num_sms, int prefill_min_q) {
     WorkspaceLayout L{};
     const int G = num_q_heads / num_kv_heads;
-    const int pairs = std::max(1, num_reqs * num_kv_heads);
-    int max_splits = cdiv(2 * kItemsPerSm * num_sms, pairs);
-    max_splits = std::min(64, std::max(4, max_splits));
-    L.max_splits = max_splits;
-    L.max_split_items = num_reqs * num_kv_heads * max_splits;
-    L.max_items = L.max_split_items + total_q_tokens * num_kv_heads;
-    // prefill tiles: none unless some request can reach prefill_min_q tokens; then at most
-    // T/128 full tiles plus one partial tile per prefilling request
+    // decode rows: every row of a request below the prefill threshold
+    L.max_rows = std::min(total_q_tokens,
+                          num_reqs * std::max(0, std::min(max_q_len, prefill_min_q - 1)));
+    L.target_items = 2 * kDecWarps * kItemsPerWarp * num_sms;  // 2 CTAs per SM
+    // pages per split >= total / target, so items <= target + one per (row, KV head);
+    // pages per split >= kMinSplitPages bounds them by the longest row as well
+    const long long row_pages = cdiv(max_context_len + max_q_len, kPage);
+    const long long by_len = static_cast<long long>(L.max_rows) * num_kv_heads *
+                             ((row_pages + kMinSplitPages - 1) / kMinSplitPages);
+    const long long by_target = L.target_items + static_cast<long long>(L.max_rows) * num_kv_heads;
+    L.max_items = L.max_rows ? static_cast<int>(std::min(by_len, by_target)) : 0;
     const int prefill_reqs = max_q_len >= prefill_min_q
                                  ? std::min(num_reqs, total_q_tokens / std::max(1, prefill_min_q))
                                  : 0;
@@ -631,17 +706,19 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
     size_t off = 0;
     L.ctrl = off; off = up(off + 64 * sizeof(int32_t));
     L.req_info = off; off = up(off + static_cast<size_t>(num_reqs) * 16);
-    L.items = off; off = up(off + static_cast<size_t>(L.max_items) * 16);
+    L.rows = off; off = up(off + static_cast<size_t>(L.max_rows) * 16);
+    L.items = off; off = up(off + static_cast<size_t>(L.max_items) * 32);
     L.tiles = off; off = up(off + static_cast<size_t>(L.max_tiles) * 16);
-    L.part_ml = off; off = up(off + static_cast<size_t>(L.max_split_items) * G * 8);
-    L.part_o = off; off = up(off + static_cast<size_t>(L.max_split_items) * G * head_dim * 4);
+    L.part_ml = off; off = up(off + static_cast<size_t>(L.max_items) * G * 8);
+    L.part_o = off; off = up(off + static_cast<size_t>(L.max_items) * G * head_dim * 4);
     L.total = off;
     return L;
 }
 
 int launch_plan(const StepArgs& a, cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
 }
 
 template <typename T, int D, int G>
@@ -662,11 +739,14 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
     }
     const int grid = blocks_per_sm * a.num_sms;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return PKV_ERR_CUDA;
-    decode_kernel<T, D, G><<<grid, kDecThreads, S::kBytes, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (launch_pdl(decode_kernel<T, D, G>, dim3(grid), dim3(kDecThreads), S::kBytes, stream, a) !=
+        cudaSuccess)
+        return PKV_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return PKV_ERR_CUDA;
-    combine_kernel<T, D, G><<<std::max(1, a.num_reqs * a.num_kv_heads), 128, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_pdl(combine_kernel<T, D, G>, dim3(std::max(1, a.lay.max_rows * a.num_kv_heads)),
+                      dim3(G * D / 4), 0, stream, a) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
 }
 
 template <typename T, int D>
@@ -681,6 +761,7 @@ static int dispatch_group(const StepArgs& a, cudaStream_t s, cudaEvent_t e0, cud
 }
 
 int launch_decode(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
+    if (a.lay.max_items <= 0) return PKV_OK;  // no request can have decode rows
     if (a.dtype == PKV_BF16)
         return a.head_dim == 128 ? dispatch_group<__nv_bfloat16, 128>(a, stream, e0, e1)
                                  : dispatch_group<__nv_bfloat16, 64>(a, stream, e0, e1);

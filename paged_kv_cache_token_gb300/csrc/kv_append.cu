@@ -5,77 +5,81 @@
 // page; §4.3: a write kernel must also cover lengths that are exact multiples of the
 // page size.  hotelren.com/news/6181127 §3.1: the new K and V are appended to the cache.
 //
-// One warp copies one (token, KV head): D 16-bit values of K and of V, 16 bytes per lane,
-// so a token's K and V rows move as full 128-byte transactions.  The request of a token
-// comes from a binary search of q_offsets; the destination from the block table.  Bad
-// device data sets a flag bit and skips the copy; nothing traps.
+// A CTA takes up to 32 tokens of one request (grid.y = request, so no search for the
+// request of a token); one warp copies one (token, KV head): D 16-bit values of K and of
+// V, 16 bytes per lane, so each row moves as full 128-byte transactions.  The destination
+// comes from the block table.  Bad device data sets a flag bit and skips the copy; nothing
+// traps.
 #include "common.cuh"
 #include "launch.h"
 
 namespace pkv {
 
+constexpr int kTokPerBlock = 32;  // tokens of one request per CTA
+
+// grid.y = request, grid.x = chunk of kTokPerBlock tokens of that request
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
     constexpr int kLanesPerRow = D * 2 / 16;  // 16-byte chunks per K (or V) row: 16 or 8
-    const int warp_global = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    const int lane = threadIdx.x & 31;
-    const int t = warp_global / a.num_kv_heads;
-    const int h = warp_global % a.num_kv_heads;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && a.q_offsets[a.num_reqs] != a.total_q_tokens)
+    const int r = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // earlier kernels on the stream (the previous step) may still read the pool: wait for
+    // them before writing; then the attention plan, which reads only metadata, may start
+    pdl_wait();
+    pdl_trigger();
+    if (r == 0 && blockIdx.x == 0 && threadIdx.x == 0 &&
+        (a.q_offsets[0] != 0 || a.q_offsets[a.num_reqs] != a.total_q_tokens))
         set_error(a.err, PKV_DEVERR_TOKENS);
-    if (t >= a.total_q_tokens) return;
-
-    // request of token t: last r with q_offsets[r] <= t
-    int lo = 0, hi = a.num_reqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(a.q_offsets + mid) <= t) lo = mid; else hi = mid - 1;
-    }
-    const int r = lo;
-    const int start = __ldg(a.q_offsets + r);
     const int qlen = __ldg(a.q_lens + r);
-    if (t - start >= qlen) {  // q_offsets and q_lens disagree
-        if (lane == 0) set_error(a.err, PKV_DEVERR_TOKENS);
+    const int start = __ldg(a.q_offsets + r);
+    const int ctx = __ldg(a.context_lens + r);
+    const int tok0 = blockIdx.x * kTokPerBlock;
+    if (tok0 >= qlen) return;
+    if (__ldg(a.q_offsets + r + 1) - start != qlen || ctx < 0 || qlen > a.max_q_len ||
+        start + qlen > a.total_q_tokens) {
+        if (threadIdx.x == 0) set_error(a.err, PKV_DEVERR_TOKENS);
         return;
     }
-    const int pos = __ldg(a.context_lens + r) + (t - start);
-    const int lp = pos / kPage;
-    if (lp >= a.max_pages) {
-        if (lane == 0) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
-        return;
-    }
-    const int page = __ldg(a.block_table + static_cast<int64_t>(r) * a.max_pages + lp);
-    if (page < 0 || page >= a.num_pages) {
-        if (lane == 0) set_error(a.err, PKV_DEVERR_PAGE_RANGE);
-        return;
-    }
-    const int slot = pos % kPage;
-    if (h == 0 && lane == 0 && a.slot_mapping)
-        a.slot_mapping[t] = static_cast<int64_t>(page) * kPage + slot;
-
-    const int64_t src = (static_cast<int64_t>(t) * a.num_kv_heads + h) * D;
-    const int64_t dst = ((static_cast<int64_t>(page) * a.num_kv_heads + h) * kPage + slot) * D;
-    if (lane < 2 * kLanesPerRow) {
-        const bool is_v = lane >= kLanesPerRow;
-        const int chunk = is_v ? lane - kLanesPerRow : lane;
-        const uint16_t* s = static_cast<const uint16_t*>(is_v ? a.v_new : a.k_new) + src;
-        uint16_t* d = static_cast<uint16_t*>(is_v ? a.v_cache : a.k_cache) + dst;
-        const uint4 val = __ldg(reinterpret_cast<const uint4*>(s) + chunk);
-        reinterpret_cast<uint4*>(d)[chunk] = val;
+    const int ntok = min(kTokPerBlock, qlen - tok0);
+    const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.max_pages;
+    // one warp per (token, KV head): 16 bytes per lane, K rows on the low lanes, V above
+    for (int w = warp; w < ntok * a.num_kv_heads; w += blockDim.x / 32) {
+        const int i = tok0 + w / a.num_kv_heads, h = w % a.num_kv_heads;
+        const int t = start + i;
+        const int pos = ctx + i;
+        const int lp = pos / kPage;
+        if (lp >= a.max_pages) {
+            if (lane == 0) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
+            continue;
+        }
+        const int page = __ldg(bt + lp);
+        if (page < 0 || page >= a.num_pages) {
+            if (lane == 0) set_error(a.err, PKV_DEVERR_PAGE_RANGE);
+            continue;
+        }
+        const int slot = pos % kPage;
+        if (h == 0 && lane == 0 && a.slot_mapping)
+            a.slot_mapping[t] = static_cast<int64_t>(page) * kPage + slot;
+        const int64_t src = (static_cast<int64_t>(t) * a.num_kv_heads + h) * D;
+        const int64_t dst = ((static_cast<int64_t>(page) * a.num_kv_heads + h) * kPage + slot) * D;
+        if (lane < 2 * kLanesPerRow) {
+            const bool is_v = lane >= kLanesPerRow;
+            const int chunk = is_v ? lane - kLanesPerRow : lane;
+            const uint16_t* sp = static_cast<const uint16_t*>(is_v ? a.v_new : a.k_new) + src;
+            uint16_t* dp = static_cast<uint16_t*>(is_v ? a.v_cache : a.k_cache) + dst;
+            reinterpret_cast<uint4*>(dp)[chunk] = __ldg(reinterpret_cast<const uint4*>(sp) + chunk);
+        }
     }
 }
 
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
-    const int64_t warps = static_cast<int64_t>(a.total_q_tokens) * a.num_kv_heads;
-    if (warps == 0) return PKV_OK;
-    const int threads = 256;
-    const int64_t blocks = (warps + 7) / 8;
-    if (blocks > 0x7fffffff) return PKV_ERR_INVALID_ARG;
-    if (a.head_dim == 128)
-        kv_append_kernel<128><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
-    else
-        kv_append_kernel<64><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (a.total_q_tokens == 0 || a.num_reqs == 0) return PKV_OK;
+    if (a.num_reqs > 65535) return PKV_ERR_UNSUPPORTED;
+    const dim3 grid(cdiv(a.max_q_len, kTokPerBlock), a.num_reqs);
+    const cudaError_t e = a.head_dim == 128
+                              ? launch_pdl(kv_append_kernel<128>, grid, dim3(256), 0, stream, a)
+                              : launch_pdl(kv_append_kernel<64>, grid, dim3(256), 0, stream, a);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -6,10 +6,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pkv {
 
 struct AppendArgs {
-    int num_reqs, num_kv_heads, head_dim, num_pages, max_pages, total_q_tokens;
+    int num_reqs, num_kv_heads, head_dim, num_pages, max_pages, total_q_tokens, max_q_len;
     const int32_t* q_lens;
     const int32_t* q_offsets;
     const int32_t* context_lens;
@@ -23,17 +25,18 @@ struct AppendArgs {
 };
 
 // Workspace layout for one attention step, all offsets 256-byte aligned.
-//   ctrl      int32[64]           [0] decode work counter, [1] decode items,
-//                                 [2] split items (those with partials), [3] pages per split
-//                                 [8] prefill tile counter, [9] prefill tiles
-//   req_info  int4[num_reqs]      {first item, splits, q_len, first prefill tile}
-//   items     int4[max_items]     decode items {request, row in request, kv head, split}
-//   tiles     int4[max_tiles]     prefill tiles {request, q tile, q head, 0}
-//   part_ml   float2[max_split_items * G]      (running max in log2 units, sum)
-//   part_o    float[max_split_items * G * D]   un-normalised partial outputs
+//   ctrl      int32[64]        [0] decode work counter, [1] decode items, [2] decode rows,
+//                              [3] pages per split, [9] prefill tiles
+//   req_info  int4[num_reqs]   {first decode row, decode rows, q_len, first prefill tile}
+//   rows      int4[max_rows]   decode rows {token, slot of the first split, keys, splits}
+//   items     2 x int4[max_items]  work queue, largest first: {token, KV head | split << 16,
+//                              first page, pages}, {keys, splits, request, slot of split 0}
+//   tiles     int4[max_tiles]  prefill tiles {request, q tile, query head (pair), 0}
+//   part_ml   float2[max_items * G]      per slot (running max in log2 units, sum)
+//   part_o    float[max_items * G * D]   per slot un-normalised outputs
 struct WorkspaceLayout {
-    size_t ctrl, req_info, items, tiles, part_ml, part_o, total;
-    int max_items, max_tiles, max_split_items, max_splits;
+    size_t ctrl, req_info, rows, items, tiles, part_ml, part_o, total;
+    int max_rows, max_items, max_tiles, target_items;
 };
 
 struct StepArgs {
@@ -57,11 +60,28 @@ struct StepArgs {
 };
 
 WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                 int total_q_tokens, int max_q_len, int num_sms,
-                                 int prefill_min_q);
+                                 int total_q_tokens, int max_q_len, int max_context_len,
+                                 int num_sms, int prefill_min_q);
 // query heads one prefill tile covers for this head configuration
 inline int prefill_heads_per_tile(int num_q_heads, int num_kv_heads) {
     return ((num_q_heads / num_kv_heads) % 2 == 0) ? 2 : 1;
+}
+
+// Launch with the programmatic-stream-serialization attribute (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream);

@@ -70,6 +70,7 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
     constexpr uint32_t kIdescS = tc::idesc_f16(kAB, 0, kBM, kBN);
     constexpr uint32_t kIdescO = tc::idesc_f16(kAB, 1, kBM, D);
 
+    pdl_wait();  // plan, kv_append and the decode kernel of this step have completed
     const int32_t* ctrl = reinterpret_cast<const int32_t*>(a.ws + a.lay.ctrl);
     if (static_cast<int>(blockIdx.x) >= ctrl[9]) return;
 
@@ -431,9 +432,9 @@ int launch_pair_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEv
     if (!make_prefill_maps(a, &mq, &mk, &mv)) return PKV_ERR_CUDA;
     if (a.lay.max_tiles <= 0) return PKV_OK;
     if (e0 && cudaEventRecord(e0, stream) != cudaSuccess) return PKV_ERR_CUDA;
-    prefill_pair_kernel<T, D><<<a.lay.max_tiles, kThreads, S::kLaunchBytes, stream>>>(a, mq, mk,
-                                                                                       mv);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (launch_pdl(prefill_pair_kernel<T, D>, dim3(a.lay.max_tiles), dim3(kThreads),
+                   S::kLaunchBytes, stream, a, mq, mk, mv) != cudaSuccess)
+        return PKV_ERR_CUDA;
     if (e1 && cudaEventRecord(e1, stream) != cudaSuccess) return PKV_ERR_CUDA;
     return PKV_OK;
 }

@@ -90,13 +90,15 @@ def test_static_workspace_repeated_call_same_step():
 
 
 def test_static_workspace_rejects_steps_beyond_its_size():
-    # 200,000 query rows need a work list larger than the 16 MiB array: refused on the host
-    T = 200_000
+    # 4,096 decode rows over 100,000-token contexts need more split-KV scratch than the
+    # 16 MiB array holds: refused on the host before anything is launched
+    n, ctx = 4096, 100_000
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
-    desc = binding.make_desc(num_reqs=1, num_q_heads=32, num_kv_heads=8, head_dim=128,
-                             num_pages=T // 16, max_pages_per_req=T // 16, total_q_tokens=T,
-                             max_q_len=T, max_context_len=0, dtype=W.BF16, q_lens=dummy,
-                             q_offsets=dummy, context_lens=dummy, block_table=dummy)
+    desc = binding.make_desc(num_reqs=n, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                             num_pages=n * (ctx // 16 + 1), max_pages_per_req=ctx // 16 + 1,
+                             total_q_tokens=n, max_q_len=1, max_context_len=ctx, dtype=W.BF16,
+                             q_lens=dummy, q_offsets=dummy, context_lens=dummy,
+                             block_table=dummy)
     assert binding.attention_workspace_bytes(desc) > binding.STATIC_WORKSPACE_BYTES
     rc = binding.paged_attention_step_static_ws(desc, dummy, dummy, dummy, dummy, 1.0,
                                                 check=False)
