@@ -127,6 +127,35 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ our arm
+# DRAM traffic per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
+# kept in profiles/dram_traffic.json with a digest of the kernel's sources at capture time;
+# reported only while the sources still match, else null.
+KERNEL_SOURCES = {
+    "decode_kernel": ["decode.cu", "common.cuh", "launch.h"],
+    "prefill_pair_kernel": ["prefill_pair.cu", "tc.cuh", "common.cuh", "launch.h"],
+}
+
+
+def kernel_source_digest(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "paged_kv_cache_token_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel, scale=1.0):
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_sha256") != kernel_source_digest(kernel):
+        return None
+    return rec["bytes_per_launch"] * scale
+
+
 def lib_event():
     """A timing event whose CUDA handle exists (torch creates it on first record), so the
     library can record it on its own stream."""
@@ -422,7 +451,8 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_source": peak_src + " hbm_gbs",
                          "kernel": "decode_kernel", "bytes_per_launch": kernel_bytes,
-                         "ms_per_launch": r["ms_kernel"], "traffic": None},
+                         "ms_per_launch": r["ms_kernel"],
+                         "traffic": captured_traffic("decode_kernel")},
             "e2e": {"value": acct["step"] * dist_ctx.world / (r["ms_e2e"] * 1e-3) / 1e9,
                     "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["ms_e2e"]},
@@ -445,6 +475,7 @@ def main():
                              "achieved": kern_tflops, "peak": bf16, "unit": "TFLOP/s",
                              "frac": kern_tflops / bf16, "ms_per_launch": one["main_kernel_ms"],
                              "flops_per_launch": one["flops"],
+                             "traffic": captured_traffic("prefill_pair_kernel"),
                              "chunked_kernel_tflops": ch["flops"] / ch["main_kernel_ms"] / 1e9}}
         if not args.no_cpu_baseline and dist_ctx.rank == 0:
             secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
