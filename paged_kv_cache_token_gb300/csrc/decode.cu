@@ -29,6 +29,7 @@ namespace pkv {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanBlocks = 32;   // CTAs sharing the record writes
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kStages = 3;
@@ -40,18 +41,28 @@ __device__ __forceinline__ T* ws_at(const StepArgs& a, size_t off) {
     return reinterpret_cast<T*>(a.ws + off);
 }
 
-// Request r is valid for this step when its lengths agree with q_offsets and the host maxima.
-__device__ __forceinline__ bool request_ok(const StepArgs& a, int r, int q, int c) {
-    return q >= 0 && c >= 0 && q <= a.max_q_len && c <= a.max_context_len &&
-           a.q_offsets[r + 1] - a.q_offsets[r] == q;
+// A request is valid for this step when its lengths agree with q_offsets (o0 = q_offsets[r],
+// o1 = q_offsets[r + 1]) and the host maxima.
+__device__ __forceinline__ bool request_ok(const StepArgs& a, int q, int c, int o0, int o1) {
+    return q >= 0 && c >= 0 && q <= a.max_q_len && c <= a.max_context_len && o1 - o0 == q;
+}
+
+// Lengths of request r, all four loads issued together (no dependent round trip).
+struct ReqLens { int q, c, t0; bool ok; };
+__device__ __forceinline__ ReqLens load_request(const StepArgs& a, int r) {
+    const int q = a.q_lens[r], c = a.context_lens[r];
+    const int o0 = a.q_offsets[r], o1 = a.q_offsets[r + 1];
+    return ReqLens{q, c, o0, request_ok(a, q, c, o0, o1)};
 }
 
 }  // namespace
 
 // ------------------------------------------------------------------------------------
 // plan: validate lengths, choose the split size, number decode rows, decode items and
-// prefill tiles.  One CTA; per-request values of a chunk of 1024 requests live in shared
-// memory so each phase reads global memory at most once.
+// prefill tiles.  kPlanBlocks CTAs each compute the same counts, split size and scans
+// (per-request values of a chunk of 1024 requests live in shared memory); the record
+// writes are dealt out across all of them, because one SM alone drains stores slowly
+// enough to dominate the step's planning time.
 // ------------------------------------------------------------------------------------
 namespace {
 // exclusive block-wide scan of three ints per thread at once
@@ -87,7 +98,8 @@ __device__ Int3 block_exclusive_scan3(Int3 v, Int3* total, Int3* s_warp) {
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
     __shared__ unsigned long long s_sum;
-    __shared__ int s_bad, s_split;
+    __shared__ int s_bad, s_split, s_npf;
+    __shared__ int s_pf[kPlanThreads];  // chunk positions of the prefill requests
     __shared__ Int3 s_warp3[32];
     __shared__ int s_q[kPlanThreads], s_c[kPlanThreads], s_t0[kPlanThreads];
     __shared__ int s_row0[kPlanThreads], s_item0[kPlanThreads], s_tile0[kPlanThreads];
@@ -100,18 +112,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
     const int slots = a.num_q_heads / a.heads_per_tile;
     if (tid == 0) {
         s_sum = 0;
-        s_bad = (a.q_offsets[0] != 0 || a.q_offsets[a.num_reqs] != a.total_q_tokens);
+        s_bad = 0;
     }
     __syncthreads();
 
-    // ---- pass A: validity and the decode page total (sets the split size)
+    // ---- pass A: validity and the decode page total (sets the split size).  The lengths of
+    //      this thread's request in the first chunk stay in registers for the fill.
     unsigned long long my_sum = 0;
+    ReqLens first{0, 0, 0, false};
+    if (tid == 0 && (a.q_offsets[0] != 0 || a.q_offsets[a.num_reqs] != a.total_q_tokens))
+        atomicOr(&s_bad, 1);
     for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
-        const int q = a.q_lens[r], c = a.context_lens[r];
-        if (!request_ok(a, r, q, c)) { atomicOr(&s_bad, 1); continue; }
-        if (cdiv(c + q, kPage) > a.max_pages) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
-        if (q >= 1 && q < a.prefill_min_q)
-            for (int i = 0; i < q; ++i) my_sum += cdiv(c + i + 1, kPage);
+        const ReqLens L = load_request(a, r);
+        if (r == tid) first = L;
+        if (!L.ok) { atomicOr(&s_bad, 1); continue; }
+        if (cdiv(L.c + L.q, kPage) > a.max_pages) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
+        if (L.q >= 1 && L.q < a.prefill_min_q)
+            for (int i = 0; i < L.q; ++i) my_sum += cdiv(L.c + i + 1, kPage);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) my_sum += __shfl_xor_sync(kFull, my_sum, o);
@@ -119,7 +136,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
     __syncthreads();
     const bool bad = s_bad != 0;
     if (tid == 0) {
-        if (bad) set_error(a.err, PKV_DEVERR_TOKENS);
+        if (bad && blockIdx.x == 0) set_error(a.err, PKV_DEVERR_TOKENS);
         const unsigned long long heads = s_sum * static_cast<unsigned long long>(Hkv);
         const unsigned long long tgt = static_cast<unsigned long long>(a.lay.target_items);
         const unsigned long long sp = (heads + tgt - 1) / tgt;
@@ -133,18 +150,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
     bool overflow = false;
     for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
         const int r = base + tid;
-        int q = 0, c = 0;
+        int q = 0, c = 0, t0 = 0;
         Int3 n{0, 0, 0};  // decode rows, decode items, prefill tiles of request r
         if (r < a.num_reqs && !bad) {
-            q = a.q_lens[r];
-            c = a.context_lens[r];
-            if (!request_ok(a, r, q, c)) q = 0;
+            const ReqLens L = base == 0 ? first : load_request(a, r);
+            q = L.ok ? L.q : 0;
+            c = L.c;
+            t0 = L.t0;
             if (q >= 1 && q < a.prefill_min_q) {
                 n.x = q;
                 for (int i = 0; i < q; ++i) n.y += Hkv * cdiv(cdiv(c + i + 1, kPage), sp);
             }
             if (q > 1 && q >= a.prefill_min_q) n.z = cdiv(q, 128) * slots;
         }
+        if (tid == 0) s_npf = 0;  // read after the scan's barriers
         Int3 tot;
         const Int3 ex = block_exclusive_scan3(n, &tot, s_warp3);
         overflow = overflow || carry.x + tot.x > a.lay.max_rows ||
@@ -152,14 +171,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
         if (r < a.num_reqs) {
             s_q[tid] = q;
             s_c[tid] = c;
-            s_t0[tid] = r < a.num_reqs ? a.q_offsets[r] : 0;
+            s_t0[tid] = t0;
             s_row0[tid] = carry.x + ex.x;
             s_item0[tid] = carry.y + ex.y;
             s_tile0[tid] = carry.z + ex.z;
+            if (n.z > 0) s_pf[atomicAdd(&s_npf, 1)] = tid;
         }
         __syncthreads();
         const int nreq = min(kPlanThreads, a.num_reqs - base);
-        for (int k = warp; !overflow && k < nreq; k += kPlanThreads / 32) {
+        // request k of the chunk belongs to warp (k / grid) of CTA (k % grid); the tiles of a
+        // prefill request are spread over every warp of every CTA
+        const int gwarp = blockIdx.x * (kPlanThreads / 32) + warp;
+        const int nwarps = gridDim.x * (kPlanThreads / 32);
+        for (int f = 0; !overflow && f < s_npf; ++f) {
+            const int k = s_pf[f], qk = s_q[k];
+            {
+                const int nt = cdiv(qk, 128), rq = base + k;
+                for (int i = gwarp * 32 + lane; i < nt * slots; i += nwarps * 32)
+                    tiles[s_tile0[k] + i] = make_int4(rq, nt - 1 - i / slots, i % slots, 0);
+            }
+        }
+        for (int k = blockIdx.x + gridDim.x * warp; !overflow && k < nreq;
+             k += gridDim.x * (kPlanThreads / 32)) {
             const int rq = base + k, qk = s_q[k], ck = s_c[k];
             if (qk >= 1 && qk < a.prefill_min_q) {
                 // rows of this request (qk <= 31): lane i = row i; warp scan of item counts
@@ -175,23 +208,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
                     rows[s_row0[k] + lane] = make_int4(s_t0[k] + lane, first, ck + lane + 1, ns);
                 }
                 for (int i = 0; i < qk; ++i) {
-                    const int ns_i = __shfl_sync(kFull, ns, i);
+                    const unsigned ns_i = __shfl_sync(kFull, ns, i);
                     const int first_i = __shfl_sync(kFull, first, i);
                     const int nkv = ck + i + 1, pages = cdiv(nkv, kPage);
                     const int t = s_t0[k] + i;
-                    for (int e = lane; e < Hkv * ns_i; e += 32) {
-                        const int g = e / ns_i, s_ = e % ns_i;
-                        const int pb = static_cast<int>(static_cast<long long>(s_) * pages / ns_i);
-                        const int pe = static_cast<int>(static_cast<long long>(s_ + 1) * pages / ns_i);
-                        const int pos = first_i + e;  // = slot: splits of a (row, head) adjacent
-                        items[2 * pos] = make_int4(t, g | (s_ << 16), pb, pe - pb);
-                        items[2 * pos + 1] = make_int4(nkv, ns_i, rq, first_i + g * ns_i);
+                    // balanced splits: the first `rem` splits get one page more than `per`
+                    const int per = pages / static_cast<int>(ns_i);
+                    const int rem = pages - per * static_cast<int>(ns_i);
+                    // lane l writes 16-byte half l of the row's item records, so a warp store
+                    // covers 512 contiguous bytes; item position = slot (splits of a (row,
+                    // head) adjacent)
+                    int4* dst = items + 2 * static_cast<int64_t>(first_i);
+                    for (unsigned h = lane; h < 2 * Hkv * ns_i; h += 32) {
+                        const unsigned e = h >> 1;
+                        const int g = static_cast<int>(e / ns_i);
+                        const int s_ = static_cast<int>(e) - g * static_cast<int>(ns_i);
+                        if (h & 1) {
+                            dst[h] = make_int4(nkv, static_cast<int>(ns_i), rq,
+                                               first_i + g * static_cast<int>(ns_i));
+                        } else {
+                            const int pb = s_ * per + min(s_, rem);
+                            const int np = per + (s_ < rem ? 1 : 0);
+                            dst[h] = make_int4(t, g | (s_ << 16), pb, np);
+                        }
                     }
                 }
-            } else if (qk > 1) {
-                const int nt = cdiv(qk, 128);
-                for (int i = lane; i < nt * slots; i += 32)
-                    tiles[s_tile0[k] + i] = make_int4(rq, nt - 1 - i / slots, i % slots, 0);
             }
         }
         carry = Int3{carry.x + tot.x, carry.y + tot.y, carry.z + tot.z};
@@ -201,7 +242,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
     // waits for the plan also sees the appended K/V), then let the attention kernels start
     pdl_wait();
     pdl_trigger();
-    if (tid == 0) {
+    if (tid == 0 && blockIdx.x == 0) {
         if (overflow) set_error(a.err, PKV_DEVERR_TOKENS);  // host maxima were wrong
         ctrl[0] = 0;
         ctrl[1] = overflow ? 0 : carry.y;
@@ -220,7 +261,7 @@ struct DecodeSmem {
     static constexpr int kPageBytes = kPage * D * 2;      // one K (or V) page block
     static constexpr int kStageBytes = 2 * kPageBytes;
     static constexpr int kRing = kDecWarps * kStages * kStageBytes;
-    static constexpr int kPbuf = kDecWarps * kPage * G * 4;
+    static constexpr int kPbuf = kDecWarps * kPage * G * 8;  // (p, p) pairs per token, head
     static constexpr int kBars = kDecWarps * kStages * 8;
     static constexpr int kBytes = kRing + kPbuf + kBars;
 };
@@ -239,13 +280,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     constexpr int QKD = D / 8;      // dims per lane in q.k (16 or 8)
     constexpr int NCH = QKD / 8;    // 16-byte chunks per lane per key row (2 or 1)
     constexpr int DPL = D / 32;     // dims per lane in p.V (4 or 2)
+    constexpr int DP2 = DPL / 2;    // ... as float2 pairs
     constexpr int N0 = 4 * G, N1 = N0 / 2, N2 = N1 / 2 > 0 ? N1 / 2 : 1;
     constexpr int NV = (N2 >= 2) ? N2 / 2 : 1;  // score values a lane holds after reduction
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* ring = smem + warp * kStages * S::kStageBytes;
-    float* pbuf = reinterpret_cast<float*>(smem + S::kRing) + warp * kPage * G;
+    float2* pbuf = reinterpret_cast<float2*>(smem + S::kRing) + warp * kPage * G;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing + S::kPbuf) + warp * kStages;
 
     if (lane == 0) {
@@ -394,7 +436,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     };
     while (cur.np > 0 && !aborted) {
         // query heads g*G .. g*G+G-1, my q.k dims, pre-scaled into base-2 units
-        float qf[G][QKD];
+        // (even dim, odd dim) pairs: the packed fp32 FMA (FFMA2) works on both at once
+        float2 qf[G][QKD / 2];
+        const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int j = 0; j < G; ++j) {
 #pragma unroll
@@ -402,19 +446,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 const uint32_t ws4[4] = {q_cur[j][ci].x, q_cur[j][ci].y, q_cur[j][ci].z,
                                          q_cur[j][ci].w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = Cv::unpack(ws4[e]);
-                    qf[j][ci * 8 + 2 * e] = f.x * a.scale_log2;
-                    qf[j][ci * 8 + 2 * e + 1] = f.y * a.scale_log2;
-                }
+                for (int e = 0; e < 4; ++e) qf[j][ci * 4 + e] = __fmul2_rn(Cv::unpack(ws4[e]), sl2);
             }
         }
-        float m[G], o[G][DPL], lsum[NV];
+        float m[G], lsum[NV];
+        float2 o[G][DP2];  // dims (2e, 2e+1) of my DPL output dims, per head
 #pragma unroll
         for (int j = 0; j < G; ++j) {
             m[j] = -1e30f;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) o[j][e] = 0.f;
+            for (int e = 0; e < DP2; ++e) o[j][e] = make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < NV; ++i) lsum[i] = 0.f;
@@ -434,9 +475,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             float v[N0];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                float acc[G];
+                float2 acc[G];  // even-dim and odd-dim partial sums
 #pragma unroll
-                for (int j = 0; j < G; ++j) acc[j] = 0.f;
+                for (int j = 0; j < G; ++j) acc[j] = make_float2(0.f, 0.f);
                 const uint4* krow = reinterpret_cast<const uint4*>(sK + (tg * 4 + kk) * D * 2) +
                                     c8 * NCH;
 #pragma unroll
@@ -447,14 +488,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = Cv::unpack(ws4[e]);
 #pragma unroll
-                        for (int j = 0; j < G; ++j) {
-                            acc[j] = fmaf(qf[j][ci * 8 + 2 * e], f.x, acc[j]);
-                            acc[j] = fmaf(qf[j][ci * 8 + 2 * e + 1], f.y, acc[j]);
-                        }
+                        for (int j = 0; j < G; ++j) acc[j] = __ffma2_rn(qf[j][ci * 4 + e], f, acc[j]);
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < G; ++j) v[kk * G + j] = acc[j];
+                for (int j = 0; j < G; ++j) v[kk * G + j] = acc[j].x + acc[j].y;
             }
             // ---- reduce over the 8 lanes of a token group by recursive halving
 #pragma unroll
@@ -520,34 +558,35 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 const float ah = (G == 1) ? alpha[0] : (b0 ? alpha[NV + i2] : alpha[i2]);
                 const float p = fast_exp2(s[i2] - mh);
                 lsum[i2] = fmaf(lsum[i2], ah, p);
-                if (G > 1 || !b0) pbuf[my_tok * G + ((G == 1) ? 0 : (b0 ? NV : 0) + i2)] = p;
+                if (G > 1 || !b0)
+                    pbuf[my_tok * G + ((G == 1) ? 0 : (b0 ? NV : 0) + i2)] = make_float2(p, p);
             }
             __syncwarp();
 
             // ---- o[j][:] = o[j][:] * alpha[j] + sum_tok p[tok][j] * V[tok][:]
             if (rescale) {
 #pragma unroll
-                for (int j = 0; j < G; ++j)
+                for (int j = 0; j < G; ++j) {
+                    const float2 a2 = make_float2(alpha[j], alpha[j]);
 #pragma unroll
-                    for (int e = 0; e < DPL; ++e) o[j][e] *= alpha[j];
+                    for (int e = 0; e < DP2; ++e) o[j][e] = __fmul2_rn(o[j][e], a2);
+                }
             }
             auto pv_token = [&](int tok) {
-                float vf[DPL];
+                float2 vf[DP2];
                 if constexpr (DPL == 4) {
                     const uint2 w = *reinterpret_cast<const uint2*>(sV + tok * D * 2 + lane * 8);
-                    const float2 f0 = Cv::unpack(w.x), f1 = Cv::unpack(w.y);
-                    vf[0] = f0.x; vf[1] = f0.y; vf[2] = f1.x; vf[3] = f1.y;
+                    vf[0] = Cv::unpack(w.x);
+                    vf[DP2 - 1] = Cv::unpack(w.y);
                 } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(sV + tok * D * 2 + lane * 4);
-                    const float2 f0 = Cv::unpack(w);
-                    vf[0] = f0.x; vf[1] = f0.y;
+                    vf[0] = Cv::unpack(*reinterpret_cast<const uint32_t*>(sV + tok * D * 2 + lane * 4));
                 }
-                const float* pr = pbuf + tok * G;
+                const float2* pr = pbuf + tok * G;
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
-                    const float pj = pr[j];
+                    const float2 pj = pr[j];
 #pragma unroll
-                    for (int e = 0; e < DPL; ++e) o[j][e] = fmaf(pj, vf[e], o[j][e]);
+                    for (int e = 0; e < DP2; ++e) o[j][e] = __ffma2_rn(pj, vf[e], o[j][e]);
                 }
             };
             if (nvalid == kPage) {
@@ -584,7 +623,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 float res[DPL];
                 const float inv = 1.f / lh[j];
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) res[e] = o[j][e] * inv;
+                for (int e = 0; e < DP2; ++e) {
+                    res[2 * e] = o[j][e].x * inv;
+                    res[2 * e + 1] = o[j][e].y * inv;
+                }
                 store_row(cur.t, cur.g, j, res);
             }
         } else {
@@ -593,9 +635,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             const int64_t slot = static_cast<int64_t>(cur.base) + cur.s;
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                float* po = part_o + (slot * G + j) * D + lane * DPL;
+                float2* po = reinterpret_cast<float2*>(part_o + (slot * G + j) * D + lane * DPL);
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) po[e] = o[j][e];
+                for (int e = 0; e < DP2; ++e) po[e] = o[j][e];
                 if (lane == 0) part_ml[slot * G + j] = make_float2(m[j], lh[j]);
             }
         }
@@ -643,31 +685,48 @@ __global__ void __launch_bounds__(G * D / 4) combine_kernel(StepArgs a) {
     using Cv = F16<T>;
     const int Hkv = a.num_kv_heads;
     const int d = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
-    pdl_wait();  // the decode kernel has finished writing the partials
+    // the row records come from the plan, which completed before the decode kernel let this
+    // grid launch: read them before waiting for the decode kernel's partials
     const int32_t* ctrl = ws_at<const int32_t>(a, a.lay.ctrl);
+    const int nrows = ctrl[2];
     const int4 row = ws_at<const int4>(a, a.lay.rows)[d];  // {token, first slot, keys, splits}
-    if (d >= ctrl[2]) return;
+    pdl_wait();  // the decode kernel has finished writing the partials
+    if (d >= nrows) return;
     const int ns = row.w;
     if (ns <= 1) return;  // finished in place by the decode kernel
     const int64_t base = row.y + static_cast<int64_t>(g) * ns;
     const float2* part_ml = ws_at<const float2>(a, a.lay.part_ml);
     const float* part_o = ws_at<const float>(a, a.lay.part_o);
     const int j = threadIdx.x / (D / 4), dim = (threadIdx.x % (D / 4)) * 4;
-    // one pass with a running maximum: acc, L rescaled when a split raises it
+    // one pass with a running maximum: acc, L rescaled when a split raises it.  Splits are
+    // read in predicated batches of kBatch so all loads of a batch are in flight together.
+    constexpr int kBatch = 8;
     float M = -1e30f, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int s = 0; s < ns; ++s) {
-        const float2 ml = part_ml[(base + s) * G + j];
-        const float4 o = *reinterpret_cast<const float4*>(part_o + ((base + s) * G + j) * D + dim);
-        const float mn = fmaxf(M, ml.x);
-        const float c = fast_exp2(M - mn), w = fast_exp2(ml.x - mn);
-        M = mn;
-        L = fmaf(L, c, ml.y * w);
-        acc.x = fmaf(acc.x, c, o.x * w);
-        acc.y = fmaf(acc.y, c, o.y * w);
-        acc.z = fmaf(acc.z, c, o.z * w);
-        acc.w = fmaf(acc.w, c, o.w * w);
+    for (int s0 = 0; s0 < ns; s0 += kBatch) {
+        float2 ml[kBatch];
+        float4 o[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (s0 + u < ns) {
+                const int64_t slot = base + s0 + u;
+                ml[u] = part_ml[slot * G + j];
+                o[u] = *reinterpret_cast<const float4*>(part_o + (slot * G + j) * D + dim);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (s0 + u < ns) {
+                const float mn = fmaxf(M, ml[u].x);
+                const float c = fast_exp2(M - mn), w = fast_exp2(ml[u].x - mn);
+                M = mn;
+                L = fmaf(L, c, ml[u].y * w);
+                acc.x = fmaf(acc.x, c, o[u].x * w);
+                acc.y = fmaf(acc.y, c, o[u].y * w);
+                acc.z = fmaf(acc.z, c, o[u].z * w);
+                acc.w = fmaf(acc.w, c, o[u].w * w);
+            }
+        }
     }
     const float inv = 1.f / L;
     const int t = row.x;
@@ -716,7 +775,8 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
 }
 
 int launch_plan(const StepArgs& a, cudaStream_t stream) {
-    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a) == cudaSuccess
+    return launch_pdl(plan_kernel, dim3(kPlanBlocks), dim3(kPlanThreads), 0, stream, a) ==
+                   cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
 }
