@@ -306,6 +306,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads;
     const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
     const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
+    // K/V pages are read once per step: evict them first so the split partials written
+    // meanwhile stay in L2 for the combine
+    const uint64_t kv_policy = l2_policy_evict_first();
     const int c8 = lane & 7, tg = lane >> 3;
     const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
     const int swz = (c8 >> 2) & 1;  // staggered chunk order: conflict-free 16-byte loads
@@ -416,8 +419,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             uint8_t* dst = ring + stage * S::kStageBytes;
             const int64_t off = (static_cast<int64_t>(phys) * Hkv + g) * (kPage * D);
             mbar_arrive_expect_tx(&bars[stage], 2 * S::kPageBytes);
-            bulk_g2s(dst, kc + off, S::kPageBytes, &bars[stage]);
-            bulk_g2s(dst + S::kPageBytes, vc + off, S::kPageBytes, &bars[stage]);
+            bulk_g2s_hint(dst, kc + off, S::kPageBytes, &bars[stage], kv_policy);
+            bulk_g2s_hint(dst + S::kPageBytes, vc + off, S::kPageBytes, &bars[stage], kv_policy);
         }
         ++issued;
     };
