@@ -87,6 +87,7 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
     uint64_t* p_full = bars + 13;   // [2] per head
     uint64_t* o_final = bars + 15;
     uint64_t* drain = bars + 16;
+    uint64_t* p_half = bars + 17;   // [2] per head: P of keys 0..63 written
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -116,6 +117,7 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
         for (int h = 0; h < 2; ++h) {
             mbar_init(&s_full[h], 1);
             mbar_init(&p_full[h], 128);
+            mbar_init(&p_half[h], 128);
         }
         mbar_init(o_final, 1);
         mbar_init(drain, 1);
@@ -218,12 +220,15 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                 }
                 tc::commit(&s_full[h]);
             };
-            auto issue_pv = [&](int h, int j) {
+            // half 0: keys 0..63 of the tile, half 1: keys 64..127
+            auto issue_pv = [&](int h, int j, int half) {
                 const uint64_t dv = dv0 + static_cast<uint64_t>(j % kStagesV) * kKStep;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
+                for (int k4 = 0; k4 < kBN / 32; ++k4) {
+                    const int kk = half * (kBN / 32) + k4;
                     tc::mma_f16_ts(tm_o(h), tm_s(h) + kk * 8, dv + static_cast<uint64_t>(kk * 2048 >> 4),
                                    kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
             };
             auto wait_k = [&](int j) {
                 return mbar_wait(&k_full[j % kStagesK], (j / kStagesK) & 1);
@@ -234,20 +239,28 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                 issue_s(1, 0);
                 tc::commit(&k_empty[0]);
             }
+            // P V of a head starts on the first half of P while the softmax finishes the
+            // second half
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (!mbar_wait(&v_full[j % kStagesV], (j / kStagesV) & 1) ||
-                    !mbar_wait(&p_full[0], j & 1)) { ok = false; break; }
+                    !mbar_wait(&p_half[0], j & 1)) { ok = false; break; }
                 tc::fence_after_sync();
-                issue_pv(0, j);
+                issue_pv(0, j, 0);
+                if (!mbar_wait(&p_full[0], j & 1)) { ok = false; break; }
+                tc::fence_after_sync();
+                issue_pv(0, j, 1);
                 const bool more = j + 1 < n_kv;
                 if (more) {
                     if (!wait_k(j + 1)) { ok = false; break; }
                     tc::fence_after_sync();
                     issue_s(0, j + 1);
                 }
+                if (!mbar_wait(&p_half[1], j & 1)) { ok = false; break; }
+                tc::fence_after_sync();
+                issue_pv(1, j, 0);
                 if (!mbar_wait(&p_full[1], j & 1)) { ok = false; break; }
                 tc::fence_after_sync();
-                issue_pv(1, j);
+                issue_pv(1, j, 1);
                 tc::commit(&v_empty[j % kStagesV]);
                 if (more) {
                     issue_s(1, j + 1);
@@ -276,31 +289,36 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             // keys at or past `lim` are masked for this row (only on the diagonal tiles)
             const bool diag = kbase + kBN - 1 > first_pos;
             const int lim = diag ? pos + 1 - kbase : kBN;
-            // pass 1: row maximum of the raw scores
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t sr[32];
-                tc::tmem_ld32(my_s + cb * 32, sr);
-                tc::tmem_wait_ld();
+            // pass 1: row maximum of the raw scores, two 32-column loads per wait; columns
+            // 64..127 first, then 0..63, which stay in registers for pass 2
+            uint32_t c0[32], c1[32];
+            float mx[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+            auto chunk_max = [&](const uint32_t (&sr)[32], int cb) {
                 if (!diag) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        mx0 = fmaxf(mx0, __uint_as_float(sr[e]));
-                        mx1 = fmaxf(mx1, __uint_as_float(sr[e + 1]));
-                        mx2 = fmaxf(mx2, __uint_as_float(sr[e + 2]));
-                        mx3 = fmaxf(mx3, __uint_as_float(sr[e + 3]));
-                    }
+                    for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[e]));
                 } else {
                     const int rem = lim - cb * 32;  // valid keys in this chunk
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = e < rem ? __uint_as_float(sr[e]) : -INFINITY;
-                        if ((e & 1) == 0) mx0 = fmaxf(mx0, x); else mx1 = fmaxf(mx1, x);
-                    }
+                    for (int e = 0; e < 32; ++e)
+                        mx[e & 7] = fmaxf(mx[e & 7], e < rem ? __uint_as_float(sr[e]) : -INFINITY);
                 }
-            }
-            const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            };
+            tc::tmem_ld32(my_s + 64, c0);
+            tc::tmem_ld32(my_s + 96, c1);
+            tc::tmem_wait_ld();
+            chunk_max(c0, 2);
+            chunk_max(c1, 3);
+            tc::tmem_ld32(my_s, c0);
+            tc::tmem_ld32(my_s + 32, c1);
+            tc::tmem_wait_ld();
+            chunk_max(c0, 0);
+            chunk_max(c1, 1);
+            const float tmax =
+                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
             const float m_new = fmaxf(m, tmax);
             const bool need = (j == 0) || (m_new > m + kRescaleThreshold);
             const float alpha = (j > 0 && need) ? tc::ex2(m - m_new) : 1.f;
@@ -318,51 +336,37 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                     tc::tmem_st32(my_o + cb * 32, orow);
                 }
             }
-            // pass 2: P = 2^(s * scale_log2 - m), packed pairs written over the scores; the
-            // next chunk's scores load while this chunk's exponentials run
-            float ls0 = 0.f, ls1 = 0.f;
-            const float nm = -m;
-            uint32_t sa[32], sb[32];
-            tc::tmem_ld32(my_s, sa);
-            tc::tmem_wait_ld();
+            // pass 2: P = 2^(s * scale_log2 - m), packed pairs written over the scores of
+            // columns already consumed (P of chunk cb goes to columns 16 cb .. 16 cb + 15);
+            // scale-and-subtract and the row sums run two columns per instruction
+            float2 ls = make_float2(0.f, 0.f);
+            const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
             auto exps = [&](const uint32_t (&sr)[32], int cb) {
                 uint32_t pk[16];
-                if (!diag) {
+                const int rem = diag ? lim - cb * 32 : 32;
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const float p0 = tc::ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, nm));
-                        const float p1 = tc::ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nm));
-                        if (u & 1) ls1 += p0 + p1; else ls0 += p0 + p1;
-                        pk[u] = Cv::pack(p0, p1);
-                    }
-                } else {
-                    const int rem = lim - cb * 32;
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        float p0 = tc::ex2(fmaf(__uint_as_float(sr[2 * u]), sl2, nm));
-                        float p1 = tc::ex2(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nm));
+                for (int u = 0; u < 16; ++u) {
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
+                        sl2x2, nm2);
+                    float p0 = tc::ex2(x.x), p1 = tc::ex2(x.y);
+                    if (diag) {
                         p0 = 2 * u < rem ? p0 : 0.f;
                         p1 = 2 * u + 1 < rem ? p1 : 0.f;
-                        if (u & 1) ls1 += p0 + p1; else ls0 += p0 + p1;
-                        pk[u] = Cv::pack(p0, p1);
                     }
+                    ls = __fadd2_rn(ls, make_float2(p0, p1));
+                    pk[u] = Cv::pack(p0, p1);
                 }
                 tc::tmem_st16(my_s + cb * 16, pk);
             };
-            tc::tmem_ld32(my_s + 32, sb);
-            exps(sa, 0);
-            tc::tmem_wait_ld();
-            tc::tmem_ld32(my_s + 64, sa);
-            exps(sb, 1);
-            tc::tmem_wait_ld();
-            tc::tmem_ld32(my_s + 96, sb);
-            exps(sa, 2);
-            tc::tmem_wait_ld();
-            exps(sb, 3);
-            tc::tmem_wait_st();
-            l = l * alpha + (ls0 + ls1);
+            // each reload (S columns 64..127, still intact) goes into the chunk just consumed
+            // and lands while the other chunk's exponentials run
+            exps(c0, 0);
+            tc::tmem_ld32(my_s + 64, c0);
+            exps(c1, 1);
             // final tile: V rows past the last key are zeroed (P is 0 there; stale pool
-            // data may be NaN and 0 * NaN would poison the product)
+            // data may be NaN and 0 * NaN would poison the product) before any P V of the
+            // tile can read them
             if (h == 0 && j == n_kv - 1 && kv_len - kbase < kBN) {
                 if (mbar_wait_warp(&v_full[j % kStagesV], (j / kStagesV) & 1) &&
                     kbase + i >= kv_len) {
@@ -376,6 +380,17 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
                 }
                 tc::fence_proxy_async_smem();
             }
+            tc::tmem_wait_st();  // P of keys 0..63 is in tensor memory
+            tc::fence_before_sync();
+            mbar_arrive(&p_half[h]);
+            tc::tmem_wait_ld();
+            tc::tmem_ld32(my_s + 96, c1);
+            exps(c0, 2);
+            tc::tmem_wait_ld();
+            exps(c1, 3);
+            tc::tmem_wait_st();
+            const float ls0 = ls.x, ls1 = ls.y;
+            l = l * alpha + (ls0 + ls1);
             tc::fence_before_sync();
             mbar_arrive(&p_full[h]);
         }
