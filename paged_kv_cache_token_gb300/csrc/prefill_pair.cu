@@ -339,28 +339,39 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             // pass 2: P = 2^(s * scale_log2 - m), packed pairs written over the scores of
             // columns already consumed (P of chunk cb goes to columns 16 cb .. 16 cb + 15);
             // scale-and-subtract and the row sums run two columns per instruction
-            float2 ls = make_float2(0.f, 0.f);
+            // two independent partial sums, so no add chain waits on each exponential
+            float2 ls[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) ls[q] = make_float2(0.f, 0.f);
             const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
             auto exps = [&](const uint32_t (&sr)[32], int cb) {
-                uint32_t pk[16];
                 const int rem = diag ? lim - cb * 32 : 32;
+                float p[32];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const float2 x = __ffma2_rn(
                         make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
                         sl2x2, nm2);
-                    float p0 = tc::ex2(x.x), p1 = tc::ex2(x.y);
-                    if (diag) {
-                        p0 = 2 * u < rem ? p0 : 0.f;
-                        p1 = 2 * u + 1 < rem ? p1 : 0.f;
-                    }
-                    ls = __fadd2_rn(ls, make_float2(p0, p1));
-                    pk[u] = Cv::pack(p0, p1);
+                    p[2 * u] = x.x;
+                    p[2 * u + 1] = x.y;
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    p[e] = tc::ex2(p[e]);
+                    if (diag) p[e] = e < rem ? p[e] : 0.f;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    ls[u & 1] = __fadd2_rn(ls[u & 1], make_float2(p[2 * u], p[2 * u + 1]));
+                    pk[u] = Cv::pack(p[2 * u], p[2 * u + 1]);
                 }
                 tc::tmem_st16(my_s + cb * 16, pk);
             };
             // each reload (S columns 64..127, still intact) goes into the chunk just consumed
             // and lands while the other chunk's exponentials run
+            // the two remaining chunks are loaded before the first half of P is released,
+            // so their loads do not queue behind the P V reads of tensor memory
             exps(c0, 0);
             tc::tmem_ld32(my_s + 64, c0);
             exps(c1, 1);
@@ -389,7 +400,8 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             tc::tmem_wait_ld();
             exps(c1, 3);
             tc::tmem_wait_st();
-            const float ls0 = ls.x, ls1 = ls.y;
+            const float2 lsum = __fadd2_rn(ls[0], ls[1]);
+            const float ls0 = lsum.x, ls1 = lsum.y;
             l = l * alpha + (ls0 + ls1);
             tc::fence_before_sync();
             mbar_arrive(&p_full[h]);
