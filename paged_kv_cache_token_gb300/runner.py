@@ -97,6 +97,109 @@ class PagedKV:
         return binding.read_device_error(self.err)
 
 
+class StepStaging:
+    """A step's inputs in one transfer each way.
+
+    Q, K_new, V_new and the four metadata arrays are packed, 256-byte aligned, into one
+    pinned host buffer; one asynchronous copy moves them into a device buffer whose views
+    are what the library calls take, and one copy brings the output back.  Separate small
+    copies would each pay the transfer latency; a decode step's inputs are under a
+    megabyte.  Buffers grow on demand and are reused across steps; ``stage`` rewrites the
+    pinned buffer, so call it only once the previous ``upload`` has completed (or keep two
+    stagings and alternate).
+    """
+
+    ALIGN = 256
+
+    def __init__(self, kv: PagedKV):
+        self.kv = kv
+        self._host = self._dev = None
+        self._out_host = self._out_dev = None
+
+    @staticmethod
+    def _up(x: int) -> int:
+        return (x + StepStaging.ALIGN - 1) // StepStaging.ALIGN * StepStaging.ALIGN
+
+    def _layout(self, plan: StepPlan):
+        kv, T, B = self.kv, plan.total_q_tokens, plan.num_reqs
+        esz = torch.tensor([], dtype=kv.dtype).element_size()
+        parts = [("q", T * kv.hq * kv.d * esz), ("k", T * kv.hkv * kv.d * esz),
+                 ("v", T * kv.hkv * kv.d * esz), ("q_lens", B * 4), ("q_offsets", (B + 1) * 4),
+                 ("context_lens", B * 4), ("block_table", B * plan.max_pages * 4)]
+        offs, off = {}, 0
+        for name, nbytes in parts:
+            offs[name] = (off, nbytes)
+            off = self._up(off + nbytes)
+        return offs, off
+
+    def _ensure(self, nbytes: int, out_bytes: int) -> None:
+        if self._host is None or self._host.numel() < nbytes:
+            self._host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+            self._dev = torch.empty(nbytes, dtype=torch.uint8, device=self.kv.device)
+        if self._out_host is None or self._out_host.numel() < out_bytes:
+            self._out_host = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+            self._out_dev = torch.empty(out_bytes, dtype=torch.uint8, device=self.kv.device)
+
+    def stage(self, plan: StepPlan, q_bits: np.ndarray, k_bits: np.ndarray,
+              v_bits: np.ndarray) -> None:
+        """Write a step's inputs (16-bit patterns and metadata) into the pinned buffer."""
+        kv = self.kv
+        offs, total = self._layout(plan)
+        out_bytes = self._up(plan.total_q_tokens * kv.hq * kv.d * 2)
+        self._ensure(total, out_bytes)
+        h = self._host.numpy()
+        src = {"q": q_bits, "k": k_bits, "v": v_bits, "q_lens": plan.q_lens,
+               "q_offsets": plan.q_offsets, "context_lens": plan.context_lens,
+               "block_table": plan.block_table}
+        for name, (off, nbytes) in offs.items():
+            a = np.ascontiguousarray(src[name])
+            assert a.nbytes == nbytes, (name, a.nbytes, nbytes)
+            h[off:off + nbytes] = a.reshape(-1).view(np.uint8)
+        self.plan, self.offs, self.total = plan, offs, total
+        T = plan.total_q_tokens
+        d = self._dev
+        view = lambda name, dt, shape: d[offs[name][0]:offs[name][0] + offs[name][1]].view(dt) \
+            .view(shape)
+        self.q = view("q", kv.dtype, (T, kv.hq, kv.d))
+        self.k_new = view("k", kv.dtype, (T, kv.hkv, kv.d))
+        self.v_new = view("v", kv.dtype, (T, kv.hkv, kv.d))
+        meta = [view(n, torch.int32, (-1,)) for n in ("q_lens", "q_offsets", "context_lens")]
+        bt = view("block_table", torch.int32, (plan.num_reqs, plan.max_pages))
+        self.desc = binding.make_desc(
+            num_reqs=plan.num_reqs, num_q_heads=kv.hq, num_kv_heads=kv.hkv, head_dim=kv.d,
+            num_pages=kv.num_pages, max_pages_per_req=plan.max_pages,
+            total_q_tokens=T, max_q_len=plan.max_q_len, max_context_len=plan.max_context_len,
+            dtype=kv.dtype_code, q_lens=meta[0], q_offsets=meta[1], context_lens=meta[2],
+            block_table=bt)
+        self.out = self._out_dev[:T * kv.hq * kv.d * 2].view(kv.dtype).view(T, kv.hq, kv.d)
+        self.out_host = self._out_host[:T * kv.hq * kv.d * 2].view(kv.dtype) \
+            .view(T, kv.hq, kv.d)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return self.total
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.out.numel() * self.out.element_size()
+
+    def upload(self) -> None:
+        """Host -> device copy of the staged inputs on the current stream."""
+        self._dev[:self.total].copy_(self._host[:self.total], non_blocking=True)
+
+    def run(self, scale: float, stream=None) -> None:
+        """kv_append then the attention step, on the staged device views."""
+        binding.kv_append(self.desc, self.k_new, self.v_new, self.kv.k_cache, self.kv.v_cache,
+                          None, self.kv.err, stream)
+        ws = self.kv.workspace(self.desc)
+        binding.paged_attention_step(self.desc, self.q, self.kv.k_cache, self.kv.v_cache,
+                                     self.out, scale, ws, self.kv.err, stream)
+
+    def download(self) -> None:
+        """Device -> host copy of the step's output on the current stream."""
+        self.out_host.copy_(self.out, non_blocking=True)
+
+
 # ---------------------------------------------------------------------- workload glue
 def step_host_inputs(workload, plan: StepPlan):
     """(q, k_new, v_new) bit arrays for a step, gathered from the workload's sequences."""

@@ -155,6 +155,38 @@ def test_prefill_chunks_small(hq, hkv, d, dtype):
     run_all(custom(300 + hq + d, hq, hkv, d, dtype, specs, budget=160, chunk_cap=96))
 
 
+def test_step_staging_bitwise_identical():
+    # the packed one-copy staging (inputs in one pinned buffer, device views into one
+    # device buffer) gives the same output bits and pool bytes as separate uploads, over
+    # decode steps, prefill chunks and mixed steps
+    w = custom(500, 8, 2, 128, 0, [(40, 0, 3), (0, 70, 1), (300, 0, 2), (0, 20, 2)],
+               budget=48)
+    results = []
+    for staged in (False, True):
+        s = scheduler_for(w)
+        kv = runner.paged_kv_for(w)
+        runner.load_history(kv, w, s.history_plan())
+        stg = runner.StepStaging(kv)
+        outs = []
+        for plan in s.all_steps():
+            if staged:
+                stg.stage(plan, *runner.step_host_inputs(w, plan))
+                stg.upload()
+                stg.run(w.scale)
+                stg.download()
+                torch.cuda.synchronize()
+                # the pinned output buffer is reused by the next step: keep a copy
+                outs.append(runner.tensor_to_bits(stg.out_host).copy())
+            else:
+                outs.append(runner.tensor_to_bits(runner.run_step(kv, w, plan)))
+        assert kv.read_error() == 0
+        results.append((outs, pool_bits(kv)))
+    assert len(results[0][0]) == len(results[1][0]) > 2
+    for a, b in zip(results[0][0], results[1][0]):
+        assert np.array_equal(a, b)
+    assert all(np.array_equal(a, b) for a, b in zip(results[0][1], results[1][1]))
+
+
 def test_block_table_permutation_bitwise_identical():
     base = custom(400, 32, 8, 128, 0, [(c, 0, 1) for c in (50, 700, 2100, 16)])
     outs = []
