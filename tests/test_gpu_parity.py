@@ -187,6 +187,16 @@ def test_step_staging_bitwise_identical():
     assert all(np.array_equal(a, b) for a, b in zip(results[0][1], results[1][1]))
 
 
+def test_long_contexts():
+    # maximum-size rows: a decode row over 131,071 cached tokens (8,192 pages, about 900
+    # splits per (row, KV head), so the combine loops over many batches), one over 40,000,
+    # and a 300-token prefill chunk on a 70,000-token history (about 550 key tiles per query
+    # tile); every row is checked against the oracle
+    worst, _, _ = run_all(custom(600, 32, 8, 128, 0, [(131071, 0, 1), (40000, 0, 1),
+                                                      (70000, 300, 0)]))
+    assert worst[0] < 2e-2
+
+
 def test_block_table_permutation_bitwise_identical():
     base = custom(400, 32, 8, 128, 0, [(c, 0, 1) for c in (50, 700, 2100, 16)])
     outs = []
