@@ -8,6 +8,8 @@ algorithmic bytes of the step (K/V read by attention, Q read, output write, appe
 write, block-table reads) divided by the step time.  The secondary object "prefill_chunk"
 times the tensor-core-bound workload: one-shot causal prefill of 8,192 tokens (32/8 heads,
 d=128) and the same prompt as 4 x 2,048-token chunks, in TFLOP/s of causal attention FLOPs.
+The object "decode_loop" times 64 consecutive decode steps of the MHA-skew workload as
+separate steps, as one device-side loop and as one CUDA graph replay (per-step overhead).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -303,6 +305,55 @@ def time_prefill(device, reps=3):
     return res
 
 
+def time_decode_loop(device, reps=5):
+    """64 consecutive decode steps of the MHA-skew workload (16 requests, 32 heads, fp16):
+    per-step time as separate steps (metadata of every step already on the device, append +
+    attention launched from the host), as one device-side loop (lengths advanced on the
+    device) and as one CUDA graph replay of all 64 steps."""
+    from paged_kv_cache_token_gb300 import binding, runner
+    w = W.mha_skew()
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, device=device, fill_sentinel=False)
+    runner.load_history(kv, w, s.history_plan())
+    plans = s.all_steps()
+    nbytes = sum(step_bytes(w, p)["step"] for p in plans)
+    loop = runner.DecodeLoop(kv, w, plans)
+    loop.capture()
+    dsteps = [kv.upload(p) for p in plans]
+    ws = kv.workspace(loop.desc)
+    for ds in dsteps:
+        ws = kv.workspace(ds.desc)
+    stream = torch.cuda.current_stream()
+
+    def separate():
+        for i, ds in enumerate(dsteps):
+            binding.kv_append(ds.desc, loop.k_new[i], loop.v_new[i], kv.k_cache, kv.v_cache,
+                              None, kv.err, stream)
+            binding.paged_attention_step(ds.desc, loop.q[i], kv.k_cache, kv.v_cache,
+                                         loop.out[i], w.scale, ws, kv.err, stream)
+
+    res = {}
+    for name, fn in (("separate_steps", separate), ("device_loop", loop.run),
+                     ("graph", loop.replay)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b))
+        ms = float(np.median(t))
+        res[name] = {"us_per_step": ms * 1e3 / len(plans), "GBps": nbytes / (ms * 1e-3) / 1e9}
+    assert kv.read_error() == 0
+    res["steps"] = len(plans)
+    res["bytes_per_step"] = nbytes / len(plans)
+    return res
+
+
 # ------------------------------------------------------------------------------ oracle arm
 def oracle_decode_sample(n_req, min_seconds=0.0):
     """Time the fp64 oracle on the first n_req decode rows of the decode workload (all 32
@@ -398,7 +449,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill"], default=None,
+    ap.add_argument("--no-decode-loop", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode-loop"], default=None,
                     help="time only the prefill workload (one-shot 8K and 4 x 2K) and print "
                          "its JSON object; used for focused profiler captures")
     ap.add_argument("--pool-pages", type=int, default=70000,
@@ -421,6 +473,10 @@ def main():
             if dist_ctx.rank == 0:
                 pf = time_prefill(device)
                 print(json.dumps({"prefill_chunk": pf, "peak_tflops": bf16}))
+            return
+        if args.only == "decode-loop":
+            if dist_ctx.rank == 0:
+                print(json.dumps({"decode_loop": time_decode_loop(device)}))
             return
         r = time_decode(device, args.steps, args.warmup, dist_ctx, args.pool_pages)
         acct = r["acct"]
@@ -470,6 +526,15 @@ def main():
                              "flops_per_launch": one["flops"],
                              "traffic": captured_traffic("prefill_pair_kernel"),
                              "chunked_kernel_tflops": ch["flops"] / ch["main_kernel_ms"] / 1e9}}
+        if not args.no_decode_loop and dist_ctx.rank == 0:
+            dl = time_decode_loop(device)
+            line["decode_loop"] = {
+                "workload": "64 consecutive decode steps, 16 requests, ctx log-uniform 32-2048, "
+                            "32 q / 32 kv heads, d 128, fp16, pages handed out round-robin",
+                "note": "one layer's cache (~%.0f MB) is re-read every step and stays largely "
+                        "in L2, so GB/s here is not an HBM rate; the comparison is between "
+                        "launch modes" % (dl["bytes_per_step"] / 1e6),
+                **dl}
         if not args.no_cpu_baseline and dist_ctx.rank == 0:
             secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
             line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores,

@@ -117,6 +117,19 @@ PKV_API int pkv_kv_append(const pkv_step_desc* desc, const void* k_new, const vo
                   int32_t* dev_err_flag, void* stream);
 
 /*
+ * pkv_advance_context -- context_lens[r] += q_lens[r] for every request of *desc, on the
+ * device.  After a step the tokens it appended are cached, so the next step of the same
+ * batch starts from the grown lengths (niuwancheng.cn "11. Chunked prefill and unified
+ * scheduling": each request records the tokens computed so far).  With it, consecutive
+ * steps of one batch need no host upload between them and can be captured in one CUDA
+ * graph; the block table must already hold the pages the later steps reach.
+ *   context_lens   device int32 [num_reqs], updated in place (normally desc->context_lens)
+ * Errors: INVALID_ARG, CUDA.  num_reqs == 0 is a no-op returning PKV_OK.  The kernel waits
+ * for earlier kernels on the stream that read the lengths before it writes them.
+ */
+PKV_API int pkv_advance_context(const pkv_step_desc* desc, int32_t* context_lens, void* stream);
+
+/*
  * pkv_attention_workspace_bytes -- device workspace the attention step needs for this
  * description (split-KV partial results and the device-built work list).  Depends only
  * on the host integers of *desc and on the current device's SM count.  Returns 0 for

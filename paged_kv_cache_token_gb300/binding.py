@@ -25,9 +25,9 @@ DEVERR_PAGE_RANGE, DEVERR_TABLE_RANGE, DEVERR_TOKENS, DEVERR_TIMEOUT = 1, 2, 4, 
 BF16, FP16 = 0, 1
 DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16}
 
-EXPORTED = ("pkv_kv_append", "pkv_attention_workspace_bytes", "pkv_paged_attention_step",
-            "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
-            "pkv_version")
+EXPORTED = ("pkv_kv_append", "pkv_advance_context", "pkv_attention_workspace_bytes",
+            "pkv_paged_attention_step", "pkv_read_device_error", "pkv_set_kernel_events",
+            "pkv_status_string", "pkv_version")
 
 
 class PkvError(RuntimeError):
@@ -66,6 +66,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     V, sz = ctypes.c_void_p, ctypes.c_size_t
     lib.pkv_kv_append.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V, V]
     lib.pkv_kv_append.restype = ctypes.c_int
+    lib.pkv_advance_context.argtypes = [ctypes.POINTER(StepDesc), V, V]
+    lib.pkv_advance_context.restype = ctypes.c_int
     lib.pkv_attention_workspace_bytes.argtypes = [ctypes.POINTER(StepDesc)]
     lib.pkv_attention_workspace_bytes.restype = sz
     lib.pkv_paged_attention_step.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V,
@@ -126,6 +128,14 @@ def kv_append(desc: StepDesc, k_new, v_new, k_cache, v_cache, slot_mapping=None,
                               _ptr(v_cache), _ptr(slot_mapping), _ptr(err), _stream(stream))
     if check and rc != OK:
         raise PkvError("pkv_kv_append", rc)
+    return rc
+
+
+def advance_context(desc: StepDesc, context_lens, stream=None, check: bool = True) -> int:
+    """context_lens[r] += q_lens[r] on the device (context_lens: int32 CUDA tensor)."""
+    rc = load().pkv_advance_context(ctypes.byref(desc), _ptr(context_lens), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_advance_context", rc)
     return rc
 
 

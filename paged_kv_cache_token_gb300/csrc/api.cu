@@ -120,6 +120,16 @@ int pkv_kv_append(const pkv_step_desc* desc, const void* k_new, const void* v_ne
     return pkv::launch_kv_append(a, static_cast<cudaStream_t>(stream));
 }
 
+int pkv_advance_context(const pkv_step_desc* desc, int32_t* context_lens, void* stream) {
+    const int rc = check_desc(desc);
+    if (rc != PKV_OK) return rc;
+    if (desc->num_reqs == 0) return PKV_OK;
+    if (!context_lens || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PKV_ERR_INVALID_ARG;
+    return pkv::launch_advance_context(desc->q_lens, context_lens, desc->num_reqs,
+                                       static_cast<cudaStream_t>(stream));
+}
+
 size_t pkv_attention_workspace_bytes(const pkv_step_desc* desc) {
     if (check_desc(desc) != PKV_OK) return 0;
     const int sms = num_sms_current_device();

@@ -72,6 +72,25 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
     }
 }
 
+// context_lens[r] += q_lens[r]: the step's tokens are now cached.  Earlier kernels on the
+// stream (the attention step) read the lengths, so the update waits for them.
+__global__ void __launch_bounds__(256) advance_context_kernel(const int32_t* q_lens,
+                                                              int32_t* context_lens, int n) {
+    pdl_wait();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < n) context_lens[r] += q_lens[r];
+    pdl_trigger();
+}
+
+int launch_advance_context(const int32_t* q_lens, int32_t* context_lens, int num_reqs,
+                           cudaStream_t stream) {
+    if (num_reqs == 0) return PKV_OK;
+    return launch_pdl(advance_context_kernel, dim3(cdiv(num_reqs, 256)), dim3(256), 0, stream,
+                      q_lens, context_lens, num_reqs) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
     if (a.total_q_tokens == 0 || a.num_reqs == 0) return PKV_OK;
     if (a.num_reqs > 65535) return PKV_ERR_UNSUPPORTED;

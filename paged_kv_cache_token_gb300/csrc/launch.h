@@ -85,6 +85,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+int launch_advance_context(const int32_t* q_lens, int32_t* context_lens, int num_reqs,
+                           cudaStream_t stream);
 int launch_plan(const StepArgs& a, cudaStream_t stream);
 // ev_start / ev_stop (may be null) are recorded around the main kernel only.
 int launch_decode(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,

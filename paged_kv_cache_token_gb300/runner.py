@@ -200,6 +200,80 @@ class StepStaging:
         self.out_host.copy_(self.out, non_blocking=True)
 
 
+class DecodeLoop:
+    """Consecutive steps of one batch run as one device-side sequence.
+
+    Every step is kv_append, the attention step and pkv_advance_context (context_lens +=
+    q_lens), so no metadata crosses from the host between steps; the block table is the
+    last step's, which already holds every page the earlier steps reach.  Each step's Q,
+    K_new, V_new are staged on the device up front and each step's output has its own slot.
+    ``capture`` records the whole sequence in one CUDA graph (the lengths are reset at its
+    start, so it can be replayed); ``replay`` then runs all steps with one launch.
+    """
+
+    def __init__(self, kv: PagedKV, workload, plans):
+        if not plans:
+            raise ValueError("no steps")
+        p0, pl = plans[0], plans[-1]
+        for i, p in enumerate(plans):
+            if (list(p.rids) != list(p0.rids) or not np.array_equal(p.q_lens, p0.q_lens)
+                    or not np.array_equal(p.context_lens, p0.context_lens + i * p0.q_lens)):
+                raise ValueError("plans are not consecutive steps of one batch")
+            for r in range(p.num_reqs):
+                n = -(-(int(p.context_lens[r]) + int(p.q_lens[r])) // 16)
+                if not np.array_equal(p.block_table[r, :n], pl.block_table[r, :n]):
+                    raise ValueError("block tables of the steps disagree")
+        self.kv, self.scale, self.steps = kv, workload.scale, len(plans)
+        dev = kv.device
+        ins = [step_host_inputs(workload, p) for p in plans]
+        stack = lambda i: bits_to_tensor(np.stack([x[i] for x in ins]), workload.dtype, dev)
+        self.q, self.k_new, self.v_new = stack(0), stack(1), stack(2)
+        T = p0.total_q_tokens
+        self.out = torch.empty((self.steps, T, kv.hq, kv.d), dtype=kv.dtype, device=dev)
+        self.q_lens = torch.from_numpy(p0.q_lens).to(dev)
+        self.q_offsets = torch.from_numpy(p0.q_offsets).to(dev)
+        self.ctx0 = torch.from_numpy(p0.context_lens).to(dev)
+        self.ctx = self.ctx0.clone()
+        self.block_table = torch.from_numpy(np.ascontiguousarray(pl.block_table)).to(dev)
+        self.desc = binding.make_desc(
+            num_reqs=p0.num_reqs, num_q_heads=kv.hq, num_kv_heads=kv.hkv, head_dim=kv.d,
+            num_pages=kv.num_pages, max_pages_per_req=pl.max_pages, total_q_tokens=T,
+            max_q_len=p0.max_q_len, max_context_len=pl.max_context_len, dtype=kv.dtype_code,
+            q_lens=self.q_lens, q_offsets=self.q_offsets, context_lens=self.ctx,
+            block_table=self.block_table)
+        self.ws = kv.workspace(self.desc)
+        self.graph = None
+
+    def _body(self, stream=None) -> None:
+        kv = self.kv
+        self.ctx.copy_(self.ctx0, non_blocking=True)
+        for s in range(self.steps):
+            binding.kv_append(self.desc, self.k_new[s], self.v_new[s], kv.k_cache, kv.v_cache,
+                              None, kv.err, stream)
+            binding.paged_attention_step(self.desc, self.q[s], kv.k_cache, kv.v_cache,
+                                         self.out[s], self.scale, self.ws, kv.err, stream)
+            binding.advance_context(self.desc, self.ctx, stream)
+
+    def run(self) -> torch.Tensor:
+        """All steps, launched one call at a time on the current stream."""
+        self._body()
+        return self.out
+
+    def capture(self) -> None:
+        """Record all steps in one CUDA graph (after one eager run, which sets up the
+        library's per-kernel attributes outside the capture)."""
+        self.run()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._body()
+        torch.cuda.synchronize()
+
+    def replay(self) -> torch.Tensor:
+        self.graph.replay()
+        return self.out
+
+
 # ---------------------------------------------------------------------- workload glue
 def step_host_inputs(workload, plan: StepPlan):
     """(q, k_new, v_new) bit arrays for a step, gathered from the workload's sequences."""

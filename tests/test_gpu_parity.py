@@ -197,6 +197,40 @@ def test_long_contexts():
     assert worst[0] < 2e-2
 
 
+def test_decode_loop_and_graph_bitwise_identical():
+    # the MHA-skew workload's 64 decode steps (16 requests, fp16, page boundaries crossed
+    # mid-run) as 64 separate steps, as one device-side loop (lengths advanced on the
+    # device, the last step's block table) and as one CUDA graph replay: same output bits
+    # and pool bytes
+    w = W.mha_skew()
+
+    def fresh():
+        s = scheduler_for(w)
+        kv = runner.paged_kv_for(w)
+        runner.load_history(kv, w, s.history_plan())
+        return s, kv
+
+    s, kv = fresh()
+    plans = s.all_steps()
+    ref = torch.stack([runner.run_step(kv, w, p) for p in plans])
+    ref_pool = pool_bits(kv)
+    for mode in ("loop", "graph"):
+        s, kv = fresh()
+        loop = runner.DecodeLoop(kv, w, plans)
+        if mode == "loop":
+            out = loop.run()
+        else:
+            loop.capture()
+            kv.k_cache.view(torch.int16).fill_(-1)  # replay must rewrite every appended slot
+            kv.v_cache.view(torch.int16).fill_(-1)
+            runner.load_history(kv, w, scheduler_for(w).history_plan())
+            out = loop.replay()
+        torch.cuda.synchronize()
+        assert kv.read_error() == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), mode
+        assert all(np.array_equal(a, b) for a, b in zip(pool_bits(kv), ref_pool)), mode
+
+
 def test_block_table_permutation_bitwise_identical():
     base = custom(400, 32, 8, 128, 0, [(c, 0, 1) for c in (50, 700, 2100, 16)])
     outs = []
