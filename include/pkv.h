@@ -63,7 +63,8 @@ typedef enum {
     PKV_ERR_CAPACITY = -3,        /* max_context_len + max_q_len beyond the block table */
     PKV_ERR_WORKSPACE = -4,       /* workspace NULL or smaller than required */
     PKV_ERR_CUDA = -5,            /* a CUDA runtime call or launch failed */
-    PKV_ERR_DEVICE = -6           /* pkv_read_device_error found a non-zero flag */
+    PKV_ERR_DEVICE = -6,          /* pkv_read_device_error found a non-zero flag */
+    PKV_ERR_NO_PAGES = -7         /* the scheduler's page pool cannot cover the step */
 } pkv_status;
 
 /* Bits OR-ed into *dev_err_flag by the kernels. */

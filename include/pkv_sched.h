@@ -1,0 +1,103 @@
+/*
+ * pkv_sched.h -- C ABI of the host-side step planner and page allocator (libpkv.so).
+ *
+ * The planner of a unified prefill/decode scheduler, as niuwancheng.cn "11. Chunked
+ * prefill and unified scheduling" describes it (section "token budget per step"):
+ *  - every request records the tokens already computed (cached) and the tokens it needs;
+ *  - each step gives every decoding request 1 token first, then prefilling requests take
+ *    min(remaining input, remaining budget) (optionally capped per chunk) in request order;
+ *  - a step never exceeds the token budget.
+ * Pages hold 16 tokens (lshu.cn/news/11576 §2.3) and come from a free list as a request's
+ * cached length crosses a page boundary (§2.2: K/V written by page index).  A plan is
+ * written straight into the arrays pkv_kv_append and pkv_paged_attention_step consume.
+ *
+ * Host code only: no CUDA call, safe to use without a GPU.  A scheduler handle is not
+ * thread-safe; use one per thread or lock around it.  Every call that plans a step either
+ * succeeds completely or leaves the scheduler exactly as it was.
+ */
+#ifndef PKV_SCHED_H_
+#define PKV_SCHED_H_
+
+#include "pkv.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_scheduler pkv_scheduler;  /* opaque */
+
+/*
+ * One planned step, written into caller-owned host arrays.
+ *   in:  max_reqs            capacity of rids, q_lens, context_lens (q_offsets: +1)
+ *        max_pages_per_req   row stride of block_table (pass it as the step
+ *                            description's max_pages_per_req)
+ *        rids .. block_table host arrays of those capacities
+ *   out: num_reqs            requests in the step, in launch order
+ *        total_q_tokens      sum of q_lens
+ *        max_q_len, max_context_len
+ *        pages_used          longest block-table row of the step (<= max_pages_per_req)
+ * block_table row i holds request i's physical pages, -1 past its last page.
+ */
+typedef struct {
+    int32_t max_reqs;
+    int32_t max_pages_per_req;
+    int32_t* rids;
+    int32_t* q_lens;
+    int32_t* context_lens;
+    int32_t* q_offsets;
+    int32_t* block_table;
+    int32_t num_reqs;
+    int32_t total_q_tokens;
+    int32_t max_q_len;
+    int32_t max_context_len;
+    int32_t pages_used;
+} pkv_plan;
+
+/*
+ * pkv_sched_create -- a planner over a pool of num_pages pages, handed out in
+ * page_order[0..num_pages) (NULL: 0, 1, 2, ...), with a per-step token budget (> 0) and
+ * an optional per-request chunk cap (0: none).  Returns NULL on bad arguments or when
+ * memory runs out.
+ */
+PKV_API pkv_scheduler* pkv_sched_create(int32_t num_pages, const int32_t* page_order,
+                                        int32_t budget, int32_t chunk_cap);
+PKV_API void pkv_sched_destroy(pkv_scheduler* s);
+
+/*
+ * pkv_sched_add_request -- append a request: `history` tokens already cached elsewhere
+ * (loaded by pkv_sched_history_plan), then `prompt` input tokens to prefill, then
+ * `decodes` generated tokens.  rid must be new.  Errors: INVALID_ARG.
+ */
+PKV_API int pkv_sched_add_request(pkv_scheduler* s, int32_t rid, int32_t history,
+                                  int32_t prompt, int32_t decodes);
+
+/*
+ * pkv_sched_history_plan -- the append that loads every request's cached history
+ * (q_len = history, context_len = 0), pages taken request by request, or round-robin one
+ * page at a time across requests when `interleave` is non-zero.  Marks the history
+ * computed.  Returns 1 with *out filled, 0 when no request has history, or INVALID_ARG,
+ * CAPACITY (out arrays too small), NO_PAGES.
+ */
+PKV_API int pkv_sched_history_plan(pkv_scheduler* s, int interleave, pkv_plan* out);
+
+/*
+ * pkv_sched_next_step -- plan the next step (decodes first, then prefill chunks within the
+ * budget), take the pages it reaches and advance the requests as if it ran.  Returns 1 with
+ * *out filled, 0 when every request is done, or INVALID_ARG, CAPACITY, NO_PAGES.
+ */
+PKV_API int pkv_sched_next_step(pkv_scheduler* s, pkv_plan* out);
+
+/*
+ * pkv_sched_release -- return a finished request's pages to the end of the free list and
+ * forget the request.  Errors: INVALID_ARG (unknown rid or request not finished).
+ */
+PKV_API int pkv_sched_release(pkv_scheduler* s, int32_t rid);
+
+/* Pages currently on the free list (-1 for a NULL handle). */
+PKV_API int32_t pkv_sched_free_pages(const pkv_scheduler* s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* PKV_SCHED_H_ */

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 OK = 0
 STATUS = {0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED",
           -3: "PKV_ERR_CAPACITY", -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_CUDA",
-          -6: "PKV_ERR_DEVICE"}
+          -6: "PKV_ERR_DEVICE", -7: "PKV_ERR_NO_PAGES"}
 DEVERR_PAGE_RANGE, DEVERR_TABLE_RANGE, DEVERR_TOKENS, DEVERR_TIMEOUT = 1, 2, 4, 8
 BF16, FP16 = 0, 1
 DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16}

@@ -1,7 +1,7 @@
 """Build libpkv.so (the C-ABI CUDA library) in-tree for sm_103a.
 
-Each .cu under csrc/ compiles to an object in parallel, then one link step makes
-paged_kv_cache_token_gb300/libpkv.so.  Only nvcc and the host compiler are needed.
+Each .cu (and host-only .cpp) under csrc/ compiles to an object in parallel, then one link
+step makes paged_kv_cache_token_gb300/libpkv.so.  Only nvcc and the host compiler are needed.
 """
 import concurrent.futures as cf
 import glob
@@ -21,7 +21,8 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompil
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    # .cu: device code; .cpp: host-only parts of the library (nvcc hands them to g++)
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _headers():
@@ -41,7 +42,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     headers = _headers()
     objs, jobs = [], []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             cmd = [NVCC, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]

@@ -84,6 +84,7 @@ const char* pkv_status_string(int status) {
         case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
         case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
         case PKV_ERR_DEVICE: return "PKV_ERR_DEVICE";
+        case PKV_ERR_NO_PAGES: return "PKV_ERR_NO_PAGES";
         default: return "PKV_UNKNOWN_STATUS";
     }
 }

@@ -1,0 +1,126 @@
+"""Python face of the native step planner and page allocator (include/pkv_sched.h).
+
+Same interface as :class:`scheduler.Scheduler` (``history_plan``, ``next_step``,
+``all_steps``) and the same plans; the planning runs in the library's C++ code.  Adds
+``release`` (return a finished request's pages to the free list) and ``num_free``.
+Host code only: usable without a GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional
+
+import numpy as np
+
+from . import binding
+from .scheduler import StepPlan
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+class _Plan(ctypes.Structure):
+    """Mirror of ``pkv_plan``."""
+    _fields_ = [("max_reqs", ctypes.c_int32), ("max_pages_per_req", ctypes.c_int32),
+                ("rids", _I32P), ("q_lens", _I32P), ("context_lens", _I32P),
+                ("q_offsets", _I32P), ("block_table", _I32P),
+                ("num_reqs", ctypes.c_int32), ("total_q_tokens", ctypes.c_int32),
+                ("max_q_len", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
+                ("pages_used", ctypes.c_int32)]
+
+
+def _lib():
+    lib = binding.load()
+    if not getattr(lib, "_pkv_sched_ready", False):
+        V = ctypes.c_void_p
+        lib.pkv_sched_create.argtypes = [ctypes.c_int32, V, ctypes.c_int32, ctypes.c_int32]
+        lib.pkv_sched_create.restype = V
+        lib.pkv_sched_destroy.argtypes = [V]
+        lib.pkv_sched_destroy.restype = None
+        lib.pkv_sched_add_request.argtypes = [V] + [ctypes.c_int32] * 4
+        lib.pkv_sched_add_request.restype = ctypes.c_int
+        lib.pkv_sched_history_plan.argtypes = [V, ctypes.c_int, ctypes.POINTER(_Plan)]
+        lib.pkv_sched_history_plan.restype = ctypes.c_int
+        lib.pkv_sched_next_step.argtypes = [V, ctypes.POINTER(_Plan)]
+        lib.pkv_sched_next_step.restype = ctypes.c_int
+        lib.pkv_sched_release.argtypes = [V, ctypes.c_int32]
+        lib.pkv_sched_release.restype = ctypes.c_int
+        lib.pkv_sched_free_pages.argtypes = [V]
+        lib.pkv_sched_free_pages.restype = ctypes.c_int32
+        lib._pkv_sched_ready = True
+    return lib
+
+
+class NativeScheduler:
+    """Token-budget planner over requests sharing one page pool (C++ implementation)."""
+
+    def __init__(self, requests, page_order, budget: int, chunk_cap: Optional[int] = None,
+                 interleave_history: bool = False):
+        self._lib = _lib()
+        order = np.ascontiguousarray(np.asarray(page_order, dtype=np.int32))
+        self._h = self._lib.pkv_sched_create(len(order), order.ctypes.data_as(ctypes.c_void_p),
+                                             int(budget), int(chunk_cap or 0))
+        if not self._h:
+            raise ValueError("bad scheduler arguments")
+        self._interleave = interleave_history
+        self.max_reqs = 0
+        self.max_pages = 1
+        for r in requests:
+            self.add_request(r.rid, r.history, r.prompt, r.decodes)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.pkv_sched_destroy(h)
+
+    def add_request(self, rid: int, history: int, prompt: int, decodes: int) -> None:
+        rc = self._lib.pkv_sched_add_request(self._h, rid, history, prompt, decodes)
+        if rc != binding.OK:
+            raise binding.PkvError("pkv_sched_add_request", rc)
+        self.max_reqs += 1
+        self.max_pages = max(self.max_pages, -(-(history + prompt + decodes) // 16))
+
+    def _call(self, fn, *args) -> Optional[StepPlan]:
+        R, P = max(1, self.max_reqs), self.max_pages
+        arr = {n: np.zeros(R + (n == "q_offsets"), np.int32)
+               for n in ("rids", "q_lens", "context_lens", "q_offsets")}
+        bt = np.zeros(R * P, np.int32)
+        ptr = lambda a: a.ctypes.data_as(_I32P)
+        plan = _Plan(R, P, ptr(arr["rids"]), ptr(arr["q_lens"]), ptr(arr["context_lens"]),
+                     ptr(arr["q_offsets"]), ptr(bt), 0, 0, 0, 0, 0)
+        rc = fn(self._h, *args, ctypes.byref(plan))
+        if rc < 0:
+            raise binding.PkvError(fn.__name__, rc)
+        if rc == 0:
+            return None
+        n, w = plan.num_reqs, max(1, plan.pages_used)
+        return StepPlan([int(x) for x in arr["rids"][:n]], arr["q_lens"][:n].copy(),
+                        arr["context_lens"][:n].copy(), arr["q_offsets"][:n + 1].copy(),
+                        np.ascontiguousarray(bt.reshape(R, P)[:n, :w]))
+
+    def history_plan(self) -> Optional[StepPlan]:
+        return self._call(self._lib.pkv_sched_history_plan, 1 if self._interleave else 0)
+
+    def next_step(self) -> Optional[StepPlan]:
+        return self._call(self._lib.pkv_sched_next_step)
+
+    def all_steps(self) -> List[StepPlan]:
+        out = []
+        while True:
+            p = self.next_step()
+            if p is None:
+                return out
+            out.append(p)
+
+    def release(self, rid: int) -> None:
+        rc = self._lib.pkv_sched_release(self._h, rid)
+        if rc != binding.OK:
+            raise binding.PkvError("pkv_sched_release", rc)
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pkv_sched_free_pages(self._h))
+
+
+def native_scheduler_for(workload) -> NativeScheduler:
+    return NativeScheduler(workload.requests, workload.page_order, workload.budget,
+                           workload.chunk_cap, workload.interleave_history)
