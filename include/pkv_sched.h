@@ -88,13 +88,43 @@ PKV_API int pkv_sched_history_plan(pkv_scheduler* s, int interleave, pkv_plan* o
 PKV_API int pkv_sched_next_step(pkv_scheduler* s, pkv_plan* out);
 
 /*
- * pkv_sched_release -- return a finished request's pages to the end of the free list and
- * forget the request.  Errors: INVALID_ARG (unknown rid or request not finished).
+ * pkv_sched_release -- return a finished request's pages to the end of the free list (its
+ * shared prefix blocks: its references to them) and forget the request.
+ * Errors: INVALID_ARG (unknown rid or request not finished).
  */
 PKV_API int pkv_sched_release(pkv_scheduler* s, int32_t rid);
 
 /* Pages currently on the free list (-1 for a NULL handle). */
 PKV_API int32_t pkv_sched_free_pages(const pkv_scheduler* s);
+
+/*
+ * Prefix caching (hotelren.com/news/6181127 §4.3): the K/V of prompt tokens already
+ * computed for one request are reused by later requests whose prompt starts with exactly
+ * the same token ids.
+ *  - Caching works on full 16-token blocks of prompt tokens.  Once a step covers a block,
+ *    the block is registered under its token ids and those of every block before it, and
+ *    its page becomes shared.
+ *  - A new prompt reuses the longest run of registered blocks that matches its leading
+ *    token ids exactly (ids are compared, not only hashed).  At least one prompt token is
+ *    always left to compute.  The request starts with context_len = the reused tokens, so
+ *    new tokens continue the positions.
+ *  - Shared blocks are reference-counted.  A request's release returns its references;
+ *    blocks nobody uses stay cached and are evicted least-recently-used first, block by
+ *    block, only when the free list is empty.
+ *  - Shared pages are always full, so no step ever writes into one.
+ */
+
+/*
+ * pkv_sched_add_prompt -- append a request whose `n_prompt` prompt token ids are known,
+ * followed by `decodes` generated tokens; it takes part in prefix caching.  Returns the
+ * number of prompt tokens reused from the cache (a multiple of 16, >= 0), or INVALID_ARG.
+ */
+PKV_API int pkv_sched_add_prompt(pkv_scheduler* s, int32_t rid, const int32_t* tokens,
+                                 int32_t n_prompt, int32_t decodes);
+
+/* Registered blocks: all of them, and those no request uses (evictable).  -1 for NULL. */
+PKV_API int32_t pkv_sched_cached_blocks(const pkv_scheduler* s);
+PKV_API int32_t pkv_sched_evictable_blocks(const pkv_scheduler* s);
 
 #ifdef __cplusplus
 }

@@ -10,9 +10,15 @@
 // Every planning call first works out the whole step (requests, lengths, pages it needs)
 // without touching the scheduler, checks the caller's arrays and the free list, and only
 // then takes pages and advances the requests, so a failed call changes nothing.
+//
+// Prefix caching, hotelren.com/news/6181127 §4.3: K/V of prompt tokens are reused by later
+// requests whose prompt starts with exactly the same token ids; memory is managed in
+// blocks (pages) and unused blocks are evicted least-recently-used, block by block.
 #include <algorithm>
+#include <array>
 #include <cstdint>
 #include <deque>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <utility>
@@ -28,6 +34,11 @@ int64_t pages_for(int64_t tokens) { return (tokens + kPage - 1) / kPage; }
 
 struct Req {
     int32_t rid = 0;
+    bool cached = false;              // takes part in prefix caching (prompt ids known)
+    std::vector<int32_t> tokens;      // prompt token ids of a cached request
+    std::vector<uint64_t> block_of;   // per page: key of the shared block it holds, or 0
+    int64_t registered = 0;           // prompt blocks already matched or registered
+    uint64_t chain = 0;               // key of the last of them (0: none)
     int64_t history = 0;
     int64_t prompt_end = 0;  // history + prompt: positions below are input, not generated
     int64_t total = 0;       // every position the request will ever hold
@@ -38,6 +49,30 @@ struct Req {
     bool prefilling() const { return computed < prompt_end; }
     bool done() const { return computed >= total; }
 };
+
+// A shared prompt block: its page, how many requests hold it, the key of the block before
+// it and its own token ids (compared on every match, so a key collision cannot alias).
+struct Block {
+    int32_t page = -1;
+    int32_t refs = 0;
+    uint64_t parent = 0;
+    std::array<int32_t, 16> tokens{};
+    std::list<uint64_t>::iterator lru;  // valid while refs == 0
+};
+
+// Key of a block from the key of the block before it and its 16 token ids (splitmix64
+// steps); 0 is reserved for "no block".
+uint64_t block_key(uint64_t parent, const int32_t* t) {
+    uint64_t h = parent ^ 0x9e3779b97f4a7c15ull;
+    for (int i = 0; i < 16; ++i) {
+        h ^= static_cast<uint32_t>(t[i]);
+        h += 0x9e3779b97f4a7c15ull;
+        h = (h ^ (h >> 30)) * 0xbf58476d1ce4e5b9ull;
+        h = (h ^ (h >> 27)) * 0x94d049bb133111ebull;
+        h ^= h >> 31;
+    }
+    return h ? h : 1;
+}
 
 // one request of a planned step: index into reqs, tokens it advances, pages it will hold
 struct Pick {
@@ -54,6 +89,63 @@ struct pkv_scheduler {
     int64_t chunk_cap = 0;  // 0: no cap
     std::vector<Req> reqs;  // in the order they were added
     std::unordered_map<int32_t, size_t> index;
+    std::unordered_map<uint64_t, Block> blocks;  // shared prompt blocks by key
+    std::list<uint64_t> lru;                      // unreferenced blocks, least recent first
+
+    int64_t available() const {
+        return static_cast<int64_t>(free_list.size()) + static_cast<int64_t>(lru.size());
+    }
+
+    // a page from the free list, else the least recently used unreferenced block's
+    int32_t take_page() {
+        if (!free_list.empty()) {
+            const int32_t p = free_list.front();
+            free_list.pop_front();
+            return p;
+        }
+        const uint64_t key = lru.front();
+        lru.pop_front();
+        const auto it = blocks.find(key);
+        const int32_t p = it->second.page;
+        blocks.erase(it);
+        return p;
+    }
+
+    // the block matching (parent, tokens) exactly, or nullptr
+    Block* find_block(uint64_t key, uint64_t parent, const int32_t* t) {
+        const auto it = blocks.find(key);
+        if (it == blocks.end() || it->second.parent != parent ||
+            !std::equal(t, t + 16, it->second.tokens.begin()))
+            return nullptr;
+        return &it->second;
+    }
+
+    // Register the prompt blocks a step has just completed: each becomes shared unless an
+    // identical block is already registered (then this request keeps its page private and
+    // stops registering, since later blocks would hang off a page it does not share).
+    void register_blocks(Req& r) {
+        const int64_t full = std::min(r.computed, r.prompt_end) / kPage;
+        while (r.registered < full) {
+            const int64_t b = r.registered;
+            if (r.block_of[static_cast<size_t>(b)] == 0) {
+                const int32_t* t = r.tokens.data() + b * kPage;
+                const uint64_t key = block_key(r.chain, t);
+                if (blocks.count(key)) {
+                    r.registered = INT64_MAX;
+                    return;
+                }
+                Block blk;
+                blk.page = r.pages[static_cast<size_t>(b)];
+                blk.refs = 1;
+                blk.parent = r.chain;
+                std::copy(t, t + 16, blk.tokens.begin());
+                blocks.emplace(key, blk);
+                r.block_of[static_cast<size_t>(b)] = key;
+            }
+            r.chain = r.block_of[static_cast<size_t>(b)];
+            ++r.registered;
+        }
+    }
 
     void reindex() {
         index.clear();
@@ -77,7 +169,7 @@ struct pkv_scheduler {
             max_ctx = std::max(max_ctx, r.computed);
         }
         if (total_q > INT32_MAX || max_ctx > INT32_MAX) return PKV_ERR_CAPACITY;
-        if (need > static_cast<int64_t>(free_list.size())) return PKV_ERR_NO_PAGES;
+        if (need > available()) return PKV_ERR_NO_PAGES;
         return PKV_OK;
     }
 
@@ -100,8 +192,8 @@ struct pkv_scheduler {
             const Pick& p = picks[k];
             Req& r = reqs[p.i];
             while (static_cast<int64_t>(r.pages.size()) < p.pages_after) {
-                r.pages.push_back(free_list.front());
-                free_list.pop_front();
+                r.pages.push_back(take_page());
+                r.block_of.push_back(0);
             }
             out->rids[k] = r.rid;
             out->q_lens[k] = static_cast<int32_t>(p.n);
@@ -126,6 +218,7 @@ struct pkv_scheduler {
             } else {
                 r.computed += p.n;
             }
+            if (r.cached && r.registered != INT64_MAX) register_blocks(r);
         }
         return 1;
     }
@@ -162,7 +255,12 @@ int pkv_sched_add_request(pkv_scheduler* s, int32_t rid, int32_t history, int32_
         r.total = r.prompt_end + decodes;
         r.history_pending = history > 0;
         s->reqs.push_back(std::move(r));
-        s->index[rid] = s->reqs.size() - 1;
+        try {
+            s->index[rid] = s->reqs.size() - 1;
+        } catch (...) {
+            s->reqs.pop_back();
+            throw;
+        }
         return PKV_OK;
     } catch (...) {
         return PKV_ERR_CAPACITY;
@@ -187,8 +285,8 @@ int pkv_sched_history_plan(pkv_scheduler* s, int interleave, pkv_plan* out) {
             for (const Pick& p : picks) {
                 Req& r = s->reqs[p.i];
                 if (static_cast<int64_t>(r.pages.size()) < p.pages_after) {
-                    r.pages.push_back(s->free_list.front());
-                    s->free_list.pop_front();
+                    r.pages.push_back(s->take_page());
+                    r.block_of.push_back(0);
                     more = true;
                 }
             }
@@ -233,7 +331,15 @@ int pkv_sched_release(pkv_scheduler* s, int32_t rid) {
     if (it == s->index.end() || !s->reqs[it->second].done()) return PKV_ERR_INVALID_ARG;
     try {
         Req& r = s->reqs[it->second];
-        for (int32_t p : r.pages) s->free_list.push_back(p);
+        for (size_t i = 0; i < r.pages.size(); ++i) {
+            const uint64_t key = i < r.block_of.size() ? r.block_of[i] : 0;
+            if (key == 0) {
+                s->free_list.push_back(r.pages[i]);
+                continue;
+            }
+            Block& blk = s->blocks.at(key);
+            if (--blk.refs == 0) blk.lru = s->lru.insert(s->lru.end(), key);
+        }
         s->reqs.erase(s->reqs.begin() + static_cast<std::ptrdiff_t>(it->second));
         s->reindex();
         return PKV_OK;
@@ -244,6 +350,58 @@ int pkv_sched_release(pkv_scheduler* s, int32_t rid) {
 
 int32_t pkv_sched_free_pages(const pkv_scheduler* s) {
     return s ? static_cast<int32_t>(s->free_list.size()) : -1;
+}
+
+int pkv_sched_add_prompt(pkv_scheduler* s, int32_t rid, const int32_t* tokens,
+                         int32_t n_prompt, int32_t decodes) {
+    if (!s || n_prompt < 0 || decodes < 0 || (n_prompt > 0 && !tokens))
+        return PKV_ERR_INVALID_ARG;
+    if (s->index.count(rid)) return PKV_ERR_INVALID_ARG;
+    try {
+        Req r;
+        r.rid = rid;
+        r.cached = true;
+        r.tokens.assign(tokens, tokens + n_prompt);
+        r.prompt_end = n_prompt;
+        r.total = static_cast<int64_t>(n_prompt) + decodes;
+        // longest run of registered blocks matching the prompt, leaving >= 1 token to run
+        const int64_t max_blocks = n_prompt > 0 ? (n_prompt - 1) / kPage : 0;
+        std::vector<Block*> hit;
+        uint64_t parent = 0;
+        for (int64_t b = 0; b < max_blocks; ++b) {
+            const int32_t* t = r.tokens.data() + b * kPage;
+            const uint64_t key = block_key(parent, t);
+            Block* blk = s->find_block(key, parent, t);
+            if (!blk) break;
+            hit.push_back(blk);
+            r.pages.push_back(blk->page);
+            r.block_of.push_back(key);
+            parent = key;
+        }
+        r.registered = static_cast<int64_t>(hit.size());
+        r.chain = parent;
+        r.computed = r.registered * kPage;
+        s->reqs.push_back(std::move(r));
+        try {
+            s->index[rid] = s->reqs.size() - 1;
+        } catch (...) {
+            s->reqs.pop_back();
+            throw;
+        }
+        for (Block* blk : hit)  // nothing can fail any more: take the references
+            if (blk->refs++ == 0) s->lru.erase(blk->lru);
+        return static_cast<int>(hit.size() * kPage);
+    } catch (...) {
+        return PKV_ERR_CAPACITY;
+    }
+}
+
+int32_t pkv_sched_cached_blocks(const pkv_scheduler* s) {
+    return s ? static_cast<int32_t>(s->blocks.size()) : -1;
+}
+
+int32_t pkv_sched_evictable_blocks(const pkv_scheduler* s) {
+    return s ? static_cast<int32_t>(s->lru.size()) : -1;
 }
 
 }  // extern "C"

@@ -2,7 +2,9 @@
 
 Same interface as :class:`scheduler.Scheduler` (``history_plan``, ``next_step``,
 ``all_steps``) and the same plans; the planning runs in the library's C++ code.  Adds
-``release`` (return a finished request's pages to the free list) and ``num_free``.
+``release`` (return a finished request's pages to the free list), ``num_free`` and prefix
+caching: ``add_prompt`` takes a request's prompt token ids and reuses the pages of
+matching full 16-token prompt blocks other requests computed before.
 Host code only: usable without a GPU.
 """
 from __future__ import annotations
@@ -46,6 +48,12 @@ def _lib():
         lib.pkv_sched_release.restype = ctypes.c_int
         lib.pkv_sched_free_pages.argtypes = [V]
         lib.pkv_sched_free_pages.restype = ctypes.c_int32
+        lib.pkv_sched_add_prompt.argtypes = [V, ctypes.c_int32, V, ctypes.c_int32,
+                                             ctypes.c_int32]
+        lib.pkv_sched_add_prompt.restype = ctypes.c_int
+        for fn in (lib.pkv_sched_cached_blocks, lib.pkv_sched_evictable_blocks):
+            fn.argtypes = [V]
+            fn.restype = ctypes.c_int32
         lib._pkv_sched_ready = True
     return lib
 
@@ -78,6 +86,26 @@ class NativeScheduler:
             raise binding.PkvError("pkv_sched_add_request", rc)
         self.max_reqs += 1
         self.max_pages = max(self.max_pages, -(-(history + prompt + decodes) // 16))
+
+    def add_prompt(self, rid: int, tokens, decodes: int) -> int:
+        """Add a request with known prompt token ids (prefix caching); returns the number
+        of prompt tokens reused from the cache."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        rc = self._lib.pkv_sched_add_prompt(self._h, rid, t.ctypes.data_as(ctypes.c_void_p),
+                                            len(t), decodes)
+        if rc < 0:
+            raise binding.PkvError("pkv_sched_add_prompt", rc)
+        self.max_reqs += 1
+        self.max_pages = max(self.max_pages, -(-(len(t) + decodes) // 16))
+        return rc
+
+    @property
+    def cached_blocks(self) -> int:
+        return int(self._lib.pkv_sched_cached_blocks(self._h))
+
+    @property
+    def evictable_blocks(self) -> int:
+        return int(self._lib.pkv_sched_evictable_blocks(self._h))
 
     def _call(self, fn, *args) -> Optional[StepPlan]:
         R, P = max(1, self.max_reqs), self.max_pages

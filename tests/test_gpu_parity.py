@@ -231,6 +231,61 @@ def test_decode_loop_and_graph_bitwise_identical():
         assert all(np.array_equal(a, b) for a, b in zip(pool_bits(kv), ref_pool)), mode
 
 
+def test_prefix_cache_reuse_matches_oracle():
+    # prefix caching (hotelren.com/news/6181127 §4.3) through the native planner: requests
+    # sharing a 100-token system prompt reuse the full prompt blocks the first one already
+    # computed, continue at the reused position, and every row they compute must match the
+    # oracle over their whole token sequence.  K, V and Q are functions of (position, token
+    # id), as a model's are, so equal prefixes really hold equal K/V; the pool must hold
+    # exactly that K/V in every slot any request's block table reaches.
+    from paged_kv_cache_token_gb300.native_scheduler import NativeScheduler
+    hq, hkv, d, vocab, P = 8, 2, 128, 40, 256
+    g = torch.Generator().manual_seed(77)
+    tab = lambda h: torch.randn(P, vocab, h, d, generator=g).to(torch.bfloat16)
+    ktab, vtab, qtab = tab(hkv), tab(hkv), tab(hq)
+    rng = np.random.default_rng(5)
+    system = rng.integers(0, vocab, 100)
+    prompts = [np.concatenate([system, rng.integers(0, vocab, n)]) for n in (30, 50, 12)]
+    prompts.append(rng.integers(0, vocab, 80))
+    decodes = [3, 2, 4, 2]
+    seqs = [np.concatenate([p, rng.integers(0, vocab, n)]) for p, n in zip(prompts, decodes)]
+    specs = [W.RequestSpec(r, 0, len(p), n) for r, (p, n) in enumerate(zip(prompts, decodes))]
+    pages = sum(-(-len(x) // 16) for x in seqs) + 4
+    w = W.Workload(900, "prefix", hq, hkv, d, 0, specs, np.arange(pages, dtype=np.int32), pages)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    for r, x in enumerate(seqs):
+        pos = torch.arange(len(x))
+        tok = torch.as_tensor(x)
+        w._cache[("kv", r)] = (bits(ktab[pos, tok]), bits(vtab[pos, tok]))
+        w._cache[("q", r)] = bits(qtab[pos, tok])
+    s = NativeScheduler([], w.page_order, 64)  # 64-token budget: chunked prefills too
+    kv = runner.paged_kv_for(w)
+    assert s.add_prompt(0, prompts[0], decodes[0]) == 0
+    tables = {}
+    reused = None
+    while True:
+        plan = s.next_step()
+        if plan is None:
+            break
+        out = runner.run_step(kv, w, plan)
+        assert kv.read_error() == 0
+        assert_close(gpu_as_f64(out), oracle_rows(w, plan), "prefix step")
+        for j, rid in enumerate(plan.rids):
+            tables[rid] = plan.block_table[j]
+        if reused is None:  # after the first step the system prompt's first blocks exist
+            reused = [s.add_prompt(r, prompts[r], decodes[r]) for r in (1, 2, 3)]
+    assert reused[0] > 0 and reused[1] > 0 and reused[2] == 0
+    shared = set(tables[0][:reused[0] // 16]) & set(tables[1][:reused[0] // 16])
+    assert len(shared) == reused[0] // 16
+    kc, vc = pool_bits(kv)
+    for r, x in enumerate(seqs):
+        k, v = w.kv(r)
+        for p_ in range(len(x)):
+            page = tables[r][p_ // 16]
+            assert np.array_equal(kc[page, :, p_ % 16], k[p_]), (r, p_)
+            assert np.array_equal(vc[page, :, p_ % 16], v[p_]), (r, p_)
+
+
 def test_block_table_permutation_bitwise_identical():
     base = custom(400, 32, 8, 128, 0, [(c, 0, 1) for c in (50, 700, 2100, 16)])
     outs = []
