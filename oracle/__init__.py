@@ -13,6 +13,8 @@ Functions (numpy in, numpy out; 16-bit inputs are passed as their uint16 bit pat
   block table (lshu.cn/news/11576 §2.2-§2.3: pages of 16 tokens written by page index).
 * :func:`kv_bytes_per_token` -- 2 x L x n_kv_heads x d_head x bytes
   (hotelren.com/news/6181127 §2.3).
+* :func:`quantize_int8`, :func:`attention_rows_int8` -- codes of a per-channel INT8 KV
+  cache and attention over the values they stand for (wmrh.cn/news/64708 §4.3, §5.4).
 """
 import ctypes
 import os
@@ -48,6 +50,11 @@ def _load():
         lib.oracle_bf16_to_double.restype = dbl
         lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_fp16_to_double.restype = dbl
+        lib.oracle_quantize_int8.argtypes = [ctypes.c_int, P, i64, i32, i32, P, P]
+        lib.oracle_quantize_int8.restype = ctypes.c_int
+        lib.oracle_attention_rows_int8.argtypes = [ctypes.c_int, P, P, i32, P, P, P, P, i32,
+                                                   i32, i32, i32, dbl, P]
+        lib.oracle_attention_rows_int8.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -102,6 +109,46 @@ def attention_rows(dtype: int, q: np.ndarray, pos: np.ndarray, k: np.ndarray, v:
                                        Hkv, D, float(scale), _ptr(out))
     if rc:
         raise ValueError("oracle_attention_rows: bad argument (rc=%d)" % rc)
+    return out
+
+
+def quantize_int8(dtype: int, x: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """x [n, H, D] uint16 bits, scale [H, D] float32 > 0 -> codes [n, H, D] int8:
+    clamp(rint(x / scale), -127, 127), the quotient in IEEE fp32, ties to even."""
+    x = _u16(x)
+    n, H, D = x.shape
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    if scale.shape != (H, D):
+        raise ValueError("scale must be [H, D]")
+    out = np.empty((n, H, D), dtype=np.int8)
+    rc = _load().oracle_quantize_int8(dtype, _ptr(x), n, H, D, _ptr(scale), _ptr(out))
+    if rc:
+        raise ValueError("oracle_quantize_int8: bad argument")
+    return out
+
+
+def attention_rows_int8(dtype: int, q: np.ndarray, pos: np.ndarray, k_codes: np.ndarray,
+                        v_codes: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray,
+                        scale: float) -> np.ndarray:
+    """As :func:`attention_rows` over an INT8 cache: k/v codes [n_kv, Hkv, D] int8 stand
+    for code * scale[Hkv, D] (float32)."""
+    q = _u16(q)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    kc = np.ascontiguousarray(k_codes, dtype=np.int8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.int8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    n, Hq, D = q.shape
+    n_kv, Hkv, Dk = kc.shape
+    if Dk != D or vc.shape != kc.shape or pos.shape != (n,) or ks.shape != (Hkv, D) or \
+            vs.shape != (Hkv, D):
+        raise ValueError("shape mismatch")
+    out = np.empty((n, Hq, D), dtype=np.float64)
+    rc = _load().oracle_attention_rows_int8(dtype, _ptr(q), _ptr(pos), n, _ptr(kc), _ptr(vc),
+                                            _ptr(ks), _ptr(vs), n_kv, Hq, Hkv, D, float(scale),
+                                            _ptr(out))
+    if rc:
+        raise ValueError("oracle_attention_rows_int8: bad argument (rc=%d)" % rc)
     return out
 
 

@@ -25,7 +25,10 @@
  *     pre-allocated pool of fixed-size pages), §2.3 (16 tokens per block);
  *
  *   * the per-token KV byte count 2 x L x n_kv_heads x d_head x bytes --
- *     hotelren.com/news/6181127 §2.3.
+ *     hotelren.com/news/6181127 §2.3;
+ *
+ *   * the INT8 codes of a per-channel quantised KV cache and attention over
+ *     the values they stand for -- wmrh.cn/news/64708 §4.3, §5.4.
  *
  * Arithmetic is IEEE double throughout; inputs arrive as the exact 16-bit
  * patterns (bf16 or IEEE binary16) and are widened here, exactly.
@@ -115,32 +118,13 @@ int64_t oracle_kv_bytes_per_token(int64_t layers, int64_t n_kv_heads, int64_t d_
 /*                        out = sum_j (w_j / Z) v_j                         */
 /* Returns 0, -1 on a bad argument (nothing written), -3 when out of memory. */
 /* ---------------------------------------------------------------------- */
-int oracle_attention_rows(int dtype, const uint16_t* q, const int32_t* pos, int32_t n_rows,
-                          const uint16_t* k, const uint16_t* v, int32_t n_kv, int32_t Hq,
-                          int32_t Hkv, int32_t D, double scale, double* out)
+/* The same, on K/V already widened to double (kd, vd: [n_kv, Hkv, D]). */
+static int attention_core(int dtype, const uint16_t* q, const int32_t* pos, int32_t n_rows,
+                          const double* kd, const double* vd, int32_t Hq, int32_t Hkv,
+                          int32_t D, double scale, double* out)
 {
-    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return -1;
-    if (n_rows < 0 || n_kv < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv) return -1;
-    for (int32_t i = 0; i < n_rows; ++i)
-        if (pos[i] < 0 || pos[i] >= n_kv) return -1;
     const int32_t group = Hq / Hkv;
     const int64_t units = (int64_t)n_rows * Hq;
-    const int64_t kv_elems = (int64_t)n_kv * Hkv * D;
-
-    /* widen K and V once (exact), then work in double only */
-    double* kd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
-    double* vd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
-    if (!kd || !vd) {
-        free(kd);
-        free(vd);
-        return -3;
-    }
-#pragma omp parallel for schedule(static)
-    for (int64_t e = 0; e < kv_elems; ++e) {
-        kd[e] = widen(dtype, k[e]);
-        vd[e] = widen(dtype, v[e]);
-    }
-
 #pragma omp parallel
     {
         double* qd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -179,6 +163,102 @@ int oracle_attention_rows(int dtype, const uint16_t* q, const int32_t* pos, int3
         }
         free(qd);
     }
+    return 0;
+}
+
+static int rows_ok(int dtype, const int32_t* pos, int32_t n_rows, int32_t n_kv, int32_t Hq,
+                   int32_t Hkv, int32_t D)
+{
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return 0;
+    if (n_rows < 0 || n_kv < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv) return 0;
+    for (int32_t i = 0; i < n_rows; ++i)
+        if (pos[i] < 0 || pos[i] >= n_kv) return 0;
+    return 1;
+}
+
+int oracle_attention_rows(int dtype, const uint16_t* q, const int32_t* pos, int32_t n_rows,
+                          const uint16_t* k, const uint16_t* v, int32_t n_kv, int32_t Hq,
+                          int32_t Hkv, int32_t D, double scale, double* out)
+{
+    if (!rows_ok(dtype, pos, n_rows, n_kv, Hq, Hkv, D)) return -1;
+    const int64_t kv_elems = (int64_t)n_kv * Hkv * D;
+
+    /* widen K and V once (exact), then work in double only */
+    double* kd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
+    double* vd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
+    if (!kd || !vd) {
+        free(kd);
+        free(vd);
+        return -3;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < kv_elems; ++e) {
+        kd[e] = widen(dtype, k[e]);
+        vd[e] = widen(dtype, v[e]);
+    }
+    attention_core(dtype, q, pos, n_rows, kd, vd, Hq, Hkv, D, scale, out);
+    free(kd);
+    free(vd);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* INT8 KV cache: wmrh.cn/news/64708 §4.3 (the KV cache in INT8 instead of  */
+/* FP16 halves its memory and bandwidth) and §5.4 (calibrate the KV cache   */
+/* per channel: the channels' value ranges differ widely).  One scale per  */
+/* (KV head, dim) channel for K and one for V, fixed by calibration.        */
+/*                                                                         */
+/* The code of a 16-bit value x in a channel with scale s > 0:             */
+/*     code = clamp(rint(x / s), -127, 127)                                 */
+/* where x / s is the IEEE single-precision quotient of the exact float    */
+/* value of x and s (round to nearest even), rint rounds to nearest with   */
+/* ties to even, and the value the code stands for is code * s.            */
+/*                                                                         */
+/* x [n_tok, H, D] 16-bit patterns, scale [H, D], out [n_tok, H, D].        */
+/* Returns 0; -1 on a bad argument (a scale not > 0 included).              */
+/* ---------------------------------------------------------------------- */
+int oracle_quantize_int8(int dtype, const uint16_t* x, int64_t n_tok, int32_t H, int32_t D,
+                         const float* scale, int8_t* out)
+{
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return -1;
+    if (n_tok < 0 || H <= 0 || D <= 0) return -1;
+    for (int64_t c = 0; c < (int64_t)H * D; ++c)
+        if (!(scale[c] > 0.0f)) return -1;
+    for (int64_t t = 0; t < n_tok; ++t)
+        for (int64_t c = 0; c < (int64_t)H * D; ++c) {
+            const float xf = (float)widen(dtype, x[t * H * D + c]); /* exact */
+            const float quot = xf / scale[c];                          /* IEEE single */
+            float r = rintf(quot);                                     /* ties to even */
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            out[t * H * D + c] = (int8_t)r;
+        }
+    return 0;
+}
+
+/* Attention as oracle_attention_rows, over an INT8 cache: key and value j of channel  */
+/* (g, d) stand for code * scale (exact in double); q stays 16-bit.                    */
+int oracle_attention_rows_int8(int dtype, const uint16_t* q, const int32_t* pos,
+                               int32_t n_rows, const int8_t* kc, const int8_t* vc,
+                               const float* k_scale, const float* v_scale, int32_t n_kv,
+                               int32_t Hq, int32_t Hkv, int32_t D, double scale, double* out)
+{
+    if (!rows_ok(dtype, pos, n_rows, n_kv, Hq, Hkv, D)) return -1;
+    const int64_t ch = (int64_t)Hkv * D;
+    const int64_t kv_elems = (int64_t)n_kv * ch;
+    double* kd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
+    double* vd = (double*)malloc(sizeof(double) * (size_t)(kv_elems ? kv_elems : 1));
+    if (!kd || !vd) {
+        free(kd);
+        free(vd);
+        return -3;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < kv_elems; ++e) {
+        kd[e] = (double)kc[e] * (double)k_scale[e % ch];
+        vd[e] = (double)vc[e] * (double)v_scale[e % ch];
+    }
+    attention_core(dtype, q, pos, n_rows, kd, vd, Hq, Hkv, D, scale, out);
     free(kd);
     free(vd);
     return 0;

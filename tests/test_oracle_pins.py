@@ -303,3 +303,67 @@ def test_pins_catch_planted_mistakes(mutate):
     np.testing.assert_allclose(good, ref, rtol=1e-10, atol=1e-12)
     bad = _py_attention(qd, kd, vd, pos, 0.5, hq // hkv, mutate)
     assert np.abs(bad - ref).max() > 1e-3
+
+
+# ------------------------------------------------------------------ INT8 KV cache
+# wmrh.cn/news/64708 §4.3 (KV cache in INT8) and §5.4 (calibrated per channel): the code of
+# x in channel (h, d) is clamp(rint(x / s[h, d]), -127, 127) and stands for code * s.
+
+def _bf16_bits(vals):
+    return torch.tensor(np.asarray(vals, np.float32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def test_int8_codes_of_exact_multiples():
+    # x = k * s with s a power of two is exact in bf16, so the code is k itself
+    k = np.arange(-127, 128, dtype=np.int64)
+    for s in (1.0, 0.5, 2.0 ** -7, 8.0):
+        x = _bf16_bits((k * s).reshape(-1, 1, 1))
+        codes = oracle.quantize_int8(oracle.BF16, x, np.full((1, 1), s, np.float32))
+        assert np.array_equal(codes.reshape(-1), k.astype(np.int8))
+
+
+def test_int8_ties_to_even_and_clamp():
+    vals = [0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, 127.5, -127.5, 200.0, -300.0, 1e30]
+    want = [0, 2, 2, 0, -2, -2, 126, 127, -127, 127, -127, 127]
+    x = _bf16_bits(np.array(vals).reshape(-1, 1, 1))
+    back = oracle.widen(oracle.BF16, x).reshape(-1)
+    assert np.array_equal(back[:9], vals[:9])  # the tie cases are exact in bf16
+    codes = oracle.quantize_int8(oracle.BF16, x, np.ones((1, 1), np.float32))
+    assert codes.reshape(-1).tolist() == want
+
+
+def test_int8_scale_per_channel():
+    # every channel (h, d) gets its own power-of-two scale; the same value 1.0 in each
+    # channel must come out as 1 / s[h, d]
+    H, D = 3, 8
+    e = (np.arange(H)[:, None] + np.arange(D)[None, :]) % 7
+    scale = (2.0 ** -e).astype(np.float32)
+    x = _bf16_bits(np.ones((2, H, D)))
+    codes = oracle.quantize_int8(oracle.BF16, x, scale)
+    assert np.array_equal(codes[0], (2 ** e).astype(np.int8)) and np.array_equal(codes[1],
+                                                                               codes[0])
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16])
+def test_int8_attention_equals_plain_attention_on_exact_codes(dtype):
+    # K and V values that are integers in [-127, 127] times per-channel power-of-two scales
+    # are exact in both 16-bit formats, so quantising them loses nothing: attention over
+    # the codes must equal attention over the 16-bit values bit for bit
+    g = np.random.default_rng(3)
+    n, Hq, Hkv, D = 40, 4, 2, 16
+    e = g.integers(0, 6, (Hkv, D))
+    ks, vs = (2.0 ** -e).astype(np.float32), (2.0 ** -((e + 3) % 6)).astype(np.float32)
+    kc = g.integers(-127, 128, (n, Hkv, D))
+    vc = g.integers(-127, 128, (n, Hkv, D))
+    tdt = torch.bfloat16 if dtype == oracle.BF16 else torch.float16
+    bits = lambda a: torch.tensor(a, dtype=torch.float32).to(tdt).view(torch.int16).numpy() \
+        .view(np.uint16)
+    k, v = bits(kc * ks), bits(vc * vs)
+    assert np.array_equal(oracle.quantize_int8(dtype, k, ks), kc.astype(np.int8))
+    assert np.array_equal(oracle.quantize_int8(dtype, v, vs), vc.astype(np.int8))
+    q = bits(g.standard_normal((7, Hq, D)))
+    pos = np.array([0, 1, 5, 17, 30, 38, 39], np.int32)
+    got = oracle.attention_rows_int8(dtype, q, pos, kc, vc, ks, vs, 0.3)
+    want = oracle.attention_rows(dtype, q, pos, k, v, 0.3)
+    assert np.array_equal(got, want)
