@@ -188,6 +188,33 @@ PKV_API int pkv_paged_attention_step_static_ws(const pkv_step_desc* desc, const 
                                                void* stream);
 
 /*
+ * INT8 KV cache (wmrh.cn/news/64708 §4.3: the cache held in INT8 instead of FP16 halves its
+ * bytes; §5.4: quantising the cache is the lever for long contexts).  The pages have the
+ * layout above with one signed byte per element; each KV head and channel has a fixed
+ * fp32 scale (per-channel, calibrated before the pool is filled):
+ *   code  = clamp(round_half_even(x / scale[h][c]), -127, 127)   (IEEE fp32 quotient)
+ *   value = code * scale[h][c]
+ * The attention step reads the codes and attends over the values they stand for; all of
+ * its arithmetic stays fp32 as in the 16-bit path.  Every row (decode and prefill chunk)
+ * runs on the streaming kernel.
+ *   k_scale, v_scale   device fp32 [num_kv_heads][head_dim], 16-byte aligned, > 0
+ *   k_cache, v_cache   device int8 [num_pages][num_kv_heads][16][head_dim]
+ * Other arguments, errors and the device error flag are those of the 16-bit calls;
+ * k_new, v_new, q and out keep desc->dtype.
+ */
+PKV_API int pkv_kv_append_int8(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                               const float* k_scale, const float* v_scale, int8_t* k_cache,
+                               int8_t* v_cache, int64_t* slot_mapping_out,
+                               int32_t* dev_err_flag, void* stream);
+PKV_API size_t pkv_attention_workspace_bytes_int8(const pkv_step_desc* desc);
+PKV_API int pkv_paged_attention_step_int8(const pkv_step_desc* desc, const void* q,
+                                          const int8_t* k_cache, const int8_t* v_cache,
+                                          const float* k_scale, const float* v_scale,
+                                          void* out, float scale, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_err_flag,
+                                          void* stream);
+
+/*
  * pkv_read_device_error -- synchronise `stream`, copy *dev_err_flag (device) to
  * *host_value and return PKV_OK when it is zero, PKV_ERR_DEVICE when not, PKV_ERR_CUDA
  * when the copy fails.  The only synchronising entry point.

@@ -26,8 +26,10 @@ BF16, FP16 = 0, 1
 DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16}
 
 EXPORTED = ("pkv_kv_append", "pkv_advance_context", "pkv_attention_workspace_bytes",
-            "pkv_paged_attention_step", "pkv_read_device_error", "pkv_set_kernel_events",
-            "pkv_status_string", "pkv_version")
+            "pkv_paged_attention_step", "pkv_kv_append_int8",
+            "pkv_attention_workspace_bytes_int8", "pkv_paged_attention_step_int8",
+            "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
+            "pkv_version")
 
 
 class PkvError(RuntimeError):
@@ -73,6 +75,13 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_attention_step.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V,
                                              ctypes.c_float, V, sz, V, V]
     lib.pkv_paged_attention_step.restype = ctypes.c_int
+    lib.pkv_kv_append_int8.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V, V, V, V]
+    lib.pkv_kv_append_int8.restype = ctypes.c_int
+    lib.pkv_attention_workspace_bytes_int8.argtypes = [ctypes.POINTER(StepDesc)]
+    lib.pkv_attention_workspace_bytes_int8.restype = sz
+    lib.pkv_paged_attention_step_int8.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V,
+                                                  ctypes.c_float, V, sz, V, V]
+    lib.pkv_paged_attention_step_int8.restype = ctypes.c_int
     lib.pkv_read_device_error.argtypes = [V, ctypes.POINTER(ctypes.c_int32), V]
     lib.pkv_read_device_error.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -153,6 +162,37 @@ def paged_attention_step(desc: StepDesc, q, k_cache, v_cache, out, scale: float,
                                          nbytes, _ptr(err), _stream(stream))
     if check and rc != OK:
         raise PkvError("pkv_paged_attention_step", rc)
+    return rc
+
+
+def kv_append_int8(desc: StepDesc, k_new, v_new, k_scale, v_scale, k_cache, v_cache,
+                   slot_mapping=None, err=None, stream=None, check: bool = True) -> int:
+    """Quantise this step's K/V (desc.dtype) to per-channel INT8 codes in the int8 pools;
+    k_scale, v_scale: float32 CUDA tensors [Hkv, D]."""
+    rc = load().pkv_kv_append_int8(ctypes.byref(desc), _ptr(k_new), _ptr(v_new),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(slot_mapping), _ptr(err), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_kv_append_int8", rc)
+    return rc
+
+
+def attention_workspace_bytes_int8(desc: StepDesc) -> int:
+    return int(load().pkv_attention_workspace_bytes_int8(ctypes.byref(desc)))
+
+
+def paged_attention_step_int8(desc: StepDesc, q, k_cache, v_cache, k_scale, v_scale, out,
+                              scale: float, workspace, err=None, stream=None,
+                              check: bool = True, workspace_bytes: Optional[int] = None) -> int:
+    """The attention step over int8 pools (codes times the per-channel scales)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None \
+        else workspace_bytes
+    rc = load().pkv_paged_attention_step_int8(ctypes.byref(desc), _ptr(q), _ptr(k_cache),
+                                              _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                              _ptr(out), float(scale), _ptr(workspace), nbytes,
+                                              _ptr(err), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_paged_attention_step_int8", rc)
     return rc
 
 

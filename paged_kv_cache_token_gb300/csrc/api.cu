@@ -63,10 +63,52 @@ int prefill_min_q() { return 16; }
 
 thread_local cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
 
-pkv::WorkspaceLayout layout_for(const pkv_step_desc* d, int num_sms) {
+// INT8 pools: every row runs on the streaming path (the tensor-core prefill reads 16-bit
+// operands), so no request counts as a prefill.
+pkv::WorkspaceLayout layout_for(const pkv_step_desc* d, int num_sms, bool int8 = false) {
     return pkv::workspace_layout(d->num_reqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
                                  d->total_q_tokens, d->max_q_len, d->max_context_len, num_sms,
-                                 prefill_min_q());
+                                 int8 ? INT_MAX : prefill_min_q());
+}
+
+int kv_append_impl(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                   void* k_cache, void* v_cache, int64_t* slot_mapping_out,
+                   int32_t* dev_err_flag, void* stream, const float* k_scale,
+                   const float* v_scale) {
+    const int rc = check_desc(desc);
+    if (rc != PKV_OK) return rc;
+    if (desc->total_q_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PKV_ERR_INVALID_ARG;
+    if (slot_mapping_out && (reinterpret_cast<uintptr_t>(slot_mapping_out) & 7u))
+        return PKV_ERR_INVALID_ARG;
+    const bool int8 = k_scale != nullptr;
+    if (int8 && (!v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+        return PKV_ERR_INVALID_ARG;
+    pkv::AppendArgs a{};
+    a.num_reqs = desc->num_reqs;
+    a.num_kv_heads = desc->num_kv_heads;
+    a.head_dim = desc->head_dim;
+    a.num_pages = desc->num_pages;
+    a.max_pages = desc->max_pages_per_req;
+    a.total_q_tokens = desc->total_q_tokens;
+    a.max_q_len = desc->max_q_len;
+    a.dtype = desc->dtype;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.q_lens = desc->q_lens;
+    a.q_offsets = desc->q_offsets;
+    a.context_lens = desc->context_lens;
+    a.block_table = desc->block_table;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.slot_mapping = slot_mapping_out;
+    a.err = dev_err_flag;
+    return int8 ? pkv::launch_kv_append_int8(a, static_cast<cudaStream_t>(stream))
+                : pkv::launch_kv_append(a, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -92,33 +134,17 @@ const char* pkv_status_string(int status) {
 int pkv_kv_append(const pkv_step_desc* desc, const void* k_new, const void* v_new,
                   void* k_cache, void* v_cache, int64_t* slot_mapping_out,
                   int32_t* dev_err_flag, void* stream) {
-    const int rc = check_desc(desc);
-    if (rc != PKV_OK) return rc;
-    if (desc->total_q_tokens == 0) return PKV_OK;
-    if (!k_new || !v_new || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
-        return PKV_ERR_INVALID_ARG;
-    if (slot_mapping_out && (reinterpret_cast<uintptr_t>(slot_mapping_out) & 7u))
-        return PKV_ERR_INVALID_ARG;
-    pkv::AppendArgs a{};
-    a.num_reqs = desc->num_reqs;
-    a.num_kv_heads = desc->num_kv_heads;
-    a.head_dim = desc->head_dim;
-    a.num_pages = desc->num_pages;
-    a.max_pages = desc->max_pages_per_req;
-    a.total_q_tokens = desc->total_q_tokens;
-    a.max_q_len = desc->max_q_len;
-    a.q_lens = desc->q_lens;
-    a.q_offsets = desc->q_offsets;
-    a.context_lens = desc->context_lens;
-    a.block_table = desc->block_table;
-    a.k_new = k_new;
-    a.v_new = v_new;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.slot_mapping = slot_mapping_out;
-    a.err = dev_err_flag;
-    return pkv::launch_kv_append(a, static_cast<cudaStream_t>(stream));
+    return kv_append_impl(desc, k_new, v_new, k_cache, v_cache, slot_mapping_out, dev_err_flag,
+                          stream, nullptr, nullptr);
+}
+
+int pkv_kv_append_int8(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                       const float* k_scale, const float* v_scale, int8_t* k_cache,
+                       int8_t* v_cache, int64_t* slot_mapping_out, int32_t* dev_err_flag,
+                       void* stream) {
+    if (!k_scale) return PKV_ERR_INVALID_ARG;
+    return kv_append_impl(desc, k_new, v_new, k_cache, v_cache, slot_mapping_out, dev_err_flag,
+                          stream, k_scale, v_scale);
 }
 
 int pkv_advance_context(const pkv_step_desc* desc, int32_t* context_lens, void* stream) {
@@ -138,18 +164,33 @@ size_t pkv_attention_workspace_bytes(const pkv_step_desc* desc) {
     return layout_for(desc, sms).total;
 }
 
-int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const void* k_cache,
-                             const void* v_cache, void* out, float scale, void* workspace,
-                             size_t workspace_bytes, int32_t* dev_err_flag, void* stream) {
+size_t pkv_attention_workspace_bytes_int8(const pkv_step_desc* desc) {
+    if (check_desc(desc) != PKV_OK) return 0;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return 0;
+    return layout_for(desc, sms, true).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache,
+                   const void* v_cache, void* out, float scale, void* workspace,
+                   size_t workspace_bytes, int32_t* dev_err_flag, void* stream,
+                   const float* k_scale, const float* v_scale) {
     int rc = check_desc(desc);
     if (rc != PKV_OK) return rc;
     if (desc->total_q_tokens == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return PKV_ERR_INVALID_ARG;
+    const bool int8 = k_scale != nullptr;
+    if (int8 && (!v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+        return PKV_ERR_INVALID_ARG;
     const int sms = num_sms_current_device();
     if (sms <= 0) return PKV_ERR_CUDA;
-    const pkv::WorkspaceLayout lay = layout_for(desc, sms);
+    const pkv::WorkspaceLayout lay = layout_for(desc, sms, int8);
     if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_WORKSPACE;
 
@@ -176,9 +217,12 @@ int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const voi
     a.scale_log2 = scale * 1.4426950408889634f;
     a.ws = static_cast<uint8_t*>(workspace);
     a.lay = lay;
-    a.prefill_min_q = prefill_min_q();
+    a.prefill_min_q = int8 ? INT_MAX : prefill_min_q();
     a.heads_per_tile = pkv::prefill_heads_per_tile(desc->num_q_heads, desc->num_kv_heads);
     a.err = dev_err_flag;
+    a.kv_int8 = int8 ? 1 : 0;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((rc = pkv::launch_plan(a, s)) != PKV_OK) return rc;
     if ((rc = pkv::launch_decode(a, s, g_events[0][0], g_events[0][1])) != PKV_OK) return rc;
@@ -186,6 +230,27 @@ int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const voi
         (rc = pkv::launch_prefill(a, s, g_events[1][0], g_events[1][1])) != PKV_OK)
         return rc;
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, const void* k_cache,
+                             const void* v_cache, void* out, float scale, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_err_flag, void* stream) {
+    return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                          dev_err_flag, stream, nullptr, nullptr);
+}
+
+int pkv_paged_attention_step_int8(const pkv_step_desc* desc, const void* q,
+                                  const int8_t* k_cache, const int8_t* v_cache,
+                                  const float* k_scale, const float* v_scale, void* out,
+                                  float scale, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_err_flag, void* stream) {
+    if (!k_scale) return PKV_ERR_INVALID_ARG;
+    return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                          dev_err_flag, stream, k_scale, v_scale);
 }
 
 int pkv_set_kernel_events(int which, void* start, void* stop) {

@@ -47,6 +47,19 @@ __device__ __forceinline__ bool request_ok(const StepArgs& a, int q, int c, int 
     return q >= 0 && c >= 0 && q <= a.max_q_len && c <= a.max_context_len && o1 - o0 == q;
 }
 
+// sum_{x=a}^{b} ceil(x / B) for 1 <= a, in closed form: with S(n) = sum_{y=0}^{n} floor(y/B)
+// = B m (m-1) / 2 + m (r+1) for n = B m + r, the sum is S(b + B - 1) - S(a + B - 2).  A decode
+// row over x keys holds ceil(x / 16) pages and, with splits of sp pages, ceil(x / (16 sp))
+// items (ceil(ceil(x/16)/sp) = ceil(x/(16 sp))), so a request's totals need no loop over
+// its rows.
+__device__ __forceinline__ long long sum_ceil(long long a, long long b, long long B) {
+    auto S = [B](long long n) {
+        const long long m = n / B, r = n - B * m;
+        return B * m * (m - 1) / 2 + m * (r + 1);
+    };
+    return b < a ? 0 : S(b + B - 1) - S(a + B - 2);
+}
+
 // Lengths of request r, all four loads issued together (no dependent round trip).
 struct ReqLens { int q, c, t0; bool ok; };
 __device__ __forceinline__ ReqLens load_request(const StepArgs& a, int r) {
@@ -127,8 +140,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
         if (r == tid) first = L;
         if (!L.ok) { atomicOr(&s_bad, 1); continue; }
         if (cdiv(L.c + L.q, kPage) > a.max_pages) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
-        if (L.q >= 1 && L.q < a.prefill_min_q)
-            for (int i = 0; i < L.q; ++i) my_sum += cdiv(L.c + i + 1, kPage);
+        if (L.q >= 1 && L.q < a.prefill_min_q) my_sum += sum_ceil(L.c + 1, L.c + L.q, kPage);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) my_sum += __shfl_xor_sync(kFull, my_sum, o);
@@ -159,7 +171,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
             t0 = L.t0;
             if (q >= 1 && q < a.prefill_min_q) {
                 n.x = q;
-                for (int i = 0; i < q; ++i) n.y += Hkv * cdiv(cdiv(c + i + 1, kPage), sp);
+                // clamped past the bound, which still trips the overflow check below
+                const long long items = Hkv * sum_ceil(c + 1, c + q, kPage * sp);
+                n.y = static_cast<int>(min(items, static_cast<long long>(a.lay.max_items) + 1));
             }
             if (q > 1 && q >= a.prefill_min_q) n.z = cdiv(q, 128) * slots;
         }
@@ -195,43 +209,48 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
              k += gridDim.x * (kPlanThreads / 32)) {
             const int rq = base + k, qk = s_q[k], ck = s_c[k];
             if (qk >= 1 && qk < a.prefill_min_q) {
-                // rows of this request (qk <= 31): lane i = row i; warp scan of item counts
-                const int ns = lane < qk ? cdiv(cdiv(ck + lane + 1, kPage), sp) : 0;
-                int incl = Hkv * ns;
+                // rows of this request, 32 at a time: lane i = row r0 + i; warp scan of item
+                // counts, carried from one group of rows to the next
+                int item0 = s_item0[k];
+                for (int r0 = 0; r0 < qk; r0 += 32) {
+                    const int row = r0 + lane;
+                    const int ns = row < qk ? cdiv(ck + row + 1, kPage * sp) : 0;
+                    int incl = Hkv * ns;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(kFull, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const int first = s_item0[k] + incl - Hkv * ns;
-                if (lane < qk) {
-                    rows[s_row0[k] + lane] = make_int4(s_t0[k] + lane, first, ck + lane + 1, ns);
-                }
-                for (int i = 0; i < qk; ++i) {
-                    const unsigned ns_i = __shfl_sync(kFull, ns, i);
-                    const int first_i = __shfl_sync(kFull, first, i);
-                    const int nkv = ck + i + 1, pages = cdiv(nkv, kPage);
-                    const int t = s_t0[k] + i;
-                    // balanced splits: the first `rem` splits get one page more than `per`
-                    const int per = pages / static_cast<int>(ns_i);
-                    const int rem = pages - per * static_cast<int>(ns_i);
-                    // lane l writes 16-byte half l of the row's item records, so a warp store
-                    // covers 512 contiguous bytes; item position = slot (splits of a (row,
-                    // head) adjacent)
-                    int4* dst = items + 2 * static_cast<int64_t>(first_i);
-                    for (unsigned h = lane; h < 2 * Hkv * ns_i; h += 32) {
-                        const unsigned e = h >> 1;
-                        const int g = static_cast<int>(e / ns_i);
-                        const int s_ = static_cast<int>(e) - g * static_cast<int>(ns_i);
-                        if (h & 1) {
-                            dst[h] = make_int4(nkv, static_cast<int>(ns_i), rq,
-                                               first_i + g * static_cast<int>(ns_i));
-                        } else {
-                            const int pb = s_ * per + min(s_, rem);
-                            const int np = per + (s_ < rem ? 1 : 0);
-                            dst[h] = make_int4(t, g | (s_ << 16), pb, np);
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(kFull, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const int first = item0 + incl - Hkv * ns;
+                    if (row < qk)
+                        rows[s_row0[k] + row] = make_int4(s_t0[k] + row, first, ck + row + 1, ns);
+                    for (int i = 0; i < min(32, qk - r0); ++i) {
+                        const unsigned ns_i = __shfl_sync(kFull, ns, i);
+                        const int first_i = __shfl_sync(kFull, first, i);
+                        const int nkv = ck + r0 + i + 1, pages = cdiv(nkv, kPage);
+                        const int t = s_t0[k] + r0 + i;
+                        // balanced splits: the first `rem` splits get one page more than `per`
+                        const int per = pages / static_cast<int>(ns_i);
+                        const int rem = pages - per * static_cast<int>(ns_i);
+                        // lane l writes 16-byte half l of the row's item records, so a warp
+                        // store covers 512 contiguous bytes; item position = slot (splits of
+                        // a (row, head) adjacent)
+                        int4* dst = items + 2 * static_cast<int64_t>(first_i);
+                        for (unsigned h = lane; h < 2 * Hkv * ns_i; h += 32) {
+                            const unsigned e = h >> 1;
+                            const int g = static_cast<int>(e / ns_i);
+                            const int s_ = static_cast<int>(e) - g * static_cast<int>(ns_i);
+                            if (h & 1) {
+                                dst[h] = make_int4(nkv, static_cast<int>(ns_i), rq,
+                                                   first_i + g * static_cast<int>(ns_i));
+                            } else {
+                                const int pb = s_ * per + min(s_, rem);
+                                const int np = per + (s_ < rem ? 1 : 0);
+                                dst[h] = make_int4(t, g | (s_ << 16), pb, np);
+                            }
                         }
                     }
+                    item0 += __shfl_sync(kFull, incl, 31);
                 }
             }
         }
@@ -256,15 +275,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
 // ------------------------------------------------------------------------------------
 // decode: independent warps pull items; see the file comment for the data flow.
 // ------------------------------------------------------------------------------------
-template <typename T, int D, int G>
+// Q8: the pools hold INT8 codes (half the bytes per page, so twice the ring stages keep the
+// same bytes in flight).
+template <typename T, int D, int G, bool Q8>
 struct DecodeSmem {
-    static constexpr int kPageBytes = kPage * D * 2;      // one K (or V) page block
+    static constexpr int kNst = Q8 ? 2 * kStages : kStages;
+    static constexpr int kPageBytes = kPage * D * (Q8 ? 1 : 2);  // one K (or V) page block
     static constexpr int kStageBytes = 2 * kPageBytes;
-    static constexpr int kRing = kDecWarps * kStages * kStageBytes;
+    static constexpr int kRing = kDecWarps * kNst * kStageBytes;
     static constexpr int kPbuf = kDecWarps * kPage * G * 8;  // (p, p) pairs per token, head
-    static constexpr int kBars = kDecWarps * kStages * 8;
+    static constexpr int kBars = kDecWarps * kNst * 8;
     static constexpr int kBytes = kRing + kPbuf + kBars;
 };
+
+// Four INT8 codes (one 32-bit word) to floats, exactly: with the sign bit flipped, a code's
+// byte u = code + 128 becomes the low mantissa byte of 2^23 + u, and subtracting 2^23 + 128
+// leaves the code.  Returns codes (0, 1) and (2, 3) as pairs.
+__device__ __forceinline__ void codes_to_float(uint32_t w, float2& f01, float2& f23) {
+    const uint32_t x = w ^ 0x80808080u;
+    const float2 bias = make_float2(-8388736.f, -8388736.f);
+    f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650)),
+                                 __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7651))), bias);
+    f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7652)),
+                                 __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7653))), bias);
+}
 
 // One work item as a warp sees it.
 struct DecItem {
@@ -273,9 +307,10 @@ struct DecItem {
     int nkv, ns, r, base;  // keys of the row, splits of the row, request, slot of split 0
 };
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool Q8>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
-    using S = DecodeSmem<T, D, G>;
+    using S = DecodeSmem<T, D, G, Q8>;
+    constexpr int kNst = S::kNst;   // ring stages per warp
     using Cv = F16<T>;
     constexpr int QKD = D / 8;      // dims per lane in q.k (16 or 8)
     constexpr int NCH = QKD / 8;    // 16-byte chunks per lane per key row (2 or 1)
@@ -286,12 +321,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t* ring = smem + warp * kStages * S::kStageBytes;
+    uint8_t* ring = smem + warp * kNst * S::kStageBytes;
     float2* pbuf = reinterpret_cast<float2*>(smem + S::kRing) + warp * kPage * G;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing + S::kPbuf) + warp * kStages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing + S::kPbuf) + warp * kNst;
 
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kNst; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
     __syncwarp();
@@ -304,14 +339,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     float2* part_ml = ws_at<float2>(a, a.lay.part_ml);
     float* part_o = ws_at<float>(a, a.lay.part_o);
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads;
-    const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
-    const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
+    const uint8_t* kc = static_cast<const uint8_t*>(a.k_cache);
+    const uint8_t* vc = static_cast<const uint8_t*>(a.v_cache);
     // K/V pages are read once per step: evict them first so the split partials written
     // meanwhile stay in L2 for the combine
     const uint64_t kv_policy = l2_policy_evict_first();
     const int c8 = lane & 7, tg = lane >> 3;
     const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
-    const int swz = (c8 >> 2) & 1;  // staggered chunk order: conflict-free 16-byte loads
+    // staggered chunk order: conflict-free 16-byte loads of 256-byte 16-bit key rows (a
+    // 128-byte INT8 row needs none)
+    const int swz = Q8 ? 0 : (c8 >> 2) & 1;
     const int my_tok = tg * 4 + 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0);  // token of my reduced scores
 
     // ---- item metadata moves through a pipeline so no dependent load sits on the critical
@@ -415,16 +452,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         }
         const int phys = __shfl_sync(kFull, win, lidx);
         if (lane == 0) {
-            const int stage = issued % kStages;
+            const int stage = issued % kNst;
             uint8_t* dst = ring + stage * S::kStageBytes;
-            const int64_t off = (static_cast<int64_t>(phys) * Hkv + g) * (kPage * D);
+            const int64_t off = (static_cast<int64_t>(phys) * Hkv + g) * S::kPageBytes;
             mbar_arrive_expect_tx(&bars[stage], 2 * S::kPageBytes);
             bulk_g2s_hint(dst, kc + off, S::kPageBytes, &bars[stage], kv_policy);
             bulk_g2s_hint(dst + S::kPageBytes, vc + off, S::kPageBytes, &bars[stage], kv_policy);
         }
         ++issued;
     };
-    for (int k = 0; k < kStages; ++k) issue_one();
+    for (int k = 0; k < kNst; ++k) issue_one();
 
     // output row of (token t, KV head g): lanes write DPL dims of each of the G heads
     auto store_row = [&](int t, int g, int j, const float (&res)[DPL]) {
@@ -442,6 +479,20 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         // (even dim, odd dim) pairs: the packed fp32 FMA (FFMA2) works on both at once
         float2 qf[G][QKD / 2];
         const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+        // INT8 pools: key channel d stands for code * k_scale[g][d], so the scale folds
+        // into q once per item and the inner loop works on the codes
+        float2 ksc[QKD / 2];
+#pragma unroll
+        for (int p = 0; p < QKD / 2; ++p) ksc[p] = make_float2(1.f, 1.f);
+        if constexpr (Q8) {
+            const float4* kp = reinterpret_cast<const float4*>(a.k_scale + cur.g * D + c8 * QKD);
+#pragma unroll
+            for (int p = 0; p < QKD / 4; ++p) {
+                const float4 f = __ldg(kp + p);
+                ksc[2 * p] = make_float2(f.x, f.y);
+                ksc[2 * p + 1] = make_float2(f.z, f.w);
+            }
+        }
 #pragma unroll
         for (int j = 0; j < G; ++j) {
 #pragma unroll
@@ -449,7 +500,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 const uint32_t ws4[4] = {q_cur[j][ci].x, q_cur[j][ci].y, q_cur[j][ci].z,
                                          q_cur[j][ci].w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) qf[j][ci * 4 + e] = __fmul2_rn(Cv::unpack(ws4[e]), sl2);
+                for (int e = 0; e < 4; ++e) {
+                    qf[j][ci * 4 + e] = __fmul2_rn(Cv::unpack(ws4[e]), sl2);
+                    if constexpr (Q8)
+                        qf[j][ci * 4 + e] = __fmul2_rn(qf[j][ci * 4 + e], ksc[ci * 4 + e]);
+                }
             }
         }
         float m[G], lsum[NV];
@@ -464,8 +519,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         for (int i = 0; i < NV; ++i) lsum[i] = 0.f;
 
         for (int i = 0; i < cur.np; ++i) {
-            const int stage = consumed % kStages;
-            if (!mbar_wait_warp(&bars[stage], (consumed / kStages) & 1)) {
+            const int stage = consumed % kNst;
+            if (!mbar_wait_warp(&bars[stage], (consumed / kNst) & 1)) {
                 if (lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
                 aborted = true;
                 break;
@@ -481,17 +536,41 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 float2 acc[G];  // even-dim and odd-dim partial sums
 #pragma unroll
                 for (int j = 0; j < G; ++j) acc[j] = make_float2(0.f, 0.f);
-                const uint4* krow = reinterpret_cast<const uint4*>(sK + (tg * 4 + kk) * D * 2) +
-                                    c8 * NCH;
+                if constexpr (Q8) {
+                    // QKD codes of the key row: word wi holds dims 4 wi .. 4 wi + 3
+                    const uint8_t* kb = sK + (tg * 4 + kk) * D + c8 * QKD;
+                    uint32_t kw[QKD / 4];
+                    if constexpr (QKD == 16) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(kb);
+                        kw[0] = w.x; kw[1] = w.y; kw[2] = w.z; kw[QKD / 4 - 1] = w.w;
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2*>(kb);
+                        kw[0] = w.x; kw[QKD / 4 - 1] = w.y;
+                    }
 #pragma unroll
-                for (int ci = 0; ci < NCH; ++ci) {
-                    const uint4 w = krow[ci ^ (NCH == 2 ? swz : 0)];
-                    const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+                    for (int wi = 0; wi < QKD / 4; ++wi) {
+                        float2 f01, f23;
+                        codes_to_float(kw[wi], f01, f23);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = Cv::unpack(ws4[e]);
+                        for (int j = 0; j < G; ++j) {
+                            acc[j] = __ffma2_rn(qf[j][2 * wi], f01, acc[j]);
+                            acc[j] = __ffma2_rn(qf[j][2 * wi + 1], f23, acc[j]);
+                        }
+                    }
+                } else {
+                    const uint4* krow =
+                        reinterpret_cast<const uint4*>(sK + (tg * 4 + kk) * D * 2) + c8 * NCH;
 #pragma unroll
-                        for (int j = 0; j < G; ++j) acc[j] = __ffma2_rn(qf[j][ci * 4 + e], f, acc[j]);
+                    for (int ci = 0; ci < NCH; ++ci) {
+                        const uint4 w = krow[ci ^ (NCH == 2 ? swz : 0)];
+                        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = Cv::unpack(ws4[e]);
+#pragma unroll
+                            for (int j = 0; j < G; ++j)
+                                acc[j] = __ffma2_rn(qf[j][ci * 4 + e], f, acc[j]);
+                        }
                     }
                 }
 #pragma unroll
@@ -577,7 +656,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             }
             auto pv_token = [&](int tok) {
                 float2 vf[DP2];
-                if constexpr (DPL == 4) {
+                if constexpr (Q8) {  // codes; the value scale is applied once per item
+                    float2 f01, f23;
+                    if constexpr (DPL == 4) {
+                        codes_to_float(
+                            *reinterpret_cast<const uint32_t*>(sV + tok * D + lane * 4), f01, f23);
+                        vf[DP2 - 1] = f23;
+                    } else {
+                        codes_to_float(
+                            *reinterpret_cast<const uint16_t*>(sV + tok * D + lane * 2), f01, f23);
+                    }
+                    vf[0] = f01;
+                } else if constexpr (DPL == 4) {
                     const uint2 w = *reinterpret_cast<const uint2*>(sV + tok * D * 2 + lane * 8);
                     vf[0] = Cv::unpack(w.x);
                     vf[DP2 - 1] = Cv::unpack(w.y);
@@ -619,6 +709,21 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 lh[i2] = b0 ? other : x;
                 lh[NV + i2] = b0 ? x : other;
             }
+        }
+        if constexpr (Q8) {  // value channel d stands for code * v_scale[g][d]
+            float2 vsc[DP2];
+            if constexpr (DPL == 4) {
+                const float4 f =
+                    __ldg(reinterpret_cast<const float4*>(a.v_scale + cur.g * D) + lane);
+                vsc[0] = make_float2(f.x, f.y);
+                vsc[DP2 - 1] = make_float2(f.z, f.w);
+            } else {
+                vsc[0] = __ldg(reinterpret_cast<const float2*>(a.v_scale + cur.g * D) + lane);
+            }
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int e = 0; e < DP2; ++e) o[j][e] = __fmul2_rn(o[j][e], vsc[e]);
         }
         if (cur.ns == 1) {
 #pragma unroll
@@ -665,7 +770,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         p2_idx = __shfl_sync(kFull, p3_lane0, 0);
         load_record(p2_idx, p2a, p2b);
         p3_lane0 = claim();
-        while (issued - consumed < static_cast<uint32_t>(kStages)) {
+        while (issued - consumed < static_cast<uint32_t>(kNst)) {
             const uint32_t before = issued;
             issue_one();
             if (issued == before) break;
@@ -673,7 +778,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     }
     // drain copies still in flight (only after an abort), bounded
     while (consumed < issued) {
-        mbar_wait_warp(&bars[consumed % kStages], (consumed / kStages) & 1);
+        mbar_wait_warp(&bars[consumed % kNst], (consumed / kNst) & 1);
         ++consumed;
     }
 }
@@ -748,8 +853,9 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
     WorkspaceLayout L{};
     const int G = num_q_heads / num_kv_heads;
     // decode rows: every row of a request below the prefill threshold
-    L.max_rows = std::min(total_q_tokens,
-                          num_reqs * std::max(0, std::min(max_q_len, prefill_min_q - 1)));
+    L.max_rows = static_cast<int>(std::min<long long>(
+        total_q_tokens,
+        static_cast<long long>(num_reqs) * std::max(0, std::min(max_q_len, prefill_min_q - 1))));
     L.target_items = 2 * kDecWarps * kItemsPerWarp * num_sms;  // 2 CTAs per SM
     // pages per split >= total / target, so items <= target + one per (row, KV head);
     // pages per split >= kMinSplitPages bounds them by the longest row as well
@@ -784,26 +890,26 @@ int launch_plan(const StepArgs& a, cudaStream_t stream) {
                : PKV_ERR_CUDA;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool Q8>
 static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev0,
                            cudaEvent_t ev1) {
-    using S = DecodeSmem<T, D, G>;
+    using S = DecodeSmem<T, D, G, Q8>;
     static int blocks_per_sm = 0;  // benign race: every thread computes the same value
     if (blocks_per_sm == 0) {
-        if (cudaFuncSetAttribute(decode_kernel<T, D, G>,
+        if (cudaFuncSetAttribute(decode_kernel<T, D, G, Q8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  S::kBytes) != cudaSuccess)
             return PKV_ERR_CUDA;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<T, D, G>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<T, D, G, Q8>,
                                                           kDecThreads, S::kBytes) != cudaSuccess)
             return PKV_ERR_CUDA;
         blocks_per_sm = std::max(1, n);
     }
     const int grid = blocks_per_sm * a.num_sms;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return PKV_ERR_CUDA;
-    if (launch_pdl(decode_kernel<T, D, G>, dim3(grid), dim3(kDecThreads), S::kBytes, stream, a) !=
-        cudaSuccess)
+    if (launch_pdl(decode_kernel<T, D, G, Q8>, dim3(grid), dim3(kDecThreads), S::kBytes, stream,
+                   a) != cudaSuccess)
         return PKV_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return PKV_ERR_CUDA;
     return launch_pdl(combine_kernel<T, D, G>, dim3(std::max(1, a.lay.max_rows * a.num_kv_heads)),
@@ -814,11 +920,16 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
 
 template <typename T, int D>
 static int dispatch_group(const StepArgs& a, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+    const bool q8 = a.kv_int8 != 0;
     switch (a.num_q_heads / a.num_kv_heads) {
-        case 1: return launch_decode_t<T, D, 1>(a, s, e0, e1);
-        case 2: return launch_decode_t<T, D, 2>(a, s, e0, e1);
-        case 4: return launch_decode_t<T, D, 4>(a, s, e0, e1);
-        case 8: return launch_decode_t<T, D, 8>(a, s, e0, e1);
+        case 1: return q8 ? launch_decode_t<T, D, 1, true>(a, s, e0, e1)
+                          : launch_decode_t<T, D, 1, false>(a, s, e0, e1);
+        case 2: return q8 ? launch_decode_t<T, D, 2, true>(a, s, e0, e1)
+                          : launch_decode_t<T, D, 2, false>(a, s, e0, e1);
+        case 4: return q8 ? launch_decode_t<T, D, 4, true>(a, s, e0, e1)
+                          : launch_decode_t<T, D, 4, false>(a, s, e0, e1);
+        case 8: return q8 ? launch_decode_t<T, D, 8, true>(a, s, e0, e1)
+                          : launch_decode_t<T, D, 8, false>(a, s, e0, e1);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }

@@ -72,6 +72,93 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
     }
 }
 
+// INT8 pools (wmrh.cn/news/64708 §4.3: the KV cache in INT8 halves its memory and
+// bandwidth; §5.4: calibrated per channel).  Same placement as kv_append_kernel; each value
+// x of channel (h, d) is stored as clamp(rint(x / s[h][d]), -127, 127), the quotient in IEEE
+// fp32 and rint rounding to nearest even.  One warp per (token, KV head); lane l quantises
+// channels l*DPL .. l*DPL+DPL-1 of K and of V and stores them as one packed word.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendArgs a) {
+    constexpr int DPL = D / 32;  // channels per lane: 4 or 2
+    using Cv = F16<T>;
+    const int r = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    if (r == 0 && blockIdx.x == 0 && threadIdx.x == 0 &&
+        (a.q_offsets[0] != 0 || a.q_offsets[a.num_reqs] != a.total_q_tokens))
+        set_error(a.err, PKV_DEVERR_TOKENS);
+    const int qlen = __ldg(a.q_lens + r);
+    const int start = __ldg(a.q_offsets + r);
+    const int ctx = __ldg(a.context_lens + r);
+    const int tok0 = blockIdx.x * kTokPerBlock;
+    if (tok0 >= qlen) return;
+    if (__ldg(a.q_offsets + r + 1) - start != qlen || ctx < 0 || qlen > a.max_q_len ||
+        start + qlen > a.total_q_tokens) {
+        if (threadIdx.x == 0) set_error(a.err, PKV_DEVERR_TOKENS);
+        return;
+    }
+    const int ntok = min(kTokPerBlock, qlen - tok0);
+    const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.max_pages;
+    auto quant = [](float x, float s) {
+        const int c = max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
+        return static_cast<uint32_t>(c) & 0xFFu;  // the code's two's-complement byte
+    };
+    for (int w = warp; w < ntok * a.num_kv_heads; w += blockDim.x / 32) {
+        const int i = tok0 + w / a.num_kv_heads, h = w % a.num_kv_heads;
+        const int t = start + i;
+        const int pos = ctx + i;
+        const int lp = pos / kPage;
+        if (lp >= a.max_pages) {
+            if (lane == 0) set_error(a.err, PKV_DEVERR_TABLE_RANGE);
+            continue;
+        }
+        const int page = __ldg(bt + lp);
+        if (page < 0 || page >= a.num_pages) {
+            if (lane == 0) set_error(a.err, PKV_DEVERR_PAGE_RANGE);
+            continue;
+        }
+        const int slot = pos % kPage;
+        if (h == 0 && lane == 0 && a.slot_mapping)
+            a.slot_mapping[t] = static_cast<int64_t>(page) * kPage + slot;
+        const int64_t src = (static_cast<int64_t>(t) * a.num_kv_heads + h) * D + lane * DPL;
+        const int64_t dst =
+            ((static_cast<int64_t>(page) * a.num_kv_heads + h) * kPage + slot) * D + lane * DPL;
+        const int chan = h * D + lane * DPL;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint16_t* sp = static_cast<const uint16_t*>(kv ? a.v_new : a.k_new) + src;
+            const float* sc = (kv ? a.v_scale : a.k_scale) + chan;
+            uint8_t* dp = static_cast<uint8_t*>(kv ? a.v_cache : a.k_cache) + dst;
+            if constexpr (DPL == 4) {
+                const uint2 xw = __ldg(reinterpret_cast<const uint2*>(sp));
+                const float4 s4 = __ldg(reinterpret_cast<const float4*>(sc));
+                const float2 x01 = Cv::unpack(xw.x), x23 = Cv::unpack(xw.y);
+                *reinterpret_cast<uint32_t*>(dp) =
+                    quant(x01.x, s4.x) | (quant(x01.y, s4.y) << 8) |
+                    (quant(x23.x, s4.z) << 16) | (quant(x23.y, s4.w) << 24);
+            } else {
+                const uint32_t xw = __ldg(reinterpret_cast<const uint32_t*>(sp));
+                const float2 s2 = __ldg(reinterpret_cast<const float2*>(sc));
+                const float2 x01 = Cv::unpack(xw);
+                *reinterpret_cast<uint16_t*>(dp) =
+                    static_cast<uint16_t>(quant(x01.x, s2.x) | (quant(x01.y, s2.y) << 8));
+            }
+        }
+    }
+}
+
+int launch_kv_append_int8(const AppendArgs& a, cudaStream_t stream) {
+    if (a.total_q_tokens == 0 || a.num_reqs == 0) return PKV_OK;
+    if (a.num_reqs > 65535) return PKV_ERR_UNSUPPORTED;
+    const dim3 grid(cdiv(a.max_q_len, kTokPerBlock), a.num_reqs);
+    const bool bf = a.dtype == PKV_BF16, d128 = a.head_dim == 128;
+    auto* k = bf ? (d128 ? kv_append_int8_kernel<__nv_bfloat16, 128>
+                         : kv_append_int8_kernel<__nv_bfloat16, 64>)
+                 : (d128 ? kv_append_int8_kernel<__half, 128> : kv_append_int8_kernel<__half, 64>);
+    return launch_pdl(k, grid, dim3(256), 0, stream, a) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 // context_lens[r] += q_lens[r]: the step's tokens are now cached.  Earlier kernels on the
 // stream (the attention step) read the lengths, so the update waits for them.
 __global__ void __launch_bounds__(256) advance_context_kernel(const int32_t* q_lens,

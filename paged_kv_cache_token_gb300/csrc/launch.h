@@ -12,6 +12,9 @@ namespace pkv {
 
 struct AppendArgs {
     int num_reqs, num_kv_heads, head_dim, num_pages, max_pages, total_q_tokens, max_q_len;
+    int dtype;                 // of k_new / v_new
+    const float* k_scale;      // [Hkv][D] per-channel INT8 scales (INT8 pools only)
+    const float* v_scale;
     const int32_t* q_lens;
     const int32_t* q_offsets;
     const int32_t* context_lens;
@@ -57,6 +60,9 @@ struct StepArgs {
     int prefill_min_q;  // requests with q_len >= this go to the tensor-core prefill path
     int heads_per_tile; // query heads per prefill tile (2 when a KV group has an even size)
     int32_t* err;
+    int kv_int8;        // K/V pools hold INT8 codes with per-channel scales
+    const float* k_scale;  // [Hkv][D], INT8 pools only
+    const float* v_scale;
 };
 
 WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -85,6 +91,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+int launch_kv_append_int8(const AppendArgs& a, cudaStream_t stream);
 int launch_advance_context(const int32_t* q_lens, int32_t* context_lens, int num_reqs,
                            cudaStream_t stream);
 int launch_plan(const StepArgs& a, cudaStream_t stream);

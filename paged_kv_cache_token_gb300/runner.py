@@ -38,19 +38,37 @@ class DeviceStep:
     tensors: tuple
 
 
+INT8_SENTINEL = -128  # a code the quantiser never writes (it clamps to +-127)
+
+
 class PagedKV:
-    """Two page pools [num_pages, Hkv, 16, D] on one device plus an error flag."""
+    """Two page pools [num_pages, Hkv, 16, D] on one device plus an error flag.
+
+    With ``k_scale``/``v_scale`` (float32 [Hkv, D], one fixed scale per KV head and channel)
+    the pools hold INT8 codes and every call goes through the library's INT8 entry points;
+    Q, the new K/V and the output keep the 16-bit dtype either way.
+    """
 
     def __init__(self, num_pages: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                 dtype_code: int, device="cuda", fill_sentinel: bool = True):
+                 dtype_code: int, device="cuda", fill_sentinel: bool = True,
+                 k_scale=None, v_scale=None):
         self.num_pages, self.hq, self.hkv, self.d = num_pages, num_q_heads, num_kv_heads, head_dim
         self.dtype_code = dtype_code
         self.dtype = TORCH_DTYPE[dtype_code]
         self.device = torch.device(device)
+        self.kv_int8 = k_scale is not None
         shape = (num_pages, num_kv_heads, 16, head_dim)
-        self.k_cache = torch.empty(shape, dtype=self.dtype, device=self.device)
-        self.v_cache = torch.empty(shape, dtype=self.dtype, device=self.device)
-        if fill_sentinel:
+        pool_dtype = torch.int8 if self.kv_int8 else self.dtype
+        self.k_cache = torch.empty(shape, dtype=pool_dtype, device=self.device)
+        self.v_cache = torch.empty(shape, dtype=pool_dtype, device=self.device)
+        if self.kv_int8:
+            as_dev = lambda x: torch.as_tensor(np.asarray(x, np.float32)).reshape(
+                num_kv_heads, head_dim).to(self.device).contiguous()
+            self.k_scale, self.v_scale = as_dev(k_scale), as_dev(v_scale)
+            if fill_sentinel:
+                self.k_cache.fill_(INT8_SENTINEL)
+                self.v_cache.fill_(INT8_SENTINEL)
+        elif fill_sentinel:
             self.k_cache.view(torch.int16).fill_(-1)
             self.v_cache.view(torch.int16).fill_(-1)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -72,25 +90,42 @@ class PagedKV:
         return DeviceStep(plan, desc, (ql, qo, cl, bt))
 
     def workspace(self, desc) -> torch.Tensor:
-        need = max(256, binding.attention_workspace_bytes(desc))
+        need = binding.attention_workspace_bytes_int8(desc) if self.kv_int8 else \
+            binding.attention_workspace_bytes(desc)
+        need = max(256, need)
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
         return self._ws
 
     # ------------------------------------------------------------------ calls
+    def append_desc(self, desc, k_new, v_new, slot_mapping=None, stream=None) -> None:
+        """kv_append (16-bit or INT8 pools) for a StepDesc whose arrays are on the device."""
+        if self.kv_int8:
+            binding.kv_append_int8(desc, k_new, v_new, self.k_scale, self.v_scale,
+                                   self.k_cache, self.v_cache, slot_mapping, self.err, stream)
+        else:
+            binding.kv_append(desc, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
+                              self.err, stream)
+
+    def attention_desc(self, desc, q, out, scale: float, ws, stream=None) -> None:
+        """The attention step (16-bit or INT8 pools) into ``out``."""
+        if self.kv_int8:
+            binding.paged_attention_step_int8(desc, q, self.k_cache, self.v_cache, self.k_scale,
+                                              self.v_scale, out, scale, ws, self.err, stream)
+        else:
+            binding.paged_attention_step(desc, q, self.k_cache, self.v_cache, out, scale, ws,
+                                         self.err, stream)
+
     def append(self, ds: DeviceStep, k_new: torch.Tensor, v_new: torch.Tensor,
                slot_mapping: Optional[torch.Tensor] = None, stream=None) -> None:
-        binding.kv_append(ds.desc, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
-                          self.err, stream)
+        self.append_desc(ds.desc, k_new, v_new, slot_mapping, stream)
 
     def attention(self, ds: DeviceStep, q: torch.Tensor, scale: float,
                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         if out is None:
             out = torch.empty((ds.plan.total_q_tokens, self.hq, self.d), dtype=self.dtype,
                               device=self.device)
-        ws = self.workspace(ds.desc)
-        binding.paged_attention_step(ds.desc, q, self.k_cache, self.v_cache, out, scale, ws,
-                                     self.err, stream)
+        self.attention_desc(ds.desc, q, out, scale, self.workspace(ds.desc), stream)
         return out
 
     def read_error(self) -> int:
@@ -189,11 +224,9 @@ class StepStaging:
 
     def run(self, scale: float, stream=None) -> None:
         """kv_append then the attention step, on the staged device views."""
-        binding.kv_append(self.desc, self.k_new, self.v_new, self.kv.k_cache, self.kv.v_cache,
-                          None, self.kv.err, stream)
-        ws = self.kv.workspace(self.desc)
-        binding.paged_attention_step(self.desc, self.q, self.kv.k_cache, self.kv.v_cache,
-                                     self.out, scale, ws, self.kv.err, stream)
+        self.kv.append_desc(self.desc, self.k_new, self.v_new, None, stream)
+        self.kv.attention_desc(self.desc, self.q, self.out, scale,
+                               self.kv.workspace(self.desc), stream)
 
     def download(self) -> None:
         """Device -> host copy of the step's output on the current stream."""
@@ -248,10 +281,8 @@ class DecodeLoop:
         kv = self.kv
         self.ctx.copy_(self.ctx0, non_blocking=True)
         for s in range(self.steps):
-            binding.kv_append(self.desc, self.k_new[s], self.v_new[s], kv.k_cache, kv.v_cache,
-                              None, kv.err, stream)
-            binding.paged_attention_step(self.desc, self.q[s], kv.k_cache, kv.v_cache,
-                                         self.out[s], self.scale, self.ws, kv.err, stream)
+            kv.append_desc(self.desc, self.k_new[s], self.v_new[s], None, stream)
+            kv.attention_desc(self.desc, self.q[s], self.out[s], self.scale, self.ws, stream)
             binding.advance_context(self.desc, self.ctx, stream)
 
     def run(self) -> torch.Tensor:
@@ -293,9 +324,12 @@ def step_host_inputs(workload, plan: StepPlan):
         cat(vs, workload.num_kv_heads)
 
 
-def paged_kv_for(workload, device="cuda", fill_sentinel=True) -> PagedKV:
+def paged_kv_for(workload, device="cuda", fill_sentinel=True, kv_int8=False) -> PagedKV:
+    """Pools for a workload; with ``kv_int8`` INT8 pools with the workload's seeded
+    per-channel scales."""
+    ks, vs = workload.int8_scales() if kv_int8 else (None, None)
     return PagedKV(workload.num_pages, workload.num_q_heads, workload.num_kv_heads,
-                   workload.head_dim, workload.dtype, device, fill_sentinel)
+                   workload.head_dim, workload.dtype, device, fill_sentinel, ks, vs)
 
 
 def load_history(kv: PagedKV, workload, plan: Optional[StepPlan]) -> None:

@@ -7,7 +7,8 @@ oracle consume what it produces; neither is imported here.
 Recipe (all values exact, all draws reproducible):
 
 * Every request ``r`` of workload ``w`` owns three independent ``torch.Generator``
-  streams seeded ``(1000 + w) * 2**20 + 4 * r + kind`` (kind 0 = Q, 1 = K, 2 = V).
+  streams seeded ``(1000 + w) * 2**20 + 4 * r + kind`` (kind 0 = Q, 1 = K, 2 = V; kind 3 of
+  requests 0 and 1 draws an INT8 cache's K and V per-channel scales).
   Values are fp32 N(0, 1) draws rounded to bf16 / fp16 with round-to-nearest-even
   (torch's ``.to(dtype)``), kept as their 16-bit patterns.
 * K and V exist for every position the request will ever hold (cached history plus the
@@ -100,6 +101,19 @@ class Workload:
             req = self.requests[rid]
             shape = (req.processed, self.num_q_heads, self.head_dim)
             self._cache[key] = draw_bits(_seed(self.index, rid, 0), shape, self.dtype)
+        return self._cache[key]
+
+    def int8_scales(self):
+        """(k_scale, v_scale) float32 [Hkv, D] for an INT8 cache: one fixed scale per KV head
+        and channel, drawn uniform in [0.02, 0.04) (127 codes then span |x| up to 2.5..5.1,
+        so the N(0, 1) values are mostly in range and a few clamp)."""
+        key = ("int8_scales",)
+        if key not in self._cache:
+            shape = (self.num_kv_heads, self.head_dim)
+            draw = lambda r: (0.02 + 0.02 * torch.rand(
+                *shape, generator=torch.Generator().manual_seed(_seed(self.index, r, 3)),
+                dtype=torch.float32)).numpy()
+            self._cache[key] = (draw(0), draw(1))
         return self._cache[key]
 
     def drop(self, rid: int) -> None:

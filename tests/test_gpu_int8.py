@@ -1,0 +1,208 @@
+"""GPU parity of the INT8 KV cache (wmrh.cn/news/64708 §4.3, §5.4) through the C ABI: the
+codes kv_append writes must equal the oracle's quantiser bit for bit, in the slots the
+block table names; attention over the codes must be within max-abs 2e-2 and mean-abs 2e-3
+of the oracle's fp64 attention over the values the codes stand for."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_token_gb300 import binding, build, runner
+from paged_kv_cache_token_gb300 import workloads as W
+from paged_kv_cache_token_gb300.scheduler import scheduler_for
+
+from gpu_common import assert_close, gpu_as_f64, oracle_rows_int8, request_codes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.load()
+
+
+def custom(index, hq, hkv, d, dtype, specs, budget=1 << 30, chunk_cap=None, extra_pages=8):
+    reqs = [W.RequestSpec(i, *s) for i, s in enumerate(specs)]
+    need = sum(-(-r.total // 16) for r in reqs) + extra_pages
+    g = torch.Generator().manual_seed(9000 + index)
+    order = torch.randperm(need, generator=g).numpy().astype(np.int32)
+    return W.Workload(index, "custom-int8", hq, hkv, d, dtype, reqs, order, need, budget=budget,
+                      chunk_cap=chunk_cap)
+
+
+def run_all_int8(w, check_rows=None):
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, kv_int8=True)
+    runner.load_history(kv, w, s.history_plan())
+    worst, outs = (0.0, 0.0), []
+    for i, plan in enumerate(s.all_steps()):
+        out = runner.run_step(kv, w, plan)
+        rows = None if check_rows is None else check_rows(plan)
+        ref = oracle_rows_int8(w, plan, rows)
+        got = gpu_as_f64(out) if rows is None else gpu_as_f64(out[torch.as_tensor(rows)])
+        assert kv.read_error() == 0
+        mx, mean = assert_close(got, ref, "%s int8 step %d" % (w.name, i))
+        worst = (max(worst[0], mx), max(worst[1], mean))
+        outs.append(out)
+    assert kv.read_error() == 0
+    return worst, outs, kv
+
+
+def expected_pools(w, kv_steps):
+    """Pools the oracle writes: its codes (as bytes in uint16 cells) placed by its append."""
+    shape = (w.num_pages, w.num_kv_heads, 16, w.head_dim)
+    kp = np.full(shape, 0x80, np.uint16)   # INT8 sentinel -128 as a byte
+    vp = kp.copy()
+    slots = []
+    for plan in kv_steps:
+        kc = np.concatenate([request_codes(w, r)[0][c:c + n] for r, c, n in
+                             zip(plan.rids, plan.context_lens.tolist(), plan.q_lens.tolist())])
+        vc = np.concatenate([request_codes(w, r)[1][c:c + n] for r, c, n in
+                             zip(plan.rids, plan.context_lens.tolist(), plan.q_lens.tolist())])
+        as_u16 = lambda x: x.view(np.uint8).astype(np.uint16)
+        kp, vp, sl = oracle.kv_append(plan.q_lens, plan.context_lens, plan.block_table,
+                                      w.num_pages, as_u16(kc), as_u16(vc), kp, vp)
+        slots.append(sl)
+    to_i8 = lambda p: p.astype(np.uint8).view(np.int8)
+    return to_i8(kp), to_i8(vp), slots
+
+
+# ------------------------------------------------------------------------------ kv_append
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(4, 2, 64, 0), (32, 8, 128, 0), (6, 3, 128, 1),
+                                            (8, 1, 64, 1)])
+def test_int8_append_codes_bit_exact(hq, hkv, d, dtype):
+    # histories and prompts across page edges, then decode steps; every pool byte and every
+    # slot id must equal the oracle's
+    specs = [(0, 1, 2), (15, 1, 1), (16, 17, 1), (31, 0, 3), (100, 40, 0), (0, 0, 2)]
+    w = custom(700 + hq + d + dtype, hq, hkv, d, dtype, specs, budget=64)
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, kv_int8=True)
+    steps = [p for p in [s.history_plan()] + s.all_steps() if p is not None]
+    got_slots = []
+    for plan in steps:
+        _, k, v = runner.step_host_inputs(w, plan)
+        ds = kv.upload(plan)
+        slots = torch.full((plan.total_q_tokens,), -7, dtype=torch.int64, device="cuda")
+        kv.append(ds, runner.bits_to_tensor(k, w.dtype), runner.bits_to_tensor(v, w.dtype),
+                  slots)
+        got_slots.append(slots.cpu().numpy())
+    ref_k, ref_v, ref_slots = expected_pools(w, steps)
+    assert kv.read_error() == 0
+    assert np.array_equal(kv.k_cache.cpu().numpy(), ref_k)
+    assert np.array_equal(kv.v_cache.cpu().numpy(), ref_v)
+    assert all(np.array_equal(a, b) for a, b in zip(got_slots, ref_slots))
+
+
+def test_int8_append_ties_and_clamps_exact():
+    # K/V values placed on code ties (k + 0.5) * s and past the +-127 range: the kernel's
+    # rounding (ties to even) and clamping must equal the oracle's
+    w = custom(750, 4, 2, 64, 0, [(0, 40, 0)])
+    ks, vs = w.int8_scales()
+    rng = np.random.default_rng(5)
+    codes = rng.integers(-140, 141, size=(40, 2, 64)).astype(np.float32)
+    # channels 0..31: s = 2^-5 and |2c + 1| <= 127, so bf16 holds x = (c + 0.5) * s exactly
+    # and x / s is an exact tie; channels 32..63 keep the drawn scales and reach past +-127
+    codes[:, :, :32] = rng.integers(-64, 64, size=(40, 2, 32))
+    ks = ks.copy()
+    ks[:, :32] = 2.0 ** -5
+    vs = ks.copy()
+    x = (codes + 0.5) * ks[None]
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w._cache[("kv", 0)] = (bits, bits.copy())
+    w._cache[("int8_scales",)] = (ks, vs)
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, kv_int8=True)
+    plan = s.next_step()
+    _, k, v = runner.step_host_inputs(w, plan)
+    ds = kv.upload(plan)
+    kv.append(ds, runner.bits_to_tensor(k, 0), runner.bits_to_tensor(v, 0))
+    ref_k, ref_v, _ = expected_pools(w, [plan])
+    assert kv.read_error() == 0
+    got = kv.k_cache.cpu().numpy()
+    assert np.array_equal(got, ref_k) and np.array_equal(kv.v_cache.cpu().numpy(), ref_v)
+    # the case really has ties and clamps
+    ref_codes = request_codes(w, 0)[0]
+    assert (np.abs(ref_codes) == 127).sum() > 100
+    assert (ref_codes[:, :, :32] % 2 == 0).all()    # exact ties round to the even code
+
+
+def test_int8_append_rejects_missing_or_unaligned_scales():
+    w = custom(760, 4, 2, 64, 0, [(0, 3, 0)])
+    kv = runner.paged_kv_for(w, kv_int8=True)
+    plan = scheduler_for(w).next_step()
+    _, k, v = runner.step_host_inputs(w, plan)
+    ds = kv.upload(plan)
+    kt, vt = runner.bits_to_tensor(k, 0), runner.bits_to_tensor(v, 0)
+    rc = binding.kv_append_int8(ds.desc, kt, vt, None, kv.v_scale, kv.k_cache, kv.v_cache,
+                                check=False)
+    assert rc == -1
+    off = torch.empty(2 * 64 + 1, dtype=torch.float32, device="cuda")[1:]
+    rc = binding.kv_append_int8(ds.desc, kt, vt, off, kv.v_scale, kv.k_cache, kv.v_cache,
+                                check=False)
+    assert rc == -1
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------------------ attention
+def test_int8_tiny_all_steps():
+    run_all_int8(W.tiny())
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(4, 2, 64, 0), (32, 8, 128, 0), (8, 8, 128, 1),
+                                            (16, 2, 128, 1), (8, 1, 64, 0), (6, 3, 64, 1)])
+def test_int8_decode_batches(hq, hkv, d, dtype):
+    ctx = [0, 1, 15, 16, 17, 100, 255, 256, 1000, 3000]  # one key, page edges, multi-split
+    run_all_int8(custom(800 + hq + d, hq, hkv, d, dtype, [(c, 0, 2) for c in ctx]))
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(4, 2, 64, 0), (32, 8, 128, 0), (8, 2, 128, 1)])
+def test_int8_prefill_chunks_stream_path(hq, hkv, d, dtype):
+    # chunks of up to 96 rows over histories: every row goes through the streaming kernel
+    specs = [(0, 1, 1), (0, 127, 1), (0, 129, 2), (0, 300, 1), (20, 33, 0), (500, 64, 1)]
+    run_all_int8(custom(900 + hq + d, hq, hkv, d, dtype, specs, budget=160, chunk_cap=96))
+
+
+def test_int8_long_rows():
+    # a decode row over 131,071 cached tokens (thousands of splits per KV head) and a
+    # 700-row prefill chunk in one step: rows many 32-row groups long in the work-list fill
+    worst, _, _ = run_all_int8(custom(950, 32, 8, 128, 0, [(131071, 0, 1), (3000, 700, 0)]))
+    assert worst[0] < 2e-2
+
+
+def test_int8_mha_skew_all_64_steps():
+    worst, _, _ = run_all_int8(W.mha_skew())
+    print("int8 mha-skew worst", worst)
+
+
+def test_int8_decode_only_full_sampled():
+    """The decode batch (64 requests, ctx U[512, 4096], 32/8 heads, d=128, bf16): every
+    request's row against the oracle."""
+    worst, _, _ = run_all_int8(W.decode_only())
+    print("int8 decode-only worst", worst)
+
+
+def test_int8_decode_loop_graph_bitwise_identical():
+    w = W.mha_skew()
+
+    def fresh():
+        s = scheduler_for(w)
+        kv = runner.paged_kv_for(w, kv_int8=True)
+        runner.load_history(kv, w, s.history_plan())
+        return s, kv
+
+    s, kv = fresh()
+    plans = s.all_steps()
+    ref = torch.stack([runner.run_step(kv, w, p) for p in plans])
+    ref_pool = (kv.k_cache.clone(), kv.v_cache.clone())
+    s, kv = fresh()
+    loop = runner.DecodeLoop(kv, w, plans)
+    loop.capture()
+    kv.k_cache.fill_(runner.INT8_SENTINEL)
+    kv.v_cache.fill_(runner.INT8_SENTINEL)
+    runner.load_history(kv, w, scheduler_for(w).history_plan())
+    out = loop.replay()
+    torch.cuda.synchronize()
+    assert kv.read_error() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(kv.k_cache, ref_pool[0]) and torch.equal(kv.v_cache, ref_pool[1])
