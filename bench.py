@@ -10,6 +10,8 @@ times the tensor-core-bound workload: one-shot causal prefill of 8,192 tokens (3
 d=128) and the same prompt as 4 x 2,048-token chunks, in TFLOP/s of causal attention FLOPs.
 The object "decode_loop" times 64 consecutive decode steps of the MHA-skew workload as
 separate steps, as one device-side loop and as one CUDA graph replay (per-step overhead).
+The object "int8_kv" times the decode step over INT8 pages (per-channel scales): half the
+K/V bytes of the bf16 step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -50,15 +52,18 @@ def peaks():
 
 
 # ------------------------------------------------------------------------------ accounting
-def step_bytes(w, plan):
-    """Algorithmic bytes of one step: every byte the definition has to touch once."""
+def step_bytes(w, plan, kv_esz=2):
+    """Algorithmic bytes of one step: every byte the definition has to touch once.  With
+    kv_esz = 1 (INT8 pages) the pages hold one byte per element and the per-channel K and V
+    scales are read once by each kernel."""
     esz = 2
     hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
     T = plan.total_q_tokens
     kv_tokens = int((plan.context_lens.astype(np.int64) + plan.q_lens).sum())
-    attn_kv = kv_tokens * hkv * d * esz * 2           # K and V read once per KV head
+    scales = 0 if kv_esz == 2 else 2 * hkv * d * 4
+    attn_kv = kv_tokens * hkv * d * kv_esz * 2 + scales  # K and V read once per KV head
     q_out = T * hq * d * esz * 2                       # Q read, output written
-    append = T * hkv * d * esz * 2 * 2                 # K_new, V_new read and written
+    append = T * hkv * d * (esz + kv_esz) * 2 + scales  # K_new, V_new read, pages written
     pages = int(((plan.context_lens + plan.q_lens + 15) // 16).sum())
     meta = pages * 4 + plan.num_reqs * 12
     return dict(attention=attn_kv + q_out + meta, append=append,
@@ -258,6 +263,54 @@ def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
                 h2d=h2d, d2h=d2h, clocks=clocks.summary(), launches=4 * steps)
 
 
+def time_decode_int8(device, steps, pool_pages=70000):
+    """The decode step over INT8 pages (same requests and shapes; per-channel scales): step
+    time, decode-kernel time and their algorithmic bytes."""
+    from paged_kv_cache_token_gb300 import binding, runner
+    w = W.decode_only(num_pages=pool_pages)
+    s = scheduler_for(w)
+    hist, plan = s.history_plan(), s.next_step()
+    kv = runner.paged_kv_for(w, device=device, fill_sentinel=False, kv_int8=True)
+    runner.load_history(kv, w, hist)
+    qh, kh, vh = runner.step_host_inputs(w, plan)
+    q, k_new, v_new = (runner.bits_to_tensor(x, w.dtype, device) for x in (qh, kh, vh))
+    ds = kv.upload(plan)
+    out = torch.empty((plan.total_q_tokens, w.num_q_heads, w.head_dim), dtype=kv.dtype,
+                      device=device)
+    ws = kv.workspace(ds.desc)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        kv.append_desc(ds.desc, k_new, v_new, None, stream)
+        kv.attention_desc(ds.desc, q, out, w.scale, ws, stream)
+
+    for _ in range(3):
+        one_step()
+    torch.cuda.synchronize()
+    assert kv.read_error() == 0
+    kstart = [lib_event() for _ in range(steps)]
+    kstop = [lib_event() for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        binding.set_kernel_events(0, kstart[i], kstop[i])
+        one_step()
+    binding.set_kernel_events(0, None, None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert kv.read_error() == 0
+    ms_step = t0.elapsed_time(t1) / steps
+    ms_kernel = float(np.mean([a.elapsed_time(b) for a, b in zip(kstart, kstop)]))
+    acct = step_bytes(w, plan, kv_esz=1)
+    res = dict(ms_step=ms_step, ms_kernel=ms_kernel, step_bytes=acct["step"],
+               kernel_bytes=acct["attention"],
+               step_GBps=acct["step"] / (ms_step * 1e-3) / 1e9,
+               kernel_GBps=acct["attention"] / (ms_kernel * 1e-3) / 1e9)
+    del kv
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_prefill(device, reps=3):
     """Attention-kernel time of the 8K one-shot prefill and of the 4 x 2048 chunks."""
     from paged_kv_cache_token_gb300 import binding, runner
@@ -450,7 +503,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-loop", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode-loop"], default=None,
+    ap.add_argument("--no-int8", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode-loop", "int8"], default=None,
                     help="time only the prefill workload (one-shot 8K and 4 x 2K) and print "
                          "its JSON object; used for focused profiler captures")
     ap.add_argument("--pool-pages", type=int, default=70000,
@@ -473,6 +527,11 @@ def main():
             if dist_ctx.rank == 0:
                 pf = time_prefill(device)
                 print(json.dumps({"prefill_chunk": pf, "peak_tflops": bf16}))
+            return
+        if args.only == "int8":
+            if dist_ctx.rank == 0:
+                print(json.dumps({"int8_kv": time_decode_int8(device, args.steps,
+                                                              args.pool_pages)}))
             return
         if args.only == "decode-loop":
             if dist_ctx.rank == 0:
@@ -535,6 +594,16 @@ def main():
                         "in L2, so GB/s here is not an HBM rate; the comparison is between "
                         "launch modes" % (dl["bytes_per_step"] / 1e6),
                 **dl}
+        if not args.no_int8 and dist_ctx.rank == 0:
+            q8 = time_decode_int8(device, args.steps, args.pool_pages)
+            line["int8_kv"] = {
+                "workload": "the decode-only step over INT8 pages (per-channel K and V "
+                            "scales; Q, new K/V and output bf16)",
+                **q8, "speedup_vs_bf16_step": r["ms_step"] / q8["ms_step"],
+                "roofline": {"bound": "hbm", "kernel": "decode_kernel (INT8 pages)",
+                             "achieved": q8["kernel_GBps"], "peak": hbm, "unit": "GB/s",
+                             "frac": q8["kernel_GBps"] / hbm,
+                             "peak_source": peak_src + " hbm_gbs", "traffic": None}}
         if not args.no_cpu_baseline and dist_ctx.rank == 0:
             secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
             line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores,

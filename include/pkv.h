@@ -195,10 +195,15 @@ PKV_API int pkv_paged_attention_step_static_ws(const pkv_step_desc* desc, const 
  *   code  = clamp(round_half_even(x / scale[h][c]), -127, 127)   (IEEE fp32 quotient)
  *   value = code * scale[h][c]
  * The attention step reads the codes and attends over the values they stand for; all of
- * its arithmetic stays fp32 as in the 16-bit path.  Every row (decode and prefill chunk)
- * runs on the streaming kernel.
+ * scores and weighted sums run on the tensor cores with fp16 operands: the codes exactly,
+ * q times the key scales (scaled by a power of two into fp16 range) and the softmax weights
+ * rounded to fp16, fp32 accumulation and softmax.  Every row (decode and prefill chunk) runs
+ * on the streaming kernel.
  *   k_scale, v_scale   device fp32 [num_kv_heads][head_dim], 16-byte aligned, > 0
- *   k_cache, v_cache   device int8 [num_pages][num_kv_heads][16][head_dim]
+ *   k_cache            device int8 [num_pages][num_kv_heads][16][head_dim]
+ *   v_cache            device int8 [num_pages][num_kv_heads][head_dim][16]: within a page
+ *                      block the 16 tokens of one dim are contiguous (the order the
+ *                      tensor-core value fragments read)
  * Other arguments, errors and the device error flag are those of the 16-bit calls;
  * k_new, v_new, q and out keep desc->dtype.
  */

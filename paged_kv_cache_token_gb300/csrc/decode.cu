@@ -276,28 +276,53 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
 // decode: independent warps pull items; see the file comment for the data flow.
 // ------------------------------------------------------------------------------------
 // Q8: the pools hold INT8 codes (half the bytes per page, so twice the ring stages keep the
-// same bytes in flight).
+// same bytes in flight; the scores need no shared-memory staging).
 template <typename T, int D, int G, bool Q8>
 struct DecodeSmem {
     static constexpr int kNst = Q8 ? 2 * kStages : kStages;
     static constexpr int kPageBytes = kPage * D * (Q8 ? 1 : 2);  // one K (or V) page block
     static constexpr int kStageBytes = 2 * kPageBytes;
     static constexpr int kRing = kDecWarps * kNst * kStageBytes;
-    static constexpr int kPbuf = kDecWarps * kPage * G * 8;  // (p, p) pairs per token, head
+    static constexpr int kPbuf = Q8 ? 0 : kDecWarps * kPage * G * 8;  // (p, p) per token, head
     static constexpr int kBars = kDecWarps * kNst * 8;
     static constexpr int kBytes = kRing + kPbuf + kBars;
 };
 
-// Four INT8 codes (one 32-bit word) to floats, exactly: with the sign bit flipped, a code's
-// byte u = code + 128 becomes the low mantissa byte of 2^23 + u, and subtracting 2^23 + 128
-// leaves the code.  Returns codes (0, 1) and (2, 3) as pairs.
-__device__ __forceinline__ void codes_to_float(uint32_t w, float2& f01, float2& f23) {
-    const uint32_t x = w ^ 0x80808080u;
-    const float2 bias = make_float2(-8388736.f, -8388736.f);
-    f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650)),
-                                 __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7651))), bias);
-    f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7652)),
-                                 __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7653))), bias);
+// ---- INT8 pages on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulate).
+// A code c of byte u = c + 128 (sign bit flipped) becomes the fp16 number 1024 + u exactly
+// when u is the low byte under an exponent byte 0x64.  Keys enter the score MMA in that
+// form: every key dim then carries an extra 1152 (= 1024 + 128), which adds
+// 1152 * sum_d q'_d to every score of a query head -- the same for every token, so the
+// softmax is unchanged.  Values get the 1152 subtracted (exact in fp16) because they are
+// summed with weights.
+__device__ __forceinline__ uint32_t codes_lo_h2(uint32_t x) {  // bytes 0, 1 -> 1024 + u
+    return __byte_perm(x, 0x6464u, 0x4140);
+}
+__device__ __forceinline__ uint32_t codes_hi_h2(uint32_t x) {  // bytes 2, 3 -> 1024 + u
+    return __byte_perm(x, 0x6464u, 0x4342);
+}
+__device__ __forceinline__ uint32_t minus_1152_h2(uint32_t h) {
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__float2half(1152.f)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// d += A (16x16, row-major fragments a0..a3) * B (16x8, col-major fragments b0, b1)
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// transpose of an 8x8 16-bit matrix held one row-pair register per thread
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 // One work item as a warp sees it.
@@ -318,6 +343,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     constexpr int DP2 = DPL / 2;    // ... as float2 pairs
     constexpr int N0 = 4 * G, N1 = N0 / 2, N2 = N1 / 2 > 0 ? N1 / 2 : 1;
     constexpr int NV = (N2 >= 2) ? N2 / 2 : 1;  // score values a lane holds after reduction
+    // INT8: lane (qg, t4) = (lane / 4, lane % 4) in the MMA fragment layouts.  In the score
+    // MMA (S^T = K q'^T: rows = tokens, k = dims, n = query heads) the lane's k-slots of step
+    // kk are dims t4 * D/4 + 4 kk .. + 3, so its key bytes are D/4 contiguous ones per row.
+    constexpr int KW = D / 16;      // MMA k-steps over the dims = key words per row per lane
+    constexpr int NQ = Q8 ? D / 32 : G * NCH;  // 16-byte q chunks a lane holds
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -346,10 +376,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     const uint64_t kv_policy = l2_policy_evict_first();
     const int c8 = lane & 7, tg = lane >> 3;
     const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
-    // staggered chunk order: conflict-free 16-byte loads of 256-byte 16-bit key rows (a
-    // 128-byte INT8 row needs none)
-    const int swz = Q8 ? 0 : (c8 >> 2) & 1;
+    const int swz = (c8 >> 2) & 1;  // staggered chunk order: conflict-free 16-byte loads
     const int my_tok = tg * 4 + 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0);  // token of my reduced scores
+    const int qg = lane >> 2, t4 = lane & 3;
+    // INT8 score rows: MMA row qg is token 4 (qg / 2) + qg % 2 and row qg + 8 the token two
+    // after it, so that after the transpose of P a lane's PV k-slots (2 t4, 2 t4 + 1,
+    // 2 t4 + 8, 2 t4 + 9) are tokens 4 t4 .. 4 t4 + 3: one 32-bit word of a value row
+    const int kr0 = 4 * (qg >> 1) + (qg & 1), kr1 = kr0 + 2;
 
     // ---- item metadata moves through a pipeline so no dependent load sits on the critical
     //      path: queue index claimed 3 items ahead, record loaded 2 ahead, page ids and q 1
@@ -389,17 +422,31 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         }
         return phys;
     };
-    // raw q of the G query heads of an item, my q.k dims (staggered chunk order)
-    auto load_q = [&](const DecItem& it, uint4 (&qr)[G][NCH]) {
+    // raw q of an item: 16-bit pages -- the G query heads, my q.k dims (staggered chunk
+    // order); INT8 pages -- query head qg (zero for qg >= G), dims t4 * D/4 .. + D/4 - 1
+    auto load_q = [&](const DecItem& it, uint4 (&qr)[NQ]) {
         if (it.np == 0) return;
-        const uint16_t* qbase = static_cast<const uint16_t*>(a.q) +
-                                (static_cast<int64_t>(it.t) * Hq + it.g * G) * D + c8 * QKD;
+        if constexpr (Q8) {
+            if (qg < G) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const uint16_t*>(a.q) +
+                    (static_cast<int64_t>(it.t) * Hq + it.g * G + qg) * D + t4 * (D / 4));
 #pragma unroll
-        for (int j = 0; j < G; ++j)
+                for (int u = 0; u < NQ; ++u) qr[u] = __ldg(src + u);
+            } else {
 #pragma unroll
-            for (int ci = 0; ci < NCH; ++ci)
-                qr[j][ci] = __ldg(reinterpret_cast<const uint4*>(qbase + j * D) +
-                                  (ci ^ (NCH == 2 ? swz : 0)));
+                for (int u = 0; u < NQ; ++u) qr[u] = make_uint4(0, 0, 0, 0);
+            }
+        } else {
+            const uint16_t* qbase = static_cast<const uint16_t*>(a.q) +
+                                    (static_cast<int64_t>(it.t) * Hq + it.g * G) * D + c8 * QKD;
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int ci = 0; ci < NCH; ++ci)
+                    qr[j * NCH + ci] = __ldg(reinterpret_cast<const uint4*>(qbase + j * D) +
+                                             (ci ^ (NCH == 2 ? swz : 0)));
+        }
     };
     auto claim = [&]() {  // lane 0 holds the claimed index; read it with __shfl_sync later
         int idx = 0;
@@ -418,8 +465,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     int cur_win = load_window(cur, 0), cur_win_base = 0;
     int nxt_win = load_window(nxt, 0);
     // the next item's q is prefetched when the registers allow (not for 8 x 128-dim heads)
-    constexpr bool kPrefetchQ = G * NCH <= 8;
-    uint4 q_cur[G][NCH], q_nxt[kPrefetchQ ? G : 1][kPrefetchQ ? NCH : 1];
+    constexpr bool kPrefetchQ = NQ <= 8;
+    uint4 q_cur[NQ], q_nxt[kPrefetchQ ? NQ : 1];
     load_q(cur, q_cur);
     if constexpr (kPrefetchQ) load_q(nxt, q_nxt);
     int p2_idx = __shfl_sync(kFull, claim(), 0);
@@ -474,37 +521,182 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             *reinterpret_cast<uint32_t*>(out_row) = Cv::pack(res[0], res[1]);
         }
     };
-    while (cur.np > 0 && !aborted) {
+
+    // ---- INT8 pages: one item on the tensor cores.  q' = q * k_scale * scale * log2(e) is
+    //      scaled by a power of two f so its largest element lies in [2^13, 2^14) (inside fp16
+    //      range at full precision); scores come back times f and are scaled by 1/f exactly.
+    //      O^T = V^T P^T accumulates in o: m-tile i rows qg, qg + 8 are dims 16 i + qg and
+    //      16 i + 8 + qg, columns 2 t4, 2 t4 + 1 query heads.  Returns false on a timeout.
+    auto run_item_q8 = [&]() -> bool {
+        if constexpr (Q8) {
+            float qv[D / 4];
+            {
+                const float4* ks = reinterpret_cast<const float4*>(a.k_scale + cur.g * D +
+                                                                   t4 * (D / 4));
+#pragma unroll
+                for (int u = 0; u < NQ; ++u) {
+                    const uint32_t w4[4] = {q_cur[u].x, q_cur[u].y, q_cur[u].z, q_cur[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = Cv::unpack(w4[e]);
+                        const int d = u * 8 + 2 * e;
+                        const float4 k4 = __ldg(ks + d / 4);
+                        const float ka = (d & 2) ? k4.z : k4.x, kb = (d & 2) ? k4.w : k4.y;
+                        qv[d] = f.x * ka * a.scale_log2;
+                        qv[d + 1] = f.y * kb * a.scale_log2;
+                    }
+                }
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int d = 0; d < D / 4; ++d) amax = fmaxf(amax, fabsf(qv[d]));
+#pragma unroll
+            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            const int ex = min(100, max(-100, 13 - (static_cast<int>(__float_as_uint(amax) >> 23) - 127)));
+            const float fq = __uint_as_float(static_cast<uint32_t>(127 + ex) << 23);
+            const float inv_f = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);
+            uint32_t qb[KW][2];
+#pragma unroll
+            for (int kk = 0; kk < KW; ++kk) {
+                qb[kk][0] = pack_h2(qv[4 * kk] * fq, qv[4 * kk + 1] * fq);
+                qb[kk][1] = pack_h2(qv[4 * kk + 2] * fq, qv[4 * kk + 3] * fq);
+            }
+            float o[KW][4];
+#pragma unroll
+            for (int i = 0; i < KW; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            float m0 = -1e30f, m1 = -1e30f, l0 = 0.f, l1 = 0.f;  // heads 2 t4, 2 t4 + 1
+
+            for (int i = 0; i < cur.np; ++i) {
+                const int stage = consumed % kNst;
+                if (!mbar_wait_warp(&bars[stage], (consumed / kNst) & 1)) {
+                    if (lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                    return false;
+                }
+                ++consumed;
+                const uint8_t* sK = ring + stage * S::kStageBytes;   // [16 tokens][D] codes
+                const uint8_t* sV = sK + S::kPageBytes;               // [D][16 tokens] codes
+                const int nvalid = min(kPage, cur.nkv - (cur.pb + i) * kPage);
+                // key words of rows kr0, kr1 (D/4 bytes each; rows kr0 of lanes qg = 2p and
+                // 2p + 1 share banks, a 2-way conflict the shared-memory pipe absorbs)
+                uint32_t k0[KW], k1[KW];
+#pragma unroll
+                for (int h = 0; h < KW / 4; ++h) {
+                    const uint4 w0 = *reinterpret_cast<const uint4*>(sK + kr0 * D + t4 * (D / 4) +
+                                                                     16 * h);
+                    const uint4 w1 = *reinterpret_cast<const uint4*>(sK + kr1 * D + t4 * (D / 4) +
+                                                                     16 * h);
+                    k0[4 * h] = w0.x; k0[4 * h + 1] = w0.y; k0[4 * h + 2] = w0.z; k0[4 * h + 3] = w0.w;
+                    k1[4 * h] = w1.x; k1[4 * h + 1] = w1.y; k1[4 * h + 2] = w1.z; k1[4 * h + 3] = w1.w;
+                }
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < KW; ++kk) {
+                    const uint32_t x0 = k0[kk] ^ 0x80808080u, x1 = k1[kk] ^ 0x80808080u;
+                    mma_16816(sc, codes_lo_h2(x0), codes_lo_h2(x1), codes_hi_h2(x0),
+                              codes_hi_h2(x1), qb[kk][0], qb[kk][1]);
+                }
+                // sc: (token kr0: heads 2 t4, 2 t4 + 1), (token kr1: same heads)
+                const float s0 = kr0 < nvalid ? sc[0] * inv_f : -INFINITY;
+                const float s1 = kr0 < nvalid ? sc[1] * inv_f : -INFINITY;
+                const float s2 = kr1 < nvalid ? sc[2] * inv_f : -INFINITY;
+                const float s3 = kr1 < nvalid ? sc[3] * inv_f : -INFINITY;
+                float pm0 = fmaxf(s0, s2), pm1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int x = 4; x < 32; x <<= 1) {
+                    pm0 = fmaxf(pm0, __shfl_xor_sync(kFull, pm0, x));
+                    pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, x));
+                }
+                const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
+                const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+                const bool rescale = mn0 != m0 || mn1 != m1;
+                m0 = mn0;
+                m1 = mn1;
+                const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
+                const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+                l0 = fmaf(l0, al0, p0 + p2);
+                l1 = fmaf(l1, al1, p1 + p3);
+                // P^T fragments: k-slots (2 t4, 2 t4 + 1) and (2 t4 + 8, 2 t4 + 9), query head qg
+                const uint32_t pb0 = movmatrix_t(pack_h2(p0, p1));
+                const uint32_t pb1 = movmatrix_t(pack_h2(p2, p3));
+                if (rescale) {
+#pragma unroll
+                    for (int ii = 0; ii < KW; ++ii) {
+                        o[ii][0] *= al0; o[ii][1] *= al1; o[ii][2] *= al0; o[ii][3] *= al1;
+                    }
+                }
+#pragma unroll
+                for (int ii = 0; ii < KW; ++ii) {
+                    const int d0 = 16 * ii + qg;
+                    const uint32_t x0 = *reinterpret_cast<const uint32_t*>(sV + d0 * kPage + 4 * t4) ^ 0x80808080u;
+                    const uint32_t x1 = *reinterpret_cast<const uint32_t*>(sV + (d0 + 8) * kPage + 4 * t4) ^ 0x80808080u;
+                    mma_16816(o[ii], minus_1152_h2(codes_lo_h2(x0)), minus_1152_h2(codes_lo_h2(x1)),
+                              minus_1152_h2(codes_hi_h2(x0)), minus_1152_h2(codes_hi_h2(x1)), pb0,
+                              pb1);
+                }
+                __syncwarp();
+                issue_one();  // refill the stage just freed
+            }
+            // row sums over the 16 token rows of every page (lanes with equal t4)
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                l0 += __shfl_xor_sync(kFull, l0, x);
+                l1 += __shfl_xor_sync(kFull, l1, x);
+            }
+            const float* vs = a.v_scale + cur.g * D;
+            const int j0 = 2 * t4, j1 = 2 * t4 + 1;
+            const bool w0 = j0 < G, w1 = j1 < G;
+            if (cur.ns == 1) {
+                const float i0 = 1.f / l0, i1 = 1.f / l1;
+                uint16_t* out0 = static_cast<uint16_t*>(a.out) +
+                                 (static_cast<int64_t>(cur.t) * Hq + cur.g * G + j0) * D;
+#pragma unroll
+                for (int ii = 0; ii < KW; ++ii) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int d = 16 * ii + 8 * hr + qg;
+                        const float sv = __ldg(vs + d);
+                        const uint32_t pk = Cv::pack(o[ii][2 * hr] * sv * i0,
+                                                     o[ii][2 * hr + 1] * sv * i1);
+                        if (w0) out0[d] = static_cast<uint16_t>(pk & 0xffffu);
+                        if (w1) out0[D + d] = static_cast<uint16_t>(pk >> 16);
+                    }
+                }
+            } else {
+                const int64_t slot = static_cast<int64_t>(cur.base) + cur.s;
+                float* po = part_o + (slot * G + j0) * D;
+#pragma unroll
+                for (int ii = 0; ii < KW; ++ii) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int d = 16 * ii + 8 * hr + qg;
+                        const float sv = __ldg(vs + d);
+                        if (w0) po[d] = o[ii][2 * hr] * sv;
+                        if (w1) po[D + d] = o[ii][2 * hr + 1] * sv;
+                    }
+                }
+                if (qg == 0) {
+                    if (w0) part_ml[slot * G + j0] = make_float2(m0, l0);
+                    if (w1) part_ml[slot * G + j1] = make_float2(m1, l1);
+                }
+            }
+        }
+        return true;
+    };
+
+    // ---- 16-bit pages: one item on the FP32 pipes.  Returns false on a timeout.
+    auto run_item_16 = [&]() -> bool {
         // query heads g*G .. g*G+G-1, my q.k dims, pre-scaled into base-2 units
         // (even dim, odd dim) pairs: the packed fp32 FMA (FFMA2) works on both at once
         float2 qf[G][QKD / 2];
         const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
-        // INT8 pools: key channel d stands for code * k_scale[g][d], so the scale folds
-        // into q once per item and the inner loop works on the codes
-        float2 ksc[QKD / 2];
-#pragma unroll
-        for (int p = 0; p < QKD / 2; ++p) ksc[p] = make_float2(1.f, 1.f);
-        if constexpr (Q8) {
-            const float4* kp = reinterpret_cast<const float4*>(a.k_scale + cur.g * D + c8 * QKD);
-#pragma unroll
-            for (int p = 0; p < QKD / 4; ++p) {
-                const float4 f = __ldg(kp + p);
-                ksc[2 * p] = make_float2(f.x, f.y);
-                ksc[2 * p + 1] = make_float2(f.z, f.w);
-            }
-        }
 #pragma unroll
         for (int j = 0; j < G; ++j) {
 #pragma unroll
             for (int ci = 0; ci < NCH; ++ci) {
-                const uint32_t ws4[4] = {q_cur[j][ci].x, q_cur[j][ci].y, q_cur[j][ci].z,
-                                         q_cur[j][ci].w};
+                const uint4 qw = q_cur[j * NCH + ci];
+                const uint32_t ws4[4] = {qw.x, qw.y, qw.z, qw.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    qf[j][ci * 4 + e] = __fmul2_rn(Cv::unpack(ws4[e]), sl2);
-                    if constexpr (Q8)
-                        qf[j][ci * 4 + e] = __fmul2_rn(qf[j][ci * 4 + e], ksc[ci * 4 + e]);
-                }
+                for (int e = 0; e < 4; ++e) qf[j][ci * 4 + e] = __fmul2_rn(Cv::unpack(ws4[e]), sl2);
             }
         }
         float m[G], lsum[NV];
@@ -522,8 +714,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             const int stage = consumed % kNst;
             if (!mbar_wait_warp(&bars[stage], (consumed / kNst) & 1)) {
                 if (lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
-                aborted = true;
-                break;
+                return false;
             }
             ++consumed;
             const uint8_t* sK = ring + stage * S::kStageBytes;
@@ -536,41 +727,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 float2 acc[G];  // even-dim and odd-dim partial sums
 #pragma unroll
                 for (int j = 0; j < G; ++j) acc[j] = make_float2(0.f, 0.f);
-                if constexpr (Q8) {
-                    // QKD codes of the key row: word wi holds dims 4 wi .. 4 wi + 3
-                    const uint8_t* kb = sK + (tg * 4 + kk) * D + c8 * QKD;
-                    uint32_t kw[QKD / 4];
-                    if constexpr (QKD == 16) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(kb);
-                        kw[0] = w.x; kw[1] = w.y; kw[2] = w.z; kw[QKD / 4 - 1] = w.w;
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2*>(kb);
-                        kw[0] = w.x; kw[QKD / 4 - 1] = w.y;
-                    }
+                const uint4* krow =
+                    reinterpret_cast<const uint4*>(sK + (tg * 4 + kk) * D * 2) + c8 * NCH;
 #pragma unroll
-                    for (int wi = 0; wi < QKD / 4; ++wi) {
-                        float2 f01, f23;
-                        codes_to_float(kw[wi], f01, f23);
+                for (int ci = 0; ci < NCH; ++ci) {
+                    const uint4 w = krow[ci ^ (NCH == 2 ? swz : 0)];
+                    const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int j = 0; j < G; ++j) {
-                            acc[j] = __ffma2_rn(qf[j][2 * wi], f01, acc[j]);
-                            acc[j] = __ffma2_rn(qf[j][2 * wi + 1], f23, acc[j]);
-                        }
-                    }
-                } else {
-                    const uint4* krow =
-                        reinterpret_cast<const uint4*>(sK + (tg * 4 + kk) * D * 2) + c8 * NCH;
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = Cv::unpack(ws4[e]);
 #pragma unroll
-                    for (int ci = 0; ci < NCH; ++ci) {
-                        const uint4 w = krow[ci ^ (NCH == 2 ? swz : 0)];
-                        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = Cv::unpack(ws4[e]);
-#pragma unroll
-                            for (int j = 0; j < G; ++j)
-                                acc[j] = __ffma2_rn(qf[j][ci * 4 + e], f, acc[j]);
-                        }
+                        for (int j = 0; j < G; ++j) acc[j] = __ffma2_rn(qf[j][ci * 4 + e], f, acc[j]);
                     }
                 }
 #pragma unroll
@@ -656,18 +823,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             }
             auto pv_token = [&](int tok) {
                 float2 vf[DP2];
-                if constexpr (Q8) {  // codes; the value scale is applied once per item
-                    float2 f01, f23;
-                    if constexpr (DPL == 4) {
-                        codes_to_float(
-                            *reinterpret_cast<const uint32_t*>(sV + tok * D + lane * 4), f01, f23);
-                        vf[DP2 - 1] = f23;
-                    } else {
-                        codes_to_float(
-                            *reinterpret_cast<const uint16_t*>(sV + tok * D + lane * 2), f01, f23);
-                    }
-                    vf[0] = f01;
-                } else if constexpr (DPL == 4) {
+                if constexpr (DPL == 4) {
                     const uint2 w = *reinterpret_cast<const uint2*>(sV + tok * D * 2 + lane * 8);
                     vf[0] = Cv::unpack(w.x);
                     vf[DP2 - 1] = Cv::unpack(w.y);
@@ -691,7 +847,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             __syncwarp();
             issue_one();  // refill the stage just freed
         }
-        if (aborted) break;
 
         // ---- totals of this split: sum lsum over the token lanes, gather every head
         float lh[G];
@@ -709,21 +864,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 lh[i2] = b0 ? other : x;
                 lh[NV + i2] = b0 ? x : other;
             }
-        }
-        if constexpr (Q8) {  // value channel d stands for code * v_scale[g][d]
-            float2 vsc[DP2];
-            if constexpr (DPL == 4) {
-                const float4 f =
-                    __ldg(reinterpret_cast<const float4*>(a.v_scale + cur.g * D) + lane);
-                vsc[0] = make_float2(f.x, f.y);
-                vsc[DP2 - 1] = make_float2(f.z, f.w);
-            } else {
-                vsc[0] = __ldg(reinterpret_cast<const float2*>(a.v_scale + cur.g * D) + lane);
-            }
-#pragma unroll
-            for (int j = 0; j < G; ++j)
-#pragma unroll
-                for (int e = 0; e < DP2; ++e) o[j][e] = __fmul2_rn(o[j][e], vsc[e]);
         }
         if (cur.ns == 1) {
 #pragma unroll
@@ -749,6 +889,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 if (lane == 0) part_ml[slot * G + j] = make_float2(m[j], lh[j]);
             }
         }
+        return true;
+    };
+
+    while (cur.np > 0 && !aborted) {
+        bool ok;
+        if constexpr (Q8) ok = run_item_q8();
+        else ok = run_item_16();
+        if (!ok) {
+            aborted = true;
+            break;
+        }
 
         // ---- advance the metadata pipeline; `nxt`'s first pages are already in flight
         cur = nxt;
@@ -756,9 +907,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         cur_win_base = 0;
         if constexpr (kPrefetchQ) {
 #pragma unroll
-            for (int j = 0; j < G; ++j)
-#pragma unroll
-                for (int ci = 0; ci < NCH; ++ci) q_cur[j][ci] = q_nxt[j][ci];
+            for (int u = 0; u < NQ; ++u) q_cur[u] = q_nxt[u];
         } else {
             load_q(cur, q_cur);
         }

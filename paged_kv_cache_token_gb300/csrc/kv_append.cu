@@ -75,8 +75,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
 // INT8 pools (wmrh.cn/news/64708 §4.3: the KV cache in INT8 halves its memory and
 // bandwidth; §5.4: calibrated per channel).  Same placement as kv_append_kernel; each value
 // x of channel (h, d) is stored as clamp(rint(x / s[h][d]), -127, 127), the quotient in IEEE
-// fp32 and rint rounding to nearest even.  One warp per (token, KV head); lane l quantises
-// channels l*DPL .. l*DPL+DPL-1 of K and of V and stores them as one packed word.
+// fp32 and rint rounding to nearest even.  A K page block is [16 slots][D] like the 16-bit
+// pools; a V page block is stored [D][16 slots] (each dim's 16 tokens contiguous), the
+// order in which the attention step's tensor-core fragments read values.  One warp per
+// (token, KV head); lane l quantises channels l*DPL .. l*DPL+DPL-1 of K and of V.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendArgs a) {
     constexpr int DPL = D / 32;  // channels per lane: 4 or 2
@@ -122,29 +124,43 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendArgs a) {
         if (h == 0 && lane == 0 && a.slot_mapping)
             a.slot_mapping[t] = static_cast<int64_t>(page) * kPage + slot;
         const int64_t src = (static_cast<int64_t>(t) * a.num_kv_heads + h) * D + lane * DPL;
-        const int64_t dst =
-            ((static_cast<int64_t>(page) * a.num_kv_heads + h) * kPage + slot) * D + lane * DPL;
+        const int64_t block = (static_cast<int64_t>(page) * a.num_kv_heads + h) * kPage * D;
         const int chan = h * D + lane * DPL;
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-            const uint16_t* sp = static_cast<const uint16_t*>(kv ? a.v_new : a.k_new) + src;
-            const float* sc = (kv ? a.v_scale : a.k_scale) + chan;
-            uint8_t* dp = static_cast<uint8_t*>(kv ? a.v_cache : a.k_cache) + dst;
+        uint32_t kq[DPL], vq[DPL];
+        {
+            const uint16_t* ks = static_cast<const uint16_t*>(a.k_new) + src;
+            const uint16_t* vs = static_cast<const uint16_t*>(a.v_new) + src;
+            const float* ksc = a.k_scale + chan;
+            const float* vsc = a.v_scale + chan;
             if constexpr (DPL == 4) {
-                const uint2 xw = __ldg(reinterpret_cast<const uint2*>(sp));
-                const float4 s4 = __ldg(reinterpret_cast<const float4*>(sc));
-                const float2 x01 = Cv::unpack(xw.x), x23 = Cv::unpack(xw.y);
-                *reinterpret_cast<uint32_t*>(dp) =
-                    quant(x01.x, s4.x) | (quant(x01.y, s4.y) << 8) |
-                    (quant(x23.x, s4.z) << 16) | (quant(x23.y, s4.w) << 24);
+                const uint2 kw = __ldg(reinterpret_cast<const uint2*>(ks));
+                const uint2 vw = __ldg(reinterpret_cast<const uint2*>(vs));
+                const float4 k4 = __ldg(reinterpret_cast<const float4*>(ksc));
+                const float4 v4 = __ldg(reinterpret_cast<const float4*>(vsc));
+                const float2 k01 = Cv::unpack(kw.x), k23 = Cv::unpack(kw.y);
+                const float2 v01 = Cv::unpack(vw.x), v23 = Cv::unpack(vw.y);
+                kq[0] = quant(k01.x, k4.x); kq[1] = quant(k01.y, k4.y);
+                kq[2] = quant(k23.x, k4.z); kq[DPL - 1] = quant(k23.y, k4.w);
+                vq[0] = quant(v01.x, v4.x); vq[1] = quant(v01.y, v4.y);
+                vq[2] = quant(v23.x, v4.z); vq[DPL - 1] = quant(v23.y, v4.w);
             } else {
-                const uint32_t xw = __ldg(reinterpret_cast<const uint32_t*>(sp));
-                const float2 s2 = __ldg(reinterpret_cast<const float2*>(sc));
-                const float2 x01 = Cv::unpack(xw);
-                *reinterpret_cast<uint16_t*>(dp) =
-                    static_cast<uint16_t>(quant(x01.x, s2.x) | (quant(x01.y, s2.y) << 8));
+                const float2 k01 = Cv::unpack(__ldg(reinterpret_cast<const uint32_t*>(ks)));
+                const float2 v01 = Cv::unpack(__ldg(reinterpret_cast<const uint32_t*>(vs)));
+                const float2 k2 = __ldg(reinterpret_cast<const float2*>(ksc));
+                const float2 v2 = __ldg(reinterpret_cast<const float2*>(vsc));
+                kq[0] = quant(k01.x, k2.x); kq[DPL - 1] = quant(k01.y, k2.y);
+                vq[0] = quant(v01.x, v2.x); vq[DPL - 1] = quant(v01.y, v2.y);
             }
         }
+        uint8_t* kd = static_cast<uint8_t*>(a.k_cache) + block + slot * D + lane * DPL;
+        uint32_t kword = 0;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) kword |= kq[e] << (8 * e);
+        if constexpr (DPL == 4) *reinterpret_cast<uint32_t*>(kd) = kword;
+        else *reinterpret_cast<uint16_t*>(kd) = static_cast<uint16_t>(kword);
+        uint8_t* vd = static_cast<uint8_t*>(a.v_cache) + block + slot;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) vd[(lane * DPL + e) * kPage] = static_cast<uint8_t>(vq[e]);
     }
 }
 

@@ -60,7 +60,9 @@ class PagedKV:
         shape = (num_pages, num_kv_heads, 16, head_dim)
         pool_dtype = torch.int8 if self.kv_int8 else self.dtype
         self.k_cache = torch.empty(shape, dtype=pool_dtype, device=self.device)
-        self.v_cache = torch.empty(shape, dtype=pool_dtype, device=self.device)
+        # INT8 value pages are dim-major: [num_pages, Hkv, D, 16]
+        vshape = (num_pages, num_kv_heads, head_dim, 16) if self.kv_int8 else shape
+        self.v_cache = torch.empty(vshape, dtype=pool_dtype, device=self.device)
         if self.kv_int8:
             as_dev = lambda x: torch.as_tensor(np.asarray(x, np.float32)).reshape(
                 num_kv_heads, head_dim).to(self.device).contiguous()

@@ -50,7 +50,8 @@ def run_all_int8(w, check_rows=None):
 
 
 def expected_pools(w, kv_steps):
-    """Pools the oracle writes: its codes (as bytes in uint16 cells) placed by its append."""
+    """Pools the oracle writes: its codes (as bytes in uint16 cells) placed by its append,
+    the value pool in the library's dim-major page order."""
     shape = (w.num_pages, w.num_kv_heads, 16, w.head_dim)
     kp = np.full(shape, 0x80, np.uint16)   # INT8 sentinel -128 as a byte
     vp = kp.copy()
@@ -65,7 +66,8 @@ def expected_pools(w, kv_steps):
                                       w.num_pages, as_u16(kc), as_u16(vc), kp, vp)
         slots.append(sl)
     to_i8 = lambda p: p.astype(np.uint8).view(np.int8)
-    return to_i8(kp), to_i8(vp), slots
+    # value pages are stored dim-major ([page][head][dim][slot])
+    return to_i8(kp), np.ascontiguousarray(np.swapaxes(to_i8(vp), 2, 3)), slots
 
 
 # ------------------------------------------------------------------------------ kv_append
