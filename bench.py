@@ -139,6 +139,7 @@ class ClockSampler:
 # reported only while the sources still match, else null.
 KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "common.cuh", "launch.h"],
+    "decode_kernel_int8": ["decode.cu", "common.cuh", "launch.h"],
     "prefill_pair_kernel": ["prefill_pair.cu", "tc.cuh", "common.cuh", "launch.h"],
 }
 
@@ -603,7 +604,8 @@ def main():
                 "roofline": {"bound": "hbm", "kernel": "decode_kernel (INT8 pages)",
                              "achieved": q8["kernel_GBps"], "peak": hbm, "unit": "GB/s",
                              "frac": q8["kernel_GBps"] / hbm,
-                             "peak_source": peak_src + " hbm_gbs", "traffic": None}}
+                             "peak_source": peak_src + " hbm_gbs",
+                             "traffic": captured_traffic("decode_kernel_int8")}}
         if not args.no_cpu_baseline and dist_ctx.rank == 0:
             secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
             line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores,

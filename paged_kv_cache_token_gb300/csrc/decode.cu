@@ -275,11 +275,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
 // ------------------------------------------------------------------------------------
 // decode: independent warps pull items; see the file comment for the data flow.
 // ------------------------------------------------------------------------------------
-// Q8: the pools hold INT8 codes (half the bytes per page, so twice the ring stages keep the
-// same bytes in flight; the scores need no shared-memory staging).
+// Q8: the pools hold INT8 codes (half the bytes per page; the scores need no shared-memory
+// staging).  Four stages of half-size pages let three CTAs share an SM: more warps to hide
+// the latency of the per-page dependency chain, with as many bytes in flight as before.
 template <typename T, int D, int G, bool Q8>
 struct DecodeSmem {
-    static constexpr int kNst = Q8 ? 2 * kStages : kStages;
+    static constexpr int kNst = Q8 ? 4 : kStages;
     static constexpr int kPageBytes = kPage * D * (Q8 ? 1 : 2);  // one K (or V) page block
     static constexpr int kStageBytes = 2 * kPageBytes;
     static constexpr int kRing = kDecWarps * kNst * kStageBytes;
@@ -302,7 +303,8 @@ __device__ __forceinline__ uint32_t codes_hi_h2(uint32_t x) {  // bytes 2, 3 -> 
     return __byte_perm(x, 0x6464u, 0x4342);
 }
 __device__ __forceinline__ uint32_t minus_1152_h2(uint32_t h) {
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__float2half(1152.f)));
+    const __half2 c = __half2half2(__float2half(1152.f));
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), c);
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -317,6 +319,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// 2^x in one MUFU operation (results below 2^-126 flush to zero: softmax weights that small
+// vanish against the row's maximum weight of 1)
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 // transpose of an 8x8 16-bit matrix held one row-pair register per thread
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -552,7 +561,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             for (int d = 0; d < D / 4; ++d) amax = fmaxf(amax, fabsf(qv[d]));
 #pragma unroll
             for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-            const int ex = min(100, max(-100, 13 - (static_cast<int>(__float_as_uint(amax) >> 23) - 127)));
+            const int e_amax = static_cast<int>(__float_as_uint(amax) >> 23) - 127;
+            const int ex = min(100, max(-100, 13 - e_amax));
             const float fq = __uint_as_float(static_cast<uint32_t>(127 + ex) << 23);
             const float inv_f = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);
             uint32_t qb[KW][2];
@@ -585,16 +595,21 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                                                                      16 * h);
                     const uint4 w1 = *reinterpret_cast<const uint4*>(sK + kr1 * D + t4 * (D / 4) +
                                                                      16 * h);
-                    k0[4 * h] = w0.x; k0[4 * h + 1] = w0.y; k0[4 * h + 2] = w0.z; k0[4 * h + 3] = w0.w;
-                    k1[4 * h] = w1.x; k1[4 * h + 1] = w1.y; k1[4 * h + 2] = w1.z; k1[4 * h + 3] = w1.w;
+                    k0[4 * h] = w0.x; k0[4 * h + 1] = w0.y;
+                    k0[4 * h + 2] = w0.z; k0[4 * h + 3] = w0.w;
+                    k1[4 * h] = w1.x; k1[4 * h + 1] = w1.y;
+                    k1[4 * h + 2] = w1.z; k1[4 * h + 3] = w1.w;
                 }
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                // two accumulators (even and odd k-steps) halve the dependent MMA chain
+                float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int kk = 0; kk < KW; ++kk) {
                     const uint32_t x0 = k0[kk] ^ 0x80808080u, x1 = k1[kk] ^ 0x80808080u;
-                    mma_16816(sc, codes_lo_h2(x0), codes_lo_h2(x1), codes_hi_h2(x0),
-                              codes_hi_h2(x1), qb[kk][0], qb[kk][1]);
+                    mma_16816((kk & 1) ? sd : sc, codes_lo_h2(x0), codes_lo_h2(x1),
+                              codes_hi_h2(x0), codes_hi_h2(x1), qb[kk][0], qb[kk][1]);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[e] += sd[e];
                 // sc: (token kr0: heads 2 t4, 2 t4 + 1), (token kr1: same heads)
                 const float s0 = kr0 < nvalid ? sc[0] * inv_f : -INFINITY;
                 const float s1 = kr0 < nvalid ? sc[1] * inv_f : -INFINITY;
@@ -607,18 +622,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                     pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, x));
                 }
                 const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
-                const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+                const float al0 = ex2_ftz(m0 - mn0), al1 = ex2_ftz(m1 - mn1);
                 const bool rescale = mn0 != m0 || mn1 != m1;
                 m0 = mn0;
                 m1 = mn1;
-                const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-                const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+                const float p0 = ex2_ftz(s0 - mn0), p1 = ex2_ftz(s1 - mn1);
+                const float p2 = ex2_ftz(s2 - mn0), p3 = ex2_ftz(s3 - mn1);
                 l0 = fmaf(l0, al0, p0 + p2);
                 l1 = fmaf(l1, al1, p1 + p3);
                 // P^T fragments: k-slots (2 t4, 2 t4 + 1) and (2 t4 + 8, 2 t4 + 9), query head qg
                 const uint32_t pb0 = movmatrix_t(pack_h2(p0, p1));
                 const uint32_t pb1 = movmatrix_t(pack_h2(p2, p3));
-                if (rescale) {
+                if (__any_sync(kFull, rescale)) {  // warp-uniform: no divergent paths
 #pragma unroll
                     for (int ii = 0; ii < KW; ++ii) {
                         o[ii][0] *= al0; o[ii][1] *= al1; o[ii][2] *= al0; o[ii][3] *= al1;
@@ -627,11 +642,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 #pragma unroll
                 for (int ii = 0; ii < KW; ++ii) {
                     const int d0 = 16 * ii + qg;
-                    const uint32_t x0 = *reinterpret_cast<const uint32_t*>(sV + d0 * kPage + 4 * t4) ^ 0x80808080u;
-                    const uint32_t x1 = *reinterpret_cast<const uint32_t*>(sV + (d0 + 8) * kPage + 4 * t4) ^ 0x80808080u;
-                    mma_16816(o[ii], minus_1152_h2(codes_lo_h2(x0)), minus_1152_h2(codes_lo_h2(x1)),
-                              minus_1152_h2(codes_hi_h2(x0)), minus_1152_h2(codes_hi_h2(x1)), pb0,
-                              pb1);
+                    const uint32_t* vrow = reinterpret_cast<const uint32_t*>(sV + d0 * kPage) + t4;
+                    const uint32_t x0 = vrow[0] ^ 0x80808080u;           // dim d0
+                    const uint32_t x1 = vrow[2 * kPage] ^ 0x80808080u;   // dim d0 + 8
+                    mma_16816(o[ii], minus_1152_h2(codes_lo_h2(x0)),
+                              minus_1152_h2(codes_lo_h2(x1)), minus_1152_h2(codes_hi_h2(x0)),
+                              minus_1152_h2(codes_hi_h2(x1)), pb0, pb1);
                 }
                 __syncwarp();
                 issue_one();  // refill the stage just freed
