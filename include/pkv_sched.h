@@ -72,6 +72,19 @@ PKV_API int pkv_sched_add_request(pkv_scheduler* s, int32_t rid, int32_t history
                                   int32_t prompt, int32_t decodes);
 
 /*
+ * pkv_sched_sort_by_length -- order the requests whose prompt has not started by prompt
+ * length, shortest first (equal lengths keep their arrival order), after every request
+ * that has started (those keep their order).  lshu.cn/news/11576 §2.2: sorting the batch by
+ * prompt length before prefill keeps requests of similar length adjacent, so their pages
+ * are allocated together rather than short requests' pages landing in the gaps between
+ * long ones; later steps plan and launch requests in the new order.  The length is the
+ * prompt tokens still to compute (less any reused prefix); a request has started once a
+ * step has computed some of its prompt (a history load or a reused prefix does not count).
+ * Errors: INVALID_ARG (NULL handle), CAPACITY (out of memory; the order is unchanged).
+ */
+PKV_API int pkv_sched_sort_by_length(pkv_scheduler* s);
+
+/*
  * pkv_sched_history_plan -- the append that loads every request's cached history
  * (q_len = history, context_len = 0), pages taken request by request, or round-robin one
  * page at a time across requests when `interleave` is non-zero.  Marks the history

@@ -44,6 +44,7 @@ struct Req {
     int64_t total = 0;       // every position the request will ever hold
     int64_t computed = 0;    // tokens already in the KV cache
     bool history_pending = false;
+    bool begun = false;      // a step has computed some of its prompt
     std::vector<int32_t> pages;
     bool decoding() const { return computed >= prompt_end && computed < total; }
     bool prefilling() const { return computed < prompt_end; }
@@ -217,6 +218,7 @@ struct pkv_scheduler {
                 r.history_pending = false;
             } else {
                 r.computed += p.n;
+                r.begun = true;
             }
             if (r.cached && r.registered != INT64_MAX) register_blocks(r);
         }
@@ -261,6 +263,29 @@ int pkv_sched_add_request(pkv_scheduler* s, int32_t rid, int32_t history, int32_
             s->reqs.pop_back();
             throw;
         }
+        return PKV_OK;
+    } catch (...) {
+        return PKV_ERR_CAPACITY;
+    }
+}
+
+int pkv_sched_sort_by_length(pkv_scheduler* s) {
+    if (!s) return PKV_ERR_INVALID_ARG;
+    try {
+        // key: prompt tokens still to compute; equal keys keep their arrival order
+        std::vector<size_t> started, waiting;
+        for (size_t i = 0; i < s->reqs.size(); ++i)
+            (s->reqs[i].begun ? started : waiting).push_back(i);
+        std::stable_sort(waiting.begin(), waiting.end(), [s](size_t a, size_t b) {
+            return s->reqs[a].prompt_end - s->reqs[a].computed <
+                   s->reqs[b].prompt_end - s->reqs[b].computed;
+        });
+        std::vector<Req> order;
+        order.reserve(s->reqs.size());
+        for (size_t i : started) order.push_back(std::move(s->reqs[i]));
+        for (size_t i : waiting) order.push_back(std::move(s->reqs[i]));
+        s->reqs.swap(order);
+        s->reindex();
         return PKV_OK;
     } catch (...) {
         return PKV_ERR_CAPACITY;

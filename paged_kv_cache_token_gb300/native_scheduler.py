@@ -51,6 +51,8 @@ def _lib():
         lib.pkv_sched_add_prompt.argtypes = [V, ctypes.c_int32, V, ctypes.c_int32,
                                              ctypes.c_int32]
         lib.pkv_sched_add_prompt.restype = ctypes.c_int
+        lib.pkv_sched_sort_by_length.argtypes = [V]
+        lib.pkv_sched_sort_by_length.restype = ctypes.c_int
         for fn in (lib.pkv_sched_cached_blocks, lib.pkv_sched_evictable_blocks):
             fn.argtypes = [V]
             fn.restype = ctypes.c_int32
@@ -98,6 +100,13 @@ class NativeScheduler:
         self.max_reqs += 1
         self.max_pages = max(self.max_pages, -(-(len(t) + decodes) // 16))
         return rc
+
+    def sort_by_length(self) -> None:
+        """Order the requests whose prompt has not started by the prompt tokens still to
+        compute, shortest first, after the started ones (lshu.cn/news/11576 §2.2)."""
+        rc = self._lib.pkv_sched_sort_by_length(self._h)
+        if rc != binding.OK:
+            raise binding.PkvError("pkv_sched_sort_by_length", rc)
 
     @property
     def cached_blocks(self) -> int:

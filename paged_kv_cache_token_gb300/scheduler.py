@@ -58,6 +58,7 @@ class ReqState:
     total: int           # every position this request will ever hold
     computed: int        # tokens already in the KV cache
     pages: List[int]
+    begun: bool = False  # a step has computed some of its prompt
 
     @property
     def decoding(self) -> bool:
@@ -131,6 +132,25 @@ class Scheduler:
         self._history = [r.history for r in requests]
         self._interleave = interleave_history
 
+    def add_request(self, r) -> None:
+        """Append a request (``rid``, ``history``, ``prompt``, ``decodes``) to the batch."""
+        self.reqs.append(ReqState(r.rid, r.history + r.prompt, r.history + r.prompt + r.decodes,
+                                  0, []))
+        self._history.append(r.history)
+
+    def sort_by_length(self) -> None:
+        """Order the requests whose prompt has not started by the prompt tokens still to
+        compute, shortest first (ties keep arrival order), after every request that has
+        started.  lshu.cn/news/11576 §2.2: sorting a batch by prompt length before prefill
+        keeps requests of similar length adjacent, so their pages are allocated together
+        instead of short requests' pages landing in the gaps between long ones."""
+        started = [i for i, st in enumerate(self.reqs) if st.begun]
+        waiting = [i for i, st in enumerate(self.reqs) if not st.begun]
+        waiting.sort(key=lambda i: self.reqs[i].prompt_end - self.reqs[i].computed)
+        order = started + waiting
+        self.reqs = [self.reqs[i] for i in order]
+        self._history = [self._history[i] for i in order]
+
     def _grow(self, st: ReqState, upto_tokens: int) -> None:
         while len(st.pages) < pages_for(upto_tokens):
             st.pages.append(self.pool.allocate())
@@ -139,7 +159,7 @@ class Scheduler:
         """The append that loads every request's cached history (q_len = history,
         context_len = 0).  Pages are taken per request, or round-robin one page at a time
         across requests when ``interleave_history`` is set.  Marks the history computed."""
-        idx = [i for i, h in enumerate(self._history) if h > 0]
+        idx = [i for i, h in enumerate(self._history) if h > 0 and self.reqs[i].computed == 0]
         if not idx:
             return None
         if self._interleave:
@@ -181,6 +201,7 @@ class Scheduler:
                          [st.computed for st, _ in chosen], [list(st.pages) for st, _ in chosen])
         for st, n in chosen:
             st.computed += n
+            st.begun = True
         return plan
 
     def all_steps(self) -> List[StepPlan]:

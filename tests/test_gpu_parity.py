@@ -365,3 +365,20 @@ def test_config_mixed_chunked_matches_oracle_and_one_shot():
     diff = (chunked.float() - o1[0].float()).abs().max().item()
     print("mixed: gpu chunked-vs-one-shot max diff", diff)
     assert diff <= 2 * 2e-2
+
+
+def test_sorted_native_plans_match_oracle():
+    # steps planned by the native planner after sorting the batch by prompt length
+    # (lshu.cn/news/11576 §2.2): launch order and page placement change, the rows do not
+    from paged_kv_cache_token_gb300.native_scheduler import native_scheduler_for
+    w = custom(520, 8, 2, 128, 0, [(0, n, 2) for n in (300, 20, 150, 5, 64, 17)], budget=128)
+    s = native_scheduler_for(w)
+    s.sort_by_length()
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    steps = s.all_steps()
+    assert list(steps[0].rids[:3]) == [3, 5, 1]
+    for i, plan in enumerate(steps):
+        out = runner.run_step(kv, w, plan)
+        assert_close(gpu_as_f64(out), oracle_rows(w, plan), "sorted step %d" % i)
+    assert kv.read_error() == 0

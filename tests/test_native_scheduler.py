@@ -113,3 +113,86 @@ def test_small_output_arrays_change_nothing():
     assert e.value.status == -3 and nat.num_free == 20
     nat.max_reqs = real_max
     same_run(py, nat)
+
+
+# ---------------------------------------------------------------- sort by prompt length
+def _pair(reqs, pages, budget, cap=None):
+    order = np.arange(pages, dtype=np.int32)
+    return (Scheduler(reqs, PagePool(order), budget, cap),
+            NativeScheduler(reqs, order, budget, cap))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_sort_by_length_identical_plans_mid_run(seed):
+    # sort a batch, run a few steps, add requests, sort again (started requests keep their
+    # place at the front), then run to the end: the native and Python planners agree
+    g = np.random.default_rng(100 + seed)
+    mk = lambda i: W.RequestSpec(i, int(g.integers(0, 100)), int(g.integers(0, 400)),
+                                 int(g.integers(0, 6)))
+    first = [mk(i) for i in range(int(g.integers(2, 9)))]
+    later = [mk(i) for i in range(len(first), len(first) + int(g.integers(1, 6)))]
+    pages = sum(-(-r.total // 16) for r in first + later) + 4
+    budget = int(g.integers(16, 300))
+    py, nat = _pair(first, pages, budget, 64 if seed % 2 else None)
+    py.sort_by_length()
+    nat.sort_by_length()
+    same_plan(py.history_plan(), nat.history_plan())
+    for _ in range(int(g.integers(1, 4))):
+        same_plan(py.next_step(), nat.next_step())
+    for r in later:
+        py.add_request(r)
+        nat.add_request(r.rid, r.history, r.prompt, r.decodes)
+    py.sort_by_length()
+    nat.sort_by_length()
+    same_plan(py.history_plan(), nat.history_plan())
+    while True:
+        p, n = py.next_step(), nat.next_step()
+        same_plan(p, n)
+        if p is None:
+            break
+
+
+def test_sort_by_length_order():
+    # prompts 300, 20, 300, 5, 20: shortest first, equal lengths in arrival order
+    reqs = [W.RequestSpec(i, 0, n, 1) for i, n in enumerate([300, 20, 300, 5, 20])]
+    py, nat = _pair(reqs, 200, 4096)
+    py.sort_by_length()
+    nat.sort_by_length()
+    p, n = py.next_step(), nat.next_step()
+    same_plan(p, n)
+    assert list(n.rids) == [3, 1, 4, 0, 2]
+    # a reused prefix counts as not started; its key is the prompt left to compute
+    s = NativeScheduler([], np.arange(64, dtype=np.int32), 4096)
+    a = np.arange(100, dtype=np.int32)
+    s.add_prompt(0, a, 0)
+    s.next_step()
+    s.add_prompt(1, np.arange(40, dtype=np.int32) + 1000, 0)   # 40 new tokens
+    assert s.add_prompt(2, a, 0) == 96                          # 4 tokens left
+    s.sort_by_length()
+    assert list(s.next_step().rids) == [2, 1]
+
+
+def test_sort_by_length_keeps_pages_together():
+    # lshu.cn/news/11576 §2.2: with prompts of mixed lengths, prefilling in arrival order
+    # leaves short requests' pages between long ones; sorted, each request's pages form
+    # fewer separate runs of the pool, and every short prompt prefills in the first step
+    lens = [1800, 32, 2048, 2048, 1800, 48, 1500, 48, 32, 64, 32, 48, 2048, 2048, 32, 1800]
+    reqs = [W.RequestSpec(i, 0, n, 2) for i, n in enumerate(lens)]
+    runs = lambda pages: 1 + sum(1 for a, b in zip(pages, pages[1:]) if b != a + 1)
+    total = {}
+    for srt in (False, True):
+        s = NativeScheduler(reqs, np.arange(4000, dtype=np.int32), 512)
+        if srt:
+            s.sort_by_length()
+        steps = s.all_steps()
+        first = {r: i for i, p in reversed(list(enumerate(steps))) for r in p.rids}
+        last = steps[-1]
+        tables = {}
+        for p in steps:
+            for j, r in enumerate(p.rids):
+                row = p.block_table[j]
+                tables[r] = [int(x) for x in row[row >= 0]]
+        total[srt] = sum(runs(t) for t in tables.values())
+        if srt:
+            assert all(first[i] == 0 for i, n in enumerate(lens) if n <= 64)
+    assert total[True] < total[False]
