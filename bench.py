@@ -312,14 +312,15 @@ def time_decode_int8(device, steps, pool_pages=70000):
     return res
 
 
-def time_prefill(device, reps=3):
-    """Attention-kernel time of the 8K one-shot prefill and of the 4 x 2048 chunks."""
+def time_prefill(device, reps=3, kv_int8=False):
+    """Attention-kernel time of the 8K one-shot prefill and of the 4 x 2048 chunks (over
+    INT8 pages with ``kv_int8``)."""
     from paged_kv_cache_token_gb300 import binding, runner
     res = {}
     for label, chunk in (("one_shot_8192", None), ("chunks_4x2048", 2048)):
         w = W.prefill(chunk=chunk)
         s = scheduler_for(w)
-        kv = runner.paged_kv_for(w, device=device, fill_sentinel=False)
+        kv = runner.paged_kv_for(w, device=device, fill_sentinel=False, kv_int8=kv_int8)
         plans = s.all_steps()
         flops = sum(causal_flops(w, p) for p in plans)
         total_ms = 0.0
@@ -505,7 +506,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-loop", action="store_true")
     ap.add_argument("--no-int8", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode-loop", "int8"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode-loop", "int8", "int8-prefill"],
+                    default=None,
                     help="time only the prefill workload (one-shot 8K and 4 x 2K) and print "
                          "its JSON object; used for focused profiler captures")
     ap.add_argument("--pool-pages", type=int, default=70000,
@@ -533,6 +535,11 @@ def main():
             if dist_ctx.rank == 0:
                 print(json.dumps({"int8_kv": time_decode_int8(device, args.steps,
                                                               args.pool_pages)}))
+            return
+        if args.only == "int8-prefill":
+            if dist_ctx.rank == 0:
+                print(json.dumps({"int8_prefill": time_prefill(device, kv_int8=True),
+                                  "peak_tflops": bf16}))
             return
         if args.only == "decode-loop":
             if dist_ctx.rank == 0:
@@ -606,6 +613,20 @@ def main():
                              "frac": q8["kernel_GBps"] / hbm,
                              "peak_source": peak_src + " hbm_gbs",
                              "traffic": captured_traffic("decode_kernel_int8")}}
+            if not args.no_prefill:
+                pq = time_prefill(device, kv_int8=True)
+                one, ch = pq["one_shot_8192"], pq["chunks_4x2048"]
+                kt = one["flops"] / one["main_kernel_ms"] / 1e9
+                line["int8_kv"]["prefill"] = {
+                    "workload": "the 8192-token causal prefill over INT8 pages, one shot and "
+                                "4 x 2048 chunks (prefill_q8_kernel)",
+                    "one_shot_tflops": one["tflops"], "chunked_tflops": ch["tflops"],
+                    "one_shot_ms": one["ms"], "kernel_ms": one["main_kernel_ms"],
+                    "roofline": {"bound": "tensor", "kernel": "prefill_q8_kernel",
+                                 "achieved": kt, "peak": bf16, "unit": "TFLOP/s",
+                                 "frac": kt / bf16,
+                                 "peak_source": peak_src + " bf16_tflops (burst; fp16 has "
+                                                           "the same nominal dense rate)"}}
         if not args.no_cpu_baseline and dist_ctx.rank == 0:
             secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
             line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores,

@@ -63,12 +63,19 @@ int prefill_min_q() { return 16; }
 
 thread_local cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
 
-// INT8 pools: every row runs on the streaming path (the tensor-core prefill reads 16-bit
-// operands), so no request counts as a prefill.
+// Requests with at least this many new tokens take the tensor-core prefill path.  INT8
+// pools have that path for two query heads per tile only (an even KV group); otherwise
+// every row runs on the streaming kernel.
+int prefill_min_q_for(const pkv_step_desc* d, bool int8) {
+    if (int8 && pkv::prefill_heads_per_tile(d->num_q_heads, d->num_kv_heads) != 2)
+        return INT_MAX;
+    return prefill_min_q();
+}
+
 pkv::WorkspaceLayout layout_for(const pkv_step_desc* d, int num_sms, bool int8 = false) {
     return pkv::workspace_layout(d->num_reqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
                                  d->total_q_tokens, d->max_q_len, d->max_context_len, num_sms,
-                                 int8 ? INT_MAX : prefill_min_q());
+                                 prefill_min_q_for(d, int8));
 }
 
 int kv_append_impl(const pkv_step_desc* desc, const void* k_new, const void* v_new,
@@ -217,7 +224,7 @@ int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache
     a.scale_log2 = scale * 1.4426950408889634f;
     a.ws = static_cast<uint8_t*>(workspace);
     a.lay = lay;
-    a.prefill_min_q = int8 ? INT_MAX : prefill_min_q();
+    a.prefill_min_q = prefill_min_q_for(desc, int8);
     a.heads_per_tile = pkv::prefill_heads_per_tile(desc->num_q_heads, desc->num_kv_heads);
     a.err = dev_err_flag;
     a.kv_int8 = int8 ? 1 : 0;

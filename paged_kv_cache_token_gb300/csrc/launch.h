@@ -102,8 +102,12 @@ int launch_prefill(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                    cudaEvent_t ev_stop);
 int launch_prefill_pair(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                         cudaEvent_t ev_stop);
+// INT8 pools, two query heads of an even KV group per tile (the only INT8 tile shape)
+int launch_prefill_q8(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
+                      cudaEvent_t ev_stop);
 // Q ([T][Hq][D], 128-row boxes) and K/V pool (16-row page boxes) tensor maps, 128-byte
 // swizzle, 64-element-wide boxes.
 bool make_prefill_maps(const StepArgs& a, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv);
+bool make_q_map(const StepArgs& a, CUtensorMap* mq);
 
 }  // namespace pkv

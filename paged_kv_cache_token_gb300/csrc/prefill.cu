@@ -422,24 +422,30 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_prefill_maps(const StepArgs& a, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+bool make_q_map(const StepArgs& a, CUtensorMap* mq) {
     auto enc = encode_fn();
     if (!enc) return false;
     const CUtensorMapDataType dt =
         a.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint64_t D = static_cast<cuuint64_t>(a.head_dim);
     // Q: [T][Hq][D] as a 3-D tensor, box 64 x 1 x 128 rows
-    {
-        cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(a.num_q_heads),
-                              static_cast<cuuint64_t>(a.total_q_tokens)};
-        cuuint64_t strides[2] = {D * 2, D * 2 * a.num_q_heads};
-        cuuint32_t box[3] = {64, 1, kBM};
-        cuuint32_t es[3] = {1, 1, 1};
-        if (enc(mq, dt, 3, const_cast<void*>(a.q), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return false;
-    }
+    cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(a.num_q_heads),
+                          static_cast<cuuint64_t>(a.total_q_tokens)};
+    cuuint64_t strides[2] = {D * 2, D * 2 * a.num_q_heads};
+    cuuint32_t box[3] = {64, 1, kBM};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(mq, dt, 3, const_cast<void*>(a.q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+bool make_prefill_maps(const StepArgs& a, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+    auto enc = encode_fn();
+    if (!enc || !make_q_map(a, mq)) return false;
+    const CUtensorMapDataType dt =
+        a.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t D = static_cast<cuuint64_t>(a.head_dim);
     // K, V pools: [num_pages * Hkv * 16 rows][D], box 64 x 16 rows (one page of one head)
     const cuuint64_t rows = static_cast<cuuint64_t>(a.num_pages) * a.num_kv_heads * kPage;
     cuuint64_t dims[2] = {D, rows};
@@ -483,6 +489,7 @@ int launch_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t
 }  // namespace
 
 int launch_prefill(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
+    if (a.kv_int8) return launch_prefill_q8(a, stream, e0, e1);
     if (a.heads_per_tile == 2) return launch_prefill_pair(a, stream, e0, e1);
     if (a.dtype == PKV_BF16)
         return a.head_dim == 128 ? launch_t<__nv_bfloat16, 128>(a, stream, e0, e1)

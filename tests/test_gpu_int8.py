@@ -158,11 +158,43 @@ def test_int8_decode_batches(hq, hkv, d, dtype):
     run_all_int8(custom(800 + hq + d, hq, hkv, d, dtype, [(c, 0, 2) for c in ctx]))
 
 
-@pytest.mark.parametrize("hq,hkv,d,dtype", [(4, 2, 64, 0), (32, 8, 128, 0), (8, 2, 128, 1)])
-def test_int8_prefill_chunks_stream_path(hq, hkv, d, dtype):
-    # chunks of up to 96 rows over histories: every row goes through the streaming kernel
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(4, 2, 64, 0), (32, 8, 128, 0), (8, 2, 128, 1),
+                                            (16, 2, 64, 1), (8, 8, 64, 0), (4, 4, 128, 1)])
+def test_int8_prefill_chunks(hq, hkv, d, dtype):
+    # chunks of up to 96 rows over histories, around the 128-row tile and 16-token page
+    # edges: an even KV group takes the tensor-core prefill over INT8 pages; with one query
+    # head per KV head every row streams
     specs = [(0, 1, 1), (0, 127, 1), (0, 129, 2), (0, 300, 1), (20, 33, 0), (500, 64, 1)]
     run_all_int8(custom(900 + hq + d, hq, hkv, d, dtype, specs, budget=160, chunk_cap=96))
+
+
+def test_int8_prefill_tiles_cross_pages_and_tiles():
+    # one-shot prompts of 1..300 tokens over histories of 0..1000: ragged last pages and
+    # tiles, diagonal tiles at every offset, pages past the end of a tile zero-filled
+    specs = [(0, 16, 0), (0, 17, 0), (15, 113, 0), (1000, 300, 0), (130, 255, 1), (7, 129, 0)]
+    run_all_int8(custom(960, 8, 2, 128, 0, specs))
+
+
+def test_int8_prefill_scale_extremes():
+    # Q' = Q * k_scale is rescaled by a power of two into fp16 range: queries of 1e-5 and
+    # of 3e4 (far outside fp16 once multiplied out) give the oracle's rows
+    for mag in (1e-5, 3e4):
+        w = custom(970 + int(mag > 1), 4, 2, 64, 0, [(40, 200, 0)])
+        q = w.q(0)
+        x = (torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).float() * mag)
+        w._cache[("q", 0)] = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        run_all_int8(w)
+
+
+def test_int8_prefill_8k_one_shot_sampled():
+    """The 8,192-token one-shot prefill (32/8 heads, d=128, bf16) over INT8 pages: sampled
+    rows (every tile's first and last, ragged spots) against the oracle."""
+    w = W.prefill()
+    rng = np.random.default_rng(3)
+    rows = lambda p: sorted(set(rng.choice(p.total_q_tokens, 40, replace=False).tolist()) |
+                            {0, 127, 128, 4095, 8191})
+    worst, _, _ = run_all_int8(w, check_rows=rows)
+    print("int8 prefill 8k worst", worst)
 
 
 def test_int8_long_rows():
