@@ -303,8 +303,9 @@ __device__ __forceinline__ uint32_t codes_hi_h2(uint32_t x) {  // bytes 2, 3 -> 
     return __byte_perm(x, 0x6464u, 0x4342);
 }
 __device__ __forceinline__ uint32_t minus_1152_h2(uint32_t h) {
-    const __half2 c = __half2half2(__float2half(1152.f));
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), c);
+    const uint32_t c = 0x64806480u;   // fp16 1152 in both halves
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
+                              *reinterpret_cast<const __half2*>(&c));
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {

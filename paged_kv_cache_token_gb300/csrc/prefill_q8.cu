@@ -63,21 +63,29 @@ struct Q8Smem {
     static_assert(kLaunchBytes <= 227 * 1024, "shared memory budget");
 };
 
-// 16 INT8 codes (one 16-byte word) -> 16 exact fp16 values in two 16-byte words.  With the
-// sign bit flipped, code c = u - 128 for the byte u, and 0x64 over u is the fp16 1024 + u.
+// 16 INT8 codes (one 16-byte word) -> 16 fp16 values in two 16-byte words.  With the sign
+// bit flipped, code c = u - 128 for the byte u, and 0x64 over u is the fp16 1024 + u, i.e.
+// c + 1152; Exact subtracts the 1152 (exactly).  Without it every score of a query row
+// would carry the same 1152 * sum_d Q'_d, which the softmax cancels, but the kernel with
+// exact keys measured faster (its producer loop compiles to less code), so both K and V
+// use exact codes.
+template <bool Exact>
 __device__ __forceinline__ uint32_t q8_pair(uint32_t x, uint32_t sel) {
     const uint32_t h = __byte_perm(x, 0x6464u, sel);
+    if constexpr (!Exact) return h;
+    const uint32_t c = 0x64806480u;   // fp16 1152 in both halves
     const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
-                              __half2half2(__float2half(1152.f)));
+                              *reinterpret_cast<const __half2*>(&c));
     return *reinterpret_cast<const uint32_t*>(&r);
 }
+template <bool Exact>
 __device__ __forceinline__ void q8_codes16(const uint4 w, uint4& lo, uint4& hi) {
     const uint32_t x0 = w.x ^ 0x80808080u, x1 = w.y ^ 0x80808080u;
     const uint32_t x2 = w.z ^ 0x80808080u, x3 = w.w ^ 0x80808080u;
-    lo = make_uint4(q8_pair(x0, 0x4140), q8_pair(x0, 0x4342), q8_pair(x1, 0x4140),
-                    q8_pair(x1, 0x4342));
-    hi = make_uint4(q8_pair(x2, 0x4140), q8_pair(x2, 0x4342), q8_pair(x3, 0x4140),
-                    q8_pair(x3, 0x4342));
+    lo = make_uint4(q8_pair<Exact>(x0, 0x4140), q8_pair<Exact>(x0, 0x4342),
+                    q8_pair<Exact>(x1, 0x4140), q8_pair<Exact>(x1, 0x4342));
+    hi = make_uint4(q8_pair<Exact>(x2, 0x4140), q8_pair<Exact>(x2, 0x4342),
+                    q8_pair<Exact>(x3, 0x4140), q8_pair<Exact>(x3, 0x4342));
 }
 
 // byte offset of the 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled region
@@ -199,63 +207,63 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
             }
             return __shfl_sync(kFull, win, lp & 31);
         };
-        // K page p of the tile: rows 16 p .. 16 p + 15 of the key tile.  Lane: key l % 16,
-        // dims (l / 16) * D/2 .. + D/2 - 1 (eight lanes of a store phase hit eight rows,
-        // so the swizzled chunks never share banks).
-        auto write_k = [&](uint8_t* dst, int p, const uint8_t* src) {
-            constexpr int W = D / 32;          // 16-byte code words per lane
-            const int key = lane & 15, d0 = (lane >> 4) * (D / 2);
-            const int row = p * kPage + key;
-            uint4 w[W];
-#pragma unroll
-            for (int u = 0; u < W; ++u)
-                w[u] = src ? __ldg(reinterpret_cast<const uint4*>(src + key * D + d0) + u)
-                           : make_uint4(0x80808080u, 0x80808080u, 0x80808080u, 0x80808080u);
-#pragma unroll
-            for (int u = 0; u < W; ++u) {
-                uint4 lo, hi;
-                q8_codes16(w[u], lo, hi);
-                if (!src) lo = hi = make_uint4(0, 0, 0, 0);
-                const int d = d0 + 16 * u;     // first dim of this word
-                uint8_t* half = dst + (d / 64) * S::kHalfBytes;
-                const int ch = (d % 64) / 8;
-                *reinterpret_cast<uint4*>(half + sw128(row, ch)) = lo;
-                *reinterpret_cast<uint4*>(half + sw128(row, ch + 1)) = hi;
-            }
-        };
-        // V page p: keys 16 p .. 16 p + 15 = 32 bytes of every V^T row (dim), in the key
-        // half p / 4.  Lane: dims l, l + 32, ... (one 16-byte word of codes each).
-        auto write_v = [&](uint8_t* dst, int p, const uint8_t* src) {
-            uint8_t* half = dst + (p / 4) * S::kVHalf;
-            const int ch = (p % 4) * 2;
-#pragma unroll
-            for (int u = 0; u < D / 32; ++u) {
-                const int d = lane + 32 * u;
-                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                if (src) q8_codes16(__ldg(reinterpret_cast<const uint4*>(src + d * kPage)), lo, hi);
-                *reinterpret_cast<uint4*>(half + sw128(d, ch)) = lo;
-                *reinterpret_cast<uint4*>(half + sw128(d, ch + 1)) = hi;
-            }
-        };
+        // A producer owns pages pi, pi + 3, pi + 6 of every tile.  All their code words are
+        // loaded first, before the wait for the stage slot, so the loads' latency is paid
+        // once per tile and overlaps that wait.  K page: lane = (key l % 16, dims
+        // (l / 16) * D/2 .. + D/2 - 1); eight lanes of a store phase hit eight rows, so the
+        // swizzled chunks never share banks.  V page (dim-major): lane = dims l, l + 32, ...;
+        // one word = the dim's 16 keys.  (One loop for both roles: separately compiled K
+        // and V loops measured slower.)
+        constexpr int PPW = (kBN / kPage + kProducers - 1) / kProducers;  // pages per warp
+        constexpr int W = D / 32;          // 16-byte code words per lane per page
+        const int lane_off = is_v ? lane * kPage : (lane & 15) * D + (lane >> 4) * (D / 2);
+        const int lane_step = is_v ? 32 * kPage : 16;
         bool ok = true;
         for (int j = 0; ok && j < n_kv; ++j) {
+            const int p0 = j * (kBN / kPage);
+            const int np = min(kBN / kPage, npages_seq - p0);
+            uint4 w[PPW][W];
+#pragma unroll
+            for (int t = 0; t < PPW; ++t) {
+                const int p = pi + kProducers * t;
+                if (p < np) {
+                    const int phys = page_of(p0 + p);
+                    const int64_t block = static_cast<int64_t>(phys) * a.num_kv_heads + g;
+                    const uint8_t* src = pool + lane_off + block * (kPage * D);
+#pragma unroll
+                    for (int u = 0; u < W; ++u)
+                        w[t][u] = __ldg(reinterpret_cast<const uint4*>(src + u * lane_step));
+                }
+            }
             const int nst = is_v ? kStagesV : kStagesK;
             uint64_t* full = is_v ? &v_full[j % kStagesV] : &k_full[j % kStagesK];
             uint64_t* empty = is_v ? &v_empty[j % kStagesV] : &k_empty[j % kStagesK];
             if (j >= nst && lane == 0 && !mbar_wait(empty, ((j / nst) - 1) & 1)) ok = false;
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            const int p0 = j * (kBN / kPage);
-            const int np = min(kBN / kPage, npages_seq - p0);
             uint8_t* dst = is_v ? sV(j) : sK(j);
-            for (int p = pi; p < kBN / kPage; p += kProducers) {
-                const uint8_t* src = nullptr;
-                if (p < np) {
-                    const int phys = page_of(p0 + p);
-                    src = pool + (static_cast<int64_t>(phys) * a.num_kv_heads + g) * (kPage * D);
+#pragma unroll
+            for (int t = 0; t < PPW; ++t) {
+                const int p = pi + kProducers * t;
+                if (p >= kBN / kPage) continue;
+#pragma unroll
+                for (int u = 0; u < W; ++u) {
+                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;   // zeros: a page past the end
+                    if (p < np) q8_codes16<true>(w[t][u], lo, hi);
+                    if (is_v) {
+                        uint8_t* half = dst + (p / 4) * S::kVHalf;
+                        const int d = lane + 32 * u, ch = (p % 4) * 2;
+                        *reinterpret_cast<uint4*>(half + sw128(d, ch)) = lo;
+                        *reinterpret_cast<uint4*>(half + sw128(d, ch + 1)) = hi;
+                    } else {
+                        const int row = p * kPage + (lane & 15);
+                        const int d = (lane >> 4) * (D / 2) + 16 * u;   // first dim of the word
+                        uint8_t* half = dst + (d / 64) * S::kHalfBytes;
+                        const int ch = (d % 64) / 8;
+                        *reinterpret_cast<uint4*>(half + sw128(row, ch)) = lo;
+                        *reinterpret_cast<uint4*>(half + sw128(row, ch + 1)) = hi;
+                    }
                 }
-                if (is_v) write_v(dst, p, src);
-                else write_k(dst, p, src);
             }
             tc::fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's reads
             __syncwarp();
@@ -414,7 +422,8 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
             auto chunk_max = [&](const uint32_t (&sr)[32], int cb) {
                 if (!diag) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[e]));
+                    for (int e = 0; e < 32; ++e)
+                        mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[e]));
                 } else {
                     const int rem = lim - cb * 32;  // valid keys in this chunk
 #pragma unroll
@@ -514,8 +523,8 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const float4 s0 = __ldg(reinterpret_cast<const float4*>(vs + cb * 32 + u * 8));
-                        const float4 s1 = __ldg(reinterpret_cast<const float4*>(vs + cb * 32 + u * 8) + 1);
+                        const float4* vp = reinterpret_cast<const float4*>(vs + cb * 32 + u * 8);
+                        const float4 s0 = __ldg(vp), s1 = __ldg(vp + 1);
                         const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
                         uint32_t w[4];
 #pragma unroll
