@@ -140,6 +140,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "common.cuh", "launch.h"],
     "decode_kernel_int8": ["decode.cu", "common.cuh", "launch.h"],
+    "prefill_q8_kernel": ["prefill_q8.cu", "tc.cuh", "common.cuh", "launch.h"],
     "prefill_pair_kernel": ["prefill_pair.cu", "tc.cuh", "common.cuh", "launch.h"],
 }
 
@@ -626,7 +627,8 @@ def main():
                                  "achieved": kt, "peak": bf16, "unit": "TFLOP/s",
                                  "frac": kt / bf16,
                                  "peak_source": peak_src + " bf16_tflops (burst; fp16 has "
-                                                           "the same nominal dense rate)"}}
+                                                           "the same nominal dense rate)",
+                                 "traffic": captured_traffic("prefill_q8_kernel")}}
         if not args.no_cpu_baseline and dist_ctx.rank == 0:
             secs, nbytes, cores, passes = oracle_decode_sample(64, min_seconds=10.0)
             line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores,
