@@ -72,6 +72,45 @@ def test_host_validation_rejects_before_launch(lib, kw, code):
     assert lib.pkv_attention_workspace_bytes(ctypes.byref(d)) == 0
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), -2),
+    (dict(num_q_heads=32, num_kv_heads=2), -2),
+    (dict(num_pages=0), -1),
+    (dict(max_q_len=100, total_q_tokens=100), -3),
+])
+def test_int8_host_validation_rejects_before_launch(lib, kw, code):
+    d = _desc(**kw)
+    s = ctypes.c_void_p(0x2000)
+    rc = lib.pkv_kv_append_int8(ctypes.byref(d), None, None, s, s, None, None, None, None, None)
+    assert rc == code
+    rc = lib.pkv_paged_attention_step_int8(ctypes.byref(d), None, None, None, s, s, None, 1.0,
+                                           None, 0, None, None)
+    assert rc == code
+    assert lib.pkv_attention_workspace_bytes_int8(ctypes.byref(d)) == 0
+
+
+def test_int8_scales_required_and_aligned(lib):
+    # every tensor 16-byte aligned (never dereferenced: the checks fail first)
+    d = _desc()
+    t = ctypes.c_void_p(0x1000)
+    good, odd = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x2004)
+    for ks, vs in ((None, good), (good, None), (odd, good), (good, odd)):
+        assert lib.pkv_kv_append_int8(ctypes.byref(d), t, t, ks, vs, t, t, None, None,
+                                      None) == -1
+        assert lib.pkv_paged_attention_step_int8(ctypes.byref(d), t, t, t, ks, vs, t, 1.0, t,
+                                                 1 << 30, None, None) == -1
+
+
+def test_int8_empty_step_is_a_no_op(lib):
+    d = _desc(num_reqs=0, total_q_tokens=0, max_q_len=0, max_context_len=0, q_lens=None,
+              q_offsets=None, context_lens=None, block_table=None)
+    s = ctypes.c_void_p(0x2000)
+    assert lib.pkv_kv_append_int8(ctypes.byref(d), None, None, s, s, None, None, None, None,
+                                  None) == 0
+    assert lib.pkv_paged_attention_step_int8(ctypes.byref(d), None, None, None, s, s, None, 1.0,
+                                             None, 0, None, None) == 0
+
+
 def test_null_tensors_rejected(lib):
     d = _desc()
     assert lib.pkv_kv_append(ctypes.byref(d), None, None, None, None, None, None, None) == -1
