@@ -11,15 +11,18 @@
 // row i of such a request attends keys 0..ctx+i.  Work item = (decode row, KV head, split),
 // a split being an even share of the row's pages.  Every warp is an independent worker:
 // it takes items from a device queue, streams each page's K block and V block (16 x D
-// each, contiguous in the pool) through a private 3-stage shared-memory ring with 1-D bulk
-// async copies, and starts the next item's first pages while finishing the current one so
-// the copy pipeline never drains.  Scores stay in base-2 units (q is pre-scaled by
-// scale * log2 e); an online softmax keeps (running max, running sum, un-normalised output)
-// per query head.  A row with one split is normalised and written directly; otherwise each
+// each, contiguous in the pool) through a private shared-memory ring with 1-D bulk async
+// copies, and starts the next item's first pages while finishing the current one so the
+// copy pipeline never drains.  A page's scores for the item's G query heads are one set of
+// mma.sync tensor-core contractions (16 tokens x 8 head columns); an online softmax in base-2
+// units keeps (running max, running sum, un-normalised output) per query head; the weighted
+// sum over the page's values runs on the FP32 pipes for 16-bit pages (FFMA2 over V rows)
+// and on the tensor cores for INT8 pages.  A row with one split is normalised and written directly; otherwise each
 // split leaves its partial (m, l, O) in a fixed slot and the combine kernel reduces them:
 // m* = max m_s, l* = sum l_s 2^(m_s - m*), O = sum O_s 2^(m_s - m*) / l*.
 #include <algorithm>
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -328,6 +331,20 @@ __device__ __forceinline__ float ex2_ftz(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// the same for 16-bit T operands (bf16 or fp16), exact products, fp32 accumulation
+template <typename T>
+__device__ __forceinline__ void mma_16816_t(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+    if constexpr (std::is_same<T, __half>::value) {
+        mma_16816(d, a0, a1, a2, a3, b0, b1);
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
 // transpose of an 8x8 16-bit matrix held one row-pair register per thread
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     uint32_t y;
@@ -347,17 +364,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     using S = DecodeSmem<T, D, G, Q8>;
     constexpr int kNst = S::kNst;   // ring stages per warp
     using Cv = F16<T>;
-    constexpr int QKD = D / 8;      // dims per lane in q.k (16 or 8)
-    constexpr int NCH = QKD / 8;    // 16-byte chunks per lane per key row (2 or 1)
-    constexpr int DPL = D / 32;     // dims per lane in p.V (4 or 2)
+    constexpr int DPL = D / 32;     // dims per lane in the 16-bit p.V (4 or 2)
     constexpr int DP2 = DPL / 2;    // ... as float2 pairs
-    constexpr int N0 = 4 * G, N1 = N0 / 2, N2 = N1 / 2 > 0 ? N1 / 2 : 1;
-    constexpr int NV = (N2 >= 2) ? N2 / 2 : 1;  // score values a lane holds after reduction
-    // INT8: lane (qg, t4) = (lane / 4, lane % 4) in the MMA fragment layouts.  In the score
-    // MMA (S^T = K q'^T: rows = tokens, k = dims, n = query heads) the lane's k-slots of step
-    // kk are dims t4 * D/4 + 4 kk .. + 3, so its key bytes are D/4 contiguous ones per row.
-    constexpr int KW = D / 16;      // MMA k-steps over the dims = key words per row per lane
-    constexpr int NQ = Q8 ? D / 32 : G * NCH;  // 16-byte q chunks a lane holds
+    // Lane (qg, t4) = (lane / 4, lane % 4) in the MMA fragment layouts.  The score MMA is
+    // S^T = K q^T (rows = tokens, k = dims, n = query heads, padded to 8).  A lane's k-slots
+    // of step kk are 4 dims: INT8 pages -- t4 * D/4 + 4 kk .. + 3, so its key bytes are D/4
+    // contiguous ones per row; 16-bit pages -- chunk kk / 2 of 8 dims at t4 * 8 + 32 (kk / 2),
+    // so one 16-byte load per row serves two k-steps and the four lanes of a row group read
+    // four different bank groups.
+    constexpr int KW = D / 16;      // MMA k-steps over the dims
+    constexpr int NQ = D / 32;      // 16-byte q chunks a lane holds
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,14 +400,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     // K/V pages are read once per step: evict them first so the split partials written
     // meanwhile stay in L2 for the combine
     const uint64_t kv_policy = l2_policy_evict_first();
-    const int c8 = lane & 7, tg = lane >> 3;
-    const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
-    const int swz = (c8 >> 2) & 1;  // staggered chunk order: conflict-free 16-byte loads
-    const int my_tok = tg * 4 + 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0);  // token of my reduced scores
     const int qg = lane >> 2, t4 = lane & 3;
-    // INT8 score rows: MMA row qg is token 4 (qg / 2) + qg % 2 and row qg + 8 the token two
-    // after it, so that after the transpose of P a lane's PV k-slots (2 t4, 2 t4 + 1,
-    // 2 t4 + 8, 2 t4 + 9) are tokens 4 t4 .. 4 t4 + 3: one 32-bit word of a value row
+    // Score rows: MMA row qg is token 4 (qg / 2) + qg % 2 and row qg + 8 the token two after
+    // it.  INT8 pages need this order: after the transpose of P a lane's PV k-slots (2 t4,
+    // 2 t4 + 1, 2 t4 + 8, 2 t4 + 9) are tokens 4 t4 .. 4 t4 + 3, one 32-bit word of a value
+    // row.  16-bit pages share it (any order serves their pbuf hand-off).
     const int kr0 = 4 * (qg >> 1) + (qg & 1), kr1 = kr0 + 2;
 
     // ---- item metadata moves through a pipeline so no dependent load sits on the critical
@@ -432,30 +445,20 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         }
         return phys;
     };
-    // raw q of an item: 16-bit pages -- the G query heads, my q.k dims (staggered chunk
-    // order); INT8 pages -- query head qg (zero for qg >= G), dims t4 * D/4 .. + D/4 - 1
+    // raw q of an item: query head qg (zero for qg >= G).  INT8 pages: dims t4 * D/4 ..
+    // + D/4 - 1; 16-bit pages: chunks of 8 dims t4 * 8 + 32 m (m = 0 .. D/32 - 1)
     auto load_q = [&](const DecItem& it, uint4 (&qr)[NQ]) {
         if (it.np == 0) return;
-        if constexpr (Q8) {
-            if (qg < G) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    static_cast<const uint16_t*>(a.q) +
-                    (static_cast<int64_t>(it.t) * Hq + it.g * G + qg) * D + t4 * (D / 4));
+        if (qg < G) {
+            const uint16_t* qh = static_cast<const uint16_t*>(a.q) +
+                                 (static_cast<int64_t>(it.t) * Hq + it.g * G + qg) * D;
 #pragma unroll
-                for (int u = 0; u < NQ; ++u) qr[u] = __ldg(src + u);
-            } else {
-#pragma unroll
-                for (int u = 0; u < NQ; ++u) qr[u] = make_uint4(0, 0, 0, 0);
-            }
+            for (int u = 0; u < NQ; ++u)
+                qr[u] = __ldg(reinterpret_cast<const uint4*>(qh + (Q8 ? t4 * (D / 4) + 8 * u
+                                                                      : t4 * 8 + 32 * u)));
         } else {
-            const uint16_t* qbase = static_cast<const uint16_t*>(a.q) +
-                                    (static_cast<int64_t>(it.t) * Hq + it.g * G) * D + c8 * QKD;
 #pragma unroll
-            for (int j = 0; j < G; ++j)
-#pragma unroll
-                for (int ci = 0; ci < NCH; ++ci)
-                    qr[j * NCH + ci] = __ldg(reinterpret_cast<const uint4*>(qbase + j * D) +
-                                             (ci ^ (NCH == 2 ? swz : 0)));
+            for (int u = 0; u < NQ; ++u) qr[u] = make_uint4(0, 0, 0, 0);
         }
     };
     auto claim = [&]() {  // lane 0 holds the claimed index; read it with __shfl_sync later
@@ -700,23 +703,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         return true;
     };
 
-    // ---- 16-bit pages: one item on the FP32 pipes.  Returns false on a timeout.
+    // ---- 16-bit pages: scores on the tensor cores (S^T = K q^T as in the INT8 path, exact
+    //      16-bit products), weighted sums on the FP32 pipes (FFMA2 over V rows, with the
+    //      weights shared through pbuf).  Returns false on a timeout.
     auto run_item_16 = [&]() -> bool {
-        // query heads g*G .. g*G+G-1, my q.k dims, pre-scaled into base-2 units
-        // (even dim, odd dim) pairs: the packed fp32 FMA (FFMA2) works on both at once
-        float2 qf[G][QKD / 2];
-        const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+        uint32_t qb[KW][2];
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-#pragma unroll
-            for (int ci = 0; ci < NCH; ++ci) {
-                const uint4 qw = q_cur[j * NCH + ci];
-                const uint32_t ws4[4] = {qw.x, qw.y, qw.z, qw.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) qf[j][ci * 4 + e] = __fmul2_rn(Cv::unpack(ws4[e]), sl2);
-            }
+        for (int kk = 0; kk < KW; ++kk) {
+            const uint4 w = q_cur[kk >> 1];
+            qb[kk][0] = (kk & 1) ? w.z : w.x;
+            qb[kk][1] = (kk & 1) ? w.w : w.y;
         }
-        float m[G], lsum[NV];
+        float m[G];              // running max per query head (same in every lane)
+        float ma = -1e30f, mb = -1e30f, la = 0.f, lb = 0.f;  // my heads 2 t4, 2 t4 + 1
         float2 o[G][DP2];  // dims (2e, 2e+1) of my DPL output dims, per head
 #pragma unroll
         for (int j = 0; j < G; ++j) {
@@ -724,9 +723,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 #pragma unroll
             for (int e = 0; e < DP2; ++e) o[j][e] = make_float2(0.f, 0.f);
         }
-#pragma unroll
-        for (int i = 0; i < NV; ++i) lsum[i] = 0.f;
-
+        const int ja = 2 * t4, jb = 2 * t4 + 1;
         for (int i = 0; i < cur.np; ++i) {
             const int stage = consumed % kNst;
             if (!mbar_wait_warp(&bars[stage], (consumed / kNst) & 1)) {
@@ -737,95 +734,53 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             const uint8_t* sK = ring + stage * S::kStageBytes;
             const uint8_t* sV = sK + S::kPageBytes;
             const int nvalid = min(kPage, cur.nkv - (cur.pb + i) * kPage);
-            // ---- scores: lane (tg, c8) does tokens tg*4..tg*4+3 over dims c8*QKD..+QKD
-            float v[N0];
+            // ---- scores: rows kr0, kr1, chunk m of 8 dims = k-steps 2m, 2m + 1
+            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                float2 acc[G];  // even-dim and odd-dim partial sums
-#pragma unroll
-                for (int j = 0; j < G; ++j) acc[j] = make_float2(0.f, 0.f);
-                const uint4* krow =
-                    reinterpret_cast<const uint4*>(sK + (tg * 4 + kk) * D * 2) + c8 * NCH;
-#pragma unroll
-                for (int ci = 0; ci < NCH; ++ci) {
-                    const uint4 w = krow[ci ^ (NCH == 2 ? swz : 0)];
-                    const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = Cv::unpack(ws4[e]);
-#pragma unroll
-                        for (int j = 0; j < G; ++j) acc[j] = __ffma2_rn(qf[j][ci * 4 + e], f, acc[j]);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < G; ++j) v[kk * G + j] = acc[j].x + acc[j].y;
+            for (int mm = 0; mm < NQ; ++mm) {
+                const int col = (t4 * 8 + 32 * mm) * 2;   // byte offset of the chunk in a row
+                const uint4 w0 = *reinterpret_cast<const uint4*>(sK + kr0 * D * 2 + col);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(sK + kr1 * D * 2 + col);
+                mma_16816_t<T>(sc, w0.x, w1.x, w0.y, w1.y, qb[2 * mm][0], qb[2 * mm][1]);
+                mma_16816_t<T>(sd, w0.z, w1.z, w0.w, w1.w, qb[2 * mm + 1][0], qb[2 * mm + 1][1]);
             }
-            // ---- reduce over the 8 lanes of a token group by recursive halving
+            const float sl = a.scale_log2;
+            const float s0 = kr0 < nvalid ? (sc[0] + sd[0]) * sl : -INFINITY;
+            const float s1 = kr0 < nvalid ? (sc[1] + sd[1]) * sl : -INFINITY;
+            const float s2 = kr1 < nvalid ? (sc[2] + sd[2]) * sl : -INFINITY;
+            const float s3 = kr1 < nvalid ? (sc[3] + sd[3]) * sl : -INFINITY;
+            float pa = fmaxf(s0, s2), pb = fmaxf(s1, s3);
 #pragma unroll
-            for (int i2 = 0; i2 < N1; ++i2) {
-                const float send = b2 ? v[i2] : v[i2 + N1];
-                const float keep = b2 ? v[i2 + N1] : v[i2];
-                v[i2] = keep + __shfl_xor_sync(kFull, send, 4);
+            for (int x = 4; x < 32; x <<= 1) {
+                pa = fmaxf(pa, __shfl_xor_sync(kFull, pa, x));
+                pb = fmaxf(pb, __shfl_xor_sync(kFull, pb, x));
             }
-            if constexpr (N1 >= 2) {
-#pragma unroll
-                for (int i2 = 0; i2 < N2; ++i2) {
-                    const float send = b1 ? v[i2] : v[i2 + N2];
-                    const float keep = b1 ? v[i2 + N2] : v[i2];
-                    v[i2] = keep + __shfl_xor_sync(kFull, send, 2);
-                }
-            }
-            if constexpr (N2 >= 2) {
-#pragma unroll
-                for (int i2 = 0; i2 < NV; ++i2) {
-                    const float send = b0 ? v[i2] : v[i2 + NV];
-                    const float keep = b0 ? v[i2 + NV] : v[i2];
-                    v[i2] = keep + __shfl_xor_sync(kFull, send, 1);
-                }
-            } else {
-                v[0] += __shfl_xor_sync(kFull, v[0], 1);
-            }
-            // now v[i] = score of token my_tok for head (G>=2 ? b0*NV + i : 0)
-            const bool valid = my_tok < nvalid;
-            float s[NV], pmx[NV];
-#pragma unroll
-            for (int i2 = 0; i2 < NV; ++i2) {
-                s[i2] = valid ? v[i2] : -INFINITY;
-                float x = s[i2];
-                x = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
-                x = fmaxf(x, __shfl_xor_sync(kFull, x, 4));
-                x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
-                x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
-                pmx[i2] = x;
-            }
-            float pm[G];
-            if constexpr (G == 1) {
-                pm[0] = pmx[0];
-            } else {
-#pragma unroll
-                for (int i2 = 0; i2 < NV; ++i2) {
-                    const float other = __shfl_xor_sync(kFull, pmx[i2], 1);
-                    pm[i2] = b0 ? other : pmx[i2];
-                    pm[NV + i2] = b0 ? pmx[i2] : other;
-                }
-            }
+            // every head's page max in every lane (heads 2u, 2u + 1 live in lanes t4 = u)
             float alpha[G];
             bool rescale = false;
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                const float mn = fmaxf(m[j], pm[j]);
+                const float pj = __shfl_sync(kFull, (j & 1) ? pb : pa, j >> 1);
+                const float mn = fmaxf(m[j], pj);
                 alpha[j] = fast_exp2(m[j] - mn);
                 rescale |= mn != m[j];
                 m[j] = mn;
             }
-#pragma unroll
-            for (int i2 = 0; i2 < NV; ++i2) {
-                const float mh = (G == 1) ? m[0] : (b0 ? m[NV + i2] : m[i2]);
-                const float ah = (G == 1) ? alpha[0] : (b0 ? alpha[NV + i2] : alpha[i2]);
-                const float p = fast_exp2(s[i2] - mh);
-                lsum[i2] = fmaf(lsum[i2], ah, p);
-                if (G > 1 || !b0)
-                    pbuf[my_tok * G + ((G == 1) ? 0 : (b0 ? NV : 0) + i2)] = make_float2(p, p);
+            const float mna = fmaxf(ma, pa), mnb = fmaxf(mb, pb);
+            const float ala = fast_exp2(ma - mna), alb = fast_exp2(mb - mnb);
+            ma = mna;
+            mb = mnb;
+            const float p0 = fast_exp2(s0 - mna), p1 = fast_exp2(s1 - mnb);
+            const float p2 = fast_exp2(s2 - mna), p3 = fast_exp2(s3 - mnb);
+            la = fmaf(la, ala, p0 + p2);
+            lb = fmaf(lb, alb, p1 + p3);
+            if (ja < G) {
+                pbuf[kr0 * G + ja] = make_float2(p0, p0);
+                pbuf[kr1 * G + ja] = make_float2(p2, p2);
+            }
+            if (jb < G) {
+                pbuf[kr0 * G + jb] = make_float2(p1, p1);
+                pbuf[kr1 * G + jb] = make_float2(p3, p3);
             }
             __syncwarp();
 
@@ -845,7 +800,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                     vf[0] = Cv::unpack(w.x);
                     vf[DP2 - 1] = Cv::unpack(w.y);
                 } else {
-                    vf[0] = Cv::unpack(*reinterpret_cast<const uint32_t*>(sV + tok * D * 2 + lane * 4));
+                    vf[0] = Cv::unpack(
+                        *reinterpret_cast<const uint32_t*>(sV + tok * D * 2 + lane * 4));
                 }
                 const float2* pr = pbuf + tok * G;
 #pragma unroll
@@ -865,23 +821,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             issue_one();  // refill the stage just freed
         }
 
-        // ---- totals of this split: sum lsum over the token lanes, gather every head
+        // ---- totals of this split: row sums over the 16 token rows, every head's in every lane
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            la += __shfl_xor_sync(kFull, la, x);
+            lb += __shfl_xor_sync(kFull, lb, x);
+        }
         float lh[G];
 #pragma unroll
-        for (int i2 = 0; i2 < NV; ++i2) {
-            float x = lsum[i2];
-            x += __shfl_xor_sync(kFull, x, 2);
-            x += __shfl_xor_sync(kFull, x, 4);
-            x += __shfl_xor_sync(kFull, x, 8);
-            x += __shfl_xor_sync(kFull, x, 16);
-            if constexpr (G == 1) {
-                lh[0] = x;
-            } else {
-                const float other = __shfl_xor_sync(kFull, x, 1);
-                lh[i2] = b0 ? other : x;
-                lh[NV + i2] = b0 ? x : other;
-            }
-        }
+        for (int j = 0; j < G; ++j) lh[j] = __shfl_sync(kFull, (j & 1) ? lb : la, j >> 1);
         if (cur.ns == 1) {
 #pragma unroll
             for (int j = 0; j < G; ++j) {
