@@ -63,14 +63,9 @@ int prefill_min_q() { return 16; }
 
 thread_local cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
 
-// Requests with at least this many new tokens take the tensor-core prefill path.  INT8
-// pools have that path for two query heads per tile only (an even KV group); otherwise
-// every row runs on the streaming kernel.
-int prefill_min_q_for(const pkv_step_desc* d, bool int8) {
-    if (int8 && pkv::prefill_heads_per_tile(d->num_q_heads, d->num_kv_heads) != 2)
-        return INT_MAX;
-    return prefill_min_q();
-}
+// Requests with at least this many new tokens take the tensor-core prefill path (16-bit
+// and INT8 pools alike).
+int prefill_min_q_for(const pkv_step_desc*, bool) { return prefill_min_q(); }
 
 pkv::WorkspaceLayout layout_for(const pkv_step_desc* d, int num_sms, bool int8 = false) {
     return pkv::workspace_layout(d->num_reqs, d->num_q_heads, d->num_kv_heads, d->head_dim,

@@ -126,6 +126,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
     int4* tiles = ws_at<int4>(a, a.lay.tiles);
     const int Hkv = a.num_kv_heads;
     const int slots = a.num_q_heads / a.heads_per_tile;
+    // prefill tiles of a request: one per 128-row query tile and head pair (an even KV
+    // group), or one per pair of 128-row query tiles and query head (one head per KV head)
+    auto tile_units = [&](int q) {
+        return a.heads_per_tile == 2 ? cdiv(q, 128) : cdiv(cdiv(q, 128), 2);
+    };
     if (tid == 0) {
         s_sum = 0;
         s_bad = 0;
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
                 const long long items = Hkv * sum_ceil(c + 1, c + q, kPage * sp);
                 n.y = static_cast<int>(min(items, static_cast<long long>(a.lay.max_items) + 1));
             }
-            if (q > 1 && q >= a.prefill_min_q) n.z = cdiv(q, 128) * slots;
+            if (q > 1 && q >= a.prefill_min_q) n.z = tile_units(q) * slots;
         }
         if (tid == 0) s_npf = 0;  // read after the scan's barriers
         Int3 tot;
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
         for (int f = 0; !overflow && f < s_npf; ++f) {
             const int k = s_pf[f], qk = s_q[k];
             {
-                const int nt = cdiv(qk, 128), rq = base + k;
+                const int nt = tile_units(qk), rq = base + k;
                 for (int i = gwarp * 32 + lane; i < nt * slots; i += nwarps * 32)
                     tiles[s_tile0[k] + i] = make_int4(rq, nt - 1 - i / slots, i % slots, 0);
             }

@@ -68,7 +68,8 @@ struct StepArgs {
 WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int total_q_tokens, int max_q_len, int max_context_len,
                                  int num_sms, int prefill_min_q);
-// query heads one prefill tile covers for this head configuration
+// What the second chain of a prefill CTA is: 2 = the next query head of the KV group (an
+// even group), 1 = the next 128-row query tile of the same head (one head per KV head)
 inline int prefill_heads_per_tile(int num_q_heads, int num_kv_heads) {
     return ((num_q_heads / num_kv_heads) % 2 == 0) ? 2 : 1;
 }
@@ -102,7 +103,7 @@ int launch_prefill(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                    cudaEvent_t ev_stop);
 int launch_prefill_pair(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                         cudaEvent_t ev_stop);
-// INT8 pools, two query heads of an even KV group per tile (the only INT8 tile shape)
+// INT8 pools
 int launch_prefill_q8(const StepArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                       cudaEvent_t ev_stop);
 // Q ([T][Hq][D], 128-row boxes) and K/V pool (16-row page boxes) tensor maps, 128-byte

@@ -1,20 +1,22 @@
-// Prefill-chunk attention for two query heads of one KV group per CTA (grouped-query
-// attention with an even group size, hotelren.com/news/6181127 §6.3).
+// Prefill-chunk attention on tcgen05 over 16-bit pages.  Each CTA works on two chains of
+// 128 query rows that share one KV head's key/value stream (prefill_tile.cuh): two query
+// heads of one KV group (grouped-query attention with an even group size,
+// hotelren.com/news/6181127 §6.3), or two consecutive query tiles of one head when every
+// query head has its own KV head.
 //
-// Same mathematics as prefill.cu -- causal softmax attention of a 128-row query tile
-// against every key of its request read from the pages (hotelren.com §1.1, §2.1;
-// niuwancheng.cn "11. chunked prefill and unified scheduling") -- organised so the tensor
-// core stays busy:
-//   * both heads consume one K/V stream: each 128-key tile (8 pages) is loaded once for
+// Causal softmax attention of each 128-row query tile against every key of its request
+// read from the pages (hotelren.com §1.1, §2.1; niuwancheng.cn "11. chunked prefill and
+// unified scheduling"), organised so the tensor core stays busy:
+//   * both chains consume one K/V stream: each 128-key tile (8 pages) is loaded once for
 //     2 x 128 query rows, halving L2->SM traffic per FLOP;
 //   * six producer warps issue the page boxes in parallel, three for keys and three for
 //     values, each stream on its own ring (a tiled TMA instruction keeps its issuing
 //     thread busy for ~190 cycles, so one issuer cannot feed the MMA);
 //   * P = 2^(s - m) is written as packed 16-bit pairs into tensor memory over the scores it
 //     came from and read from there by the P V MMA, so shared memory holds only Q, K, V;
-//   * the MMA warp alternates the heads -- S0, S1, P0 V, S0', P1 V, S1', ... -- while the
-//     two softmax warpgroups work on the other head's scores;
-//   * a head's scores S_j complete only after its previous P V (one thread issues every
+//   * the MMA warp alternates the chains -- S0, S1, P0 V, S0', P1 V, S1', ... -- while the
+//     two softmax warpgroups work on the other chain's scores;
+//   * a chain's scores S_j complete only after its previous P V (one thread issues every
 //     MMA and tcgen05.commit tracks all of them), so the softmax may rescale O right away.
 // Softmax makes two passes over the score row in tensor memory (max, then exponentials) to
 // stay within the register budget of 480 threads.
@@ -25,6 +27,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "prefill_tile.cuh"
 #include "tc.cuh"
 
 namespace pkv {
@@ -92,17 +95,11 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- tile: request r, query tile qt, head pair hp -> heads 2hp, 2hp+1 (one KV group)
-    const int4 tl = reinterpret_cast<const int4*>(a.ws + a.lay.tiles)[blockIdx.x];
-    const int r = tl.x, qt = tl.y, h0 = 2 * tl.z;
-    const int g = h0 / (a.num_q_heads / a.num_kv_heads);
-    const int ctx = a.context_lens[r];
-    const int q_off = a.q_offsets[r];
-    const int rows_valid = min(kBM, a.q_lens[r] - qt * kBM);
-    const int first_pos = ctx + qt * kBM;
-    const int kv_len = first_pos + rows_valid;
-    const int n_kv = cdiv(kv_len, kBN);
-    const int npages_seq = cdiv(kv_len, kPage);
+    // ---- two chains of 128 query rows sharing one KV head's key/value stream
+    const int4 tile_rec = reinterpret_cast<const int4*>(a.ws + a.lay.tiles)[blockIdx.x];
+    const PairTile tile = pair_tile(a, tile_rec, kBM, kBN);
+    const int g = tile.g;
+    const int kv_len = tile.kv_len, n_kv = tile.n_kv, npages_seq = tile.npages_seq;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -148,10 +145,10 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             mbar_arrive_expect_tx(q_full, 2 * S::kQ);
             for (int h = 0; h < 2; ++h)
                 for (int c = 0; c < S::kHalves; ++c)
-                    tc::tma_load_3d(sQ(h) + c * S::kHalfBytes, &tm_q, c * 64, h0 + h,
-                                    q_off + qt * kBM, q_full);
+                    tc::tma_load_3d(sQ(h) + c * S::kHalfBytes, &tm_q, c * 64, tile.head[h],
+                                    tile.q_row[h], q_full);
         }
-        const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.max_pages;
+        const int32_t* bt = a.block_table + static_cast<int64_t>(tile.r) * a.max_pages;
         int win_base = -1, win = 0;
         auto page_of = [&](int lp) -> int {  // warp-wide
             const int base = lp & ~31;
@@ -278,6 +275,11 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
         const int i = threadIdx.x & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t my_s = tm_s(h) + lane_off, my_o = tm_o(h) + lane_off;
+        // this warpgroup's chain (selects, not indexing: the tile stays in registers)
+        const int first_pos = h ? tile.first_pos[1] : tile.first_pos[0];
+        const int rows_valid = h ? tile.rows_valid[1] : tile.rows_valid[0];
+        const int q_row = h ? tile.q_row[1] : tile.q_row[0];
+        const int q_head = h ? tile.head[1] : tile.head[0];
         const int pos = first_pos + i;
         const float sl2 = a.scale_log2;
         float m = -INFINITY, l = 0.f;
@@ -406,12 +408,12 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
             tc::fence_before_sync();
             mbar_arrive(&p_full[h]);
         }
-        // ---- epilogue: O / l -> 16-bit, row i of head h0 + h
+        // ---- epilogue: O / l -> 16-bit, row i of chain h
         if (ok && n_kv > 0 && mbar_wait_warp(o_final, 0)) {
             tc::fence_after_sync();
             const float inv_l = 1.f / l;
             T* orow = static_cast<T*>(a.out) +
-                      (static_cast<int64_t>(q_off + qt * kBM + i) * a.num_q_heads + h0 + h) * D;
+                      (static_cast<int64_t>(q_row + i) * a.num_q_heads + q_head) * D;
 #pragma unroll 1
             for (int cb = 0; cb < D / 32; ++cb) {
                 uint32_t o32[32];

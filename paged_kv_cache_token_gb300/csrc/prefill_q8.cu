@@ -1,6 +1,7 @@
-// Prefill-chunk attention over INT8 pages on the tensor cores: two query heads of one KV
-// group per CTA (grouped-query attention with an even group size, hotelren.com/news/6181127
-// §6.3), the cache in INT8 with fixed per-channel scales (wmrh.cn/news/64708 §4.3, §5.4).
+// Prefill-chunk attention over INT8 pages on the tensor cores, the cache in INT8 with fixed
+// per-channel scales (wmrh.cn/news/64708 §4.3, §5.4).  Each CTA works on two chains of 128
+// query rows sharing one KV head's stream (prefill_tile.cuh): two query heads of one KV
+// group (hotelren.com/news/6181127 §6.3), or two consecutive query tiles of one head.
 //
 // Same mathematics and the same pipeline as prefill_pair.cu: causal softmax attention of a
 // 128-row query tile against every key of its request, read from the pages; one MMA warp
@@ -27,6 +28,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "prefill_tile.cuh"
 #include "tc.cuh"
 
 namespace pkv {
@@ -126,17 +128,11 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- tile: request r, query tile qt, head pair hp -> heads 2hp, 2hp+1 (one KV group)
-    const int4 tl = reinterpret_cast<const int4*>(a.ws + a.lay.tiles)[blockIdx.x];
-    const int r = tl.x, qt = tl.y, h0 = 2 * tl.z;
-    const int g = h0 / (a.num_q_heads / a.num_kv_heads);
-    const int ctx = a.context_lens[r];
-    const int q_off = a.q_offsets[r];
-    const int rows_valid = min(kBM, a.q_lens[r] - qt * kBM);
-    const int first_pos = ctx + qt * kBM;
-    const int kv_len = first_pos + rows_valid;
-    const int n_kv = cdiv(kv_len, kBN);
-    const int npages_seq = cdiv(kv_len, kPage);
+    // ---- two chains of 128 query rows sharing one KV head's key/value stream
+    const int4 tile_rec = reinterpret_cast<const int4*>(a.ws + a.lay.tiles)[blockIdx.x];
+    const PairTile tile = pair_tile(a, tile_rec, kBM, kBN);
+    const int g = tile.g;
+    const int kv_len = tile.kv_len, n_kv = tile.n_kv, npages_seq = tile.npages_seq;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -181,10 +177,10 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
             mbar_arrive_expect_tx(q_full, 2 * S::kQ);
             for (int h = 0; h < 2; ++h)
                 for (int c = 0; c < S::kHalves; ++c)
-                    tc::tma_load_3d(sQ(h) + c * S::kHalfBytes, &tm_q, c * 64, h0 + h,
-                                    q_off + qt * kBM, q_full);
+                    tc::tma_load_3d(sQ(h) + c * S::kHalfBytes, &tm_q, c * 64, tile.head[h],
+                                    tile.q_row[h], q_full);
         }
-        const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.max_pages;
+        const int32_t* bt = a.block_table + static_cast<int64_t>(tile.r) * a.max_pages;
         const uint8_t* pool = static_cast<const uint8_t*>(is_v ? a.v_cache : a.k_cache);
         int win_base = -1, win = 0;
         auto page_of = [&](int lp) -> int {  // warp-wide
@@ -351,6 +347,11 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
         const int i = threadIdx.x & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t my_s = tm_s(h) + lane_off, my_o = tm_o(h) + lane_off;
+        // this warpgroup's chain (selects, not indexing: the tile stays in registers)
+        const int first_pos = h ? tile.first_pos[1] : tile.first_pos[0];
+        const int rows_valid = h ? tile.rows_valid[1] : tile.rows_valid[0];
+        const int q_row = h ? tile.q_row[1] : tile.q_row[0];
+        const int q_head = h ? tile.head[1] : tile.head[0];
         const int pos = first_pos + i;
         bool ok = mbar_wait_warp(q_full, 0);
         // ---- Q' = Q * k_scale * f in place, row i of head h.  Physical chunk pc ^ (i & 7)
@@ -399,7 +400,10 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = Cv::unpack(ww[e]);
-                    o4[e] = Ch::pack(f.x * kv[2 * e] * fq, f.y * kv[2 * e + 1] * fq);
+                    // rows past the chunk (or a whole chain past it) become zeros: finite
+                    // scores whatever the rows held, and a chain without rows has f = 2^100
+                    o4[e] = i < rows_valid ? Ch::pack(f.x * kv[2 * e] * fq, f.y * kv[2 * e + 1] * fq)
+                                           : 0u;
                 }
                 *wp = make_uint4(o4[0], o4[1], o4[2], o4[3]);
             }
@@ -507,13 +511,13 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
             tc::fence_before_sync();
             mbar_arrive(&p_full[h]);
         }
-        // ---- epilogue: O / l * v_scale -> the step's dtype, row i of head h0 + h
+        // ---- epilogue: O / l * v_scale -> the step's dtype, row i of chain h
         if (ok && n_kv > 0 && mbar_wait_warp(o_final, 0)) {
             tc::fence_after_sync();
             const float inv_l = 1.f / l;
             const float* vs = a.v_scale + g * D;
             T* orow = static_cast<T*>(a.out) +
-                      (static_cast<int64_t>(q_off + qt * kBM + i) * a.num_q_heads + h0 + h) * D;
+                      (static_cast<int64_t>(q_row + i) * a.num_q_heads + q_head) * D;
 #pragma unroll 1
             for (int cb = 0; cb < D / 32; ++cb) {
                 uint32_t o32[32];
@@ -575,7 +579,6 @@ int launch_q8_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEven
 }  // namespace
 
 int launch_prefill_q8(const StepArgs& a, cudaStream_t stream, cudaEvent_t e0, cudaEvent_t e1) {
-    if (a.heads_per_tile != 2) return PKV_ERR_UNSUPPORTED;
     if (a.dtype == PKV_BF16)
         return a.head_dim == 128 ? launch_q8_t<__nv_bfloat16, 128>(a, stream, e0, e1)
                                  : launch_q8_t<__nv_bfloat16, 64>(a, stream, e0, e1);

@@ -240,3 +240,9 @@ def test_int8_decode_loop_graph_bitwise_identical():
     assert kv.read_error() == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(kv.k_cache, ref_pool[0]) and torch.equal(kv.v_cache, ref_pool[1])
+
+
+def test_int8_mha_prefill_tile_pairs():
+    # INT8 pages with one query head per KV head: tile pairs of one head on the tensor cores
+    specs = [(0, 1, 0), (0, 129, 1), (0, 256, 0), (0, 257, 0), (300, 383, 0), (40, 640, 1)]
+    run_all_int8(custom(1200, 8, 8, 128, 0, specs))

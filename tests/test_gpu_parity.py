@@ -382,3 +382,25 @@ def test_sorted_native_plans_match_oracle():
         out = runner.run_step(kv, w, plan)
         assert_close(gpu_as_f64(out), oracle_rows(w, plan), "sorted step %d" % i)
     assert kv.read_error() == 0
+
+
+@pytest.mark.parametrize("hq,d,dtype", [(8, 64, 1), (4, 128, 0), (2, 128, 1)])
+def test_mha_prefill_tile_pairs(hq, d, dtype):
+    # one query head per KV head: a prefill CTA takes query tiles 2u and 2u + 1 of one
+    # head; odd tile counts leave its second chain without rows, and the first chain sees
+    # the second tile's extra keys fully masked
+    specs = [(0, 1, 0), (0, 127, 0), (0, 128, 0), (0, 129, 1), (0, 256, 0), (0, 257, 0),
+             (300, 383, 0), (40, 640, 1)]
+    run_all(custom(1100 + hq + d, hq, hq, d, dtype, specs))
+
+
+def test_mha_prefill_8k_one_shot_sampled():
+    """An 8,192-token causal prefill with 32 query heads each on its own KV head (MHA):
+    sampled rows against the oracle."""
+    w = W.prefill()
+    w.num_kv_heads = 32
+    w.num_pages = w.pages_needed() + 8
+    w.page_order = torch.randperm(w.num_pages,
+                                  generator=torch.Generator().manual_seed(77)).numpy().astype(np.int32)
+    worst, _, _ = run_all(w, check_rows=lambda p: _sample_rows(p, 32))
+    print("mha prefill 8k worst", worst)
