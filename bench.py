@@ -140,8 +140,10 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "common.cuh", "launch.h"],
     "decode_kernel_int8": ["decode.cu", "common.cuh", "launch.h"],
-    "prefill_q8_kernel": ["prefill_q8.cu", "tc.cuh", "common.cuh", "launch.h"],
-    "prefill_pair_kernel": ["prefill_pair.cu", "tc.cuh", "common.cuh", "launch.h"],
+    "prefill_q8_kernel": ["prefill_q8.cu", "prefill_tile.cuh", "tc.cuh", "common.cuh",
+                          "launch.h"],
+    "prefill_pair_kernel": ["prefill_pair.cu", "prefill_tile.cuh", "tc.cuh", "common.cuh",
+                            "launch.h"],
 }
 
 
