@@ -246,3 +246,21 @@ def test_int8_mha_prefill_tile_pairs():
     # INT8 pages with one query head per KV head: tile pairs of one head on the tensor cores
     specs = [(0, 1, 0), (0, 129, 1), (0, 256, 0), (0, 257, 0), (300, 383, 0), (40, 640, 1)]
     run_all_int8(custom(1200, 8, 8, 128, 0, specs))
+
+
+def test_int8_many_requests_cross_plan_chunks():
+    rng = np.random.default_rng(2501)
+    specs = [((int(rng.integers(0, 60)), int(rng.integers(16, 40)), 0) if i % 7 == 3
+              else (int(rng.integers(0, 90)), 0, 1)) for i in range(2500)]
+    w = custom(1301, 8, 2, 128, 0, specs, extra_pages=16)
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, kv_int8=True)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    assert plan.num_reqs == 2500
+    out = runner.run_step(kv, w, plan)
+    assert kv.read_error() == 0
+    T = plan.total_q_tokens
+    rows = sorted(set(np.random.default_rng(5).choice(T, 300, replace=False).tolist()) | {0, T - 1})
+    got = gpu_as_f64(out[torch.as_tensor(rows)])
+    assert_close(got, oracle_rows_int8(w, plan, rows), "int8 2500 reqs")

@@ -404,3 +404,26 @@ def test_mha_prefill_8k_one_shot_sampled():
                                   generator=torch.Generator().manual_seed(77)).numpy().astype(np.int32)
     worst, _, _ = run_all(w, check_rows=lambda p: _sample_rows(p, 32))
     print("mha prefill 8k worst", worst)
+
+
+def test_many_requests_cross_plan_chunks():
+    # 2,500 requests in one step: the device planner works through them 1,024 at a time,
+    # carrying its row, item and tile counts from chunk to chunk; decodes and short
+    # prefill chunks are interleaved so every chunk holds both kinds
+    rng = np.random.default_rng(2500)
+    specs = []
+    for i in range(2500):
+        if i % 7 == 3:
+            specs.append((int(rng.integers(0, 60)), int(rng.integers(16, 40)), 0))
+        else:
+            specs.append((int(rng.integers(0, 90)), 0, 1))
+    w = custom(1300, 4, 2, 64, 0, specs, extra_pages=16)
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    assert plan.num_reqs == 2500 and plan.max_q_len >= 16
+    out = runner.run_step(kv, w, plan)
+    assert kv.read_error() == 0
+    rows = _sample_rows(plan, 400)
+    assert_close(gpu_as_f64(out[torch.as_tensor(rows)]), oracle_rows(w, plan, rows), "2500 reqs")
