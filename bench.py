@@ -315,7 +315,7 @@ def time_decode_int8(device, steps, pool_pages=70000):
     return res
 
 
-def time_prefill(device, reps=3, kv_int8=False):
+def time_prefill(device, reps=5, kv_int8=False):
     """Attention-kernel time of the 8K one-shot prefill and of the 4 x 2048 chunks (over
     INT8 pages with ``kv_int8``)."""
     from paged_kv_cache_token_gb300 import binding, runner
@@ -338,23 +338,22 @@ def time_prefill(device, reps=3, kv_int8=False):
                               device=device)
             kv.attention(ds, q, w.scale, out)          # warm-up
             torch.cuda.synchronize()
+            # `reps` identical steps queued back to back between the events, so the host's
+            # launch latency overlaps device work as it does in a stream of steps; the
+            # kernel events bracket the main kernel of the last step
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ka, kb = lib_event(), lib_event()
-            t = []
-            tk = []
+            binding.set_kernel_events(0, ka, kb)
+            binding.set_kernel_events(1, ka, kb)
+            a.record()
             for _ in range(reps):
-                binding.set_kernel_events(0, ka, kb)
-                binding.set_kernel_events(1, ka, kb)
-                a.record()
                 kv.attention(ds, q, w.scale, out)
-                b.record()
-                torch.cuda.synchronize()
-                binding.set_kernel_events(0, None, None)
-                binding.set_kernel_events(1, None, None)
-                t.append(a.elapsed_time(b))
-                tk.append(ka.elapsed_time(kb))
-            total_ms += float(np.median(t))
-            main_ms += float(np.median(tk))
+            b.record()
+            torch.cuda.synchronize()
+            binding.set_kernel_events(0, None, None)
+            binding.set_kernel_events(1, None, None)
+            total_ms += a.elapsed_time(b) / reps
+            main_ms += ka.elapsed_time(kb)
         assert kv.read_error() == 0
         res[label] = dict(ms=total_ms, tflops=flops / total_ms / 1e9, flops=flops,
                           main_kernel_ms=main_ms)

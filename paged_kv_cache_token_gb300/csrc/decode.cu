@@ -971,10 +971,15 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
                                  int num_sms, int prefill_min_q) {
     WorkspaceLayout L{};
     const int G = num_q_heads / num_kv_heads;
-    // decode rows: every row of a request below the prefill threshold
+    // decode rows: every row of a request below the prefill threshold.  No request can have
+    // fewer than T - (B - 1) * max_q_len new tokens; when even that reaches the threshold
+    // (one request, say) there are no decode rows and the decode kernels are not launched
     L.max_rows = static_cast<int>(std::min<long long>(
         total_q_tokens,
         static_cast<long long>(num_reqs) * std::max(0, std::min(max_q_len, prefill_min_q - 1))));
+    const long long min_q = static_cast<long long>(total_q_tokens) -
+                            static_cast<long long>(std::max(0, num_reqs - 1)) * max_q_len;
+    if (min_q >= prefill_min_q) L.max_rows = 0;
     L.target_items = 2 * kDecWarps * kItemsPerWarp * num_sms;  // 2 CTAs per SM
     // pages per split >= total / target, so items <= target + one per (row, KV head);
     // pages per split >= kMinSplitPages bounds them by the longest row as well
