@@ -11,7 +11,8 @@ d=128) and the same prompt as 4 x 2,048-token chunks, in TFLOP/s of causal atten
 The object "decode_loop" times 64 consecutive decode steps of the MHA-skew workload as
 separate steps, as one device-side loop and as one CUDA graph replay (per-step overhead).
 The object "int8_kv" times the decode step over INT8 pages (per-channel scales): half the
-K/V bytes of the bf16 step.
+K/V bytes of the bf16 step.  The object "mixed_step" times the 15 unified steps of the
+mixed workload (30 decodes plus a 2,018-token prefill chunk per step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -362,6 +363,48 @@ def time_prefill(device, reps=5, kv_int8=False):
     return res
 
 
+def time_mixed(device, reps=3):
+    """The mixed workload's 15 unified steps (30 decodes + a 2,018-token chunk of a
+    30,000-token prompt, token budget 2048): every step's append + attention, each step
+    repeated `reps` times back to back between events (the repeats rewrite the same pages
+    with the same values and recompute the same outputs)."""
+    from paged_kv_cache_token_gb300 import runner
+    w = W.mixed()
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, device=device, fill_sentinel=False)
+    runner.load_history(kv, w, s.history_plan())
+    plans = s.all_steps()
+    flops = sum(causal_flops(w, p) for p in plans)
+    nbytes = sum(step_bytes(w, p)["step"] for p in plans)
+    total = 0.0
+    per_step = []
+    for p in plans:
+        qh, kh, vh = runner.step_host_inputs(w, p)
+        ds = kv.upload(p)
+        q, k, v = (runner.bits_to_tensor(x, w.dtype, device) for x in (qh, kh, vh))
+        out = torch.empty((p.total_q_tokens, w.num_q_heads, w.head_dim), dtype=kv.dtype,
+                          device=device)
+        kv.append(ds, k, v)
+        kv.attention(ds, q, w.scale, out)   # warm-up
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            kv.append(ds, k, v)
+            kv.attention(ds, q, w.scale, out)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        per_step.append(ms)
+        total += ms
+    assert kv.read_error() == 0
+    del kv
+    torch.cuda.empty_cache()
+    return {"steps": len(plans), "ms_total": total,
+            "ms_per_step_first_last": [per_step[0], per_step[-1]],
+            "tflops": flops / total / 1e9, "flops": flops, "step_bytes_total": nbytes}
+
+
 def time_decode_loop(device, reps=5):
     """64 consecutive decode steps of the MHA-skew workload (16 requests, 32 heads, fp16):
     per-step time as separate steps (metadata of every step already on the device, append +
@@ -508,7 +551,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-loop", action="store_true")
     ap.add_argument("--no-int8", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode-loop", "int8", "int8-prefill"],
+    ap.add_argument("--only", choices=["prefill", "decode-loop", "int8", "int8-prefill", "mixed"],
                     default=None,
                     help="time only the prefill workload (one-shot 8K and 4 x 2K) and print "
                          "its JSON object; used for focused profiler captures")
@@ -532,6 +575,10 @@ def main():
             if dist_ctx.rank == 0:
                 pf = time_prefill(device)
                 print(json.dumps({"prefill_chunk": pf, "peak_tflops": bf16}))
+            return
+        if args.only == "mixed":
+            if dist_ctx.rank == 0:
+                print(json.dumps({"mixed_step": time_mixed(device), "peak_tflops": bf16}))
             return
         if args.only == "int8":
             if dist_ctx.rank == 0:
@@ -604,6 +651,13 @@ def main():
                         "in L2, so GB/s here is not an HBM rate; the comparison is between "
                         "launch modes" % (dl["bytes_per_step"] / 1e6),
                 **dl}
+        if not args.no_prefill and dist_ctx.rank == 0:
+            mx = time_mixed(device)
+            line["mixed_step"] = {
+                "workload": "15 unified steps, token budget 2048: 30 decode requests (ctx "
+                            "U[1k,8k]) + a 30,000-token prompt in 2,018-token chunks, 32/8 "
+                            "heads, d 128, bf16 (append + attention per step)",
+                **mx, "frac_of_bf16_peak": mx["tflops"] / bf16}
         if not args.no_int8 and dist_ctx.rank == 0:
             q8 = time_decode_int8(device, args.steps, args.pool_pages)
             line["int8_kv"] = {
