@@ -194,11 +194,12 @@ PKV_API int pkv_paged_attention_step_static_ws(const pkv_step_desc* desc, const 
  * fp32 scale (per-channel, calibrated before the pool is filled):
  *   code  = clamp(round_half_even(x / scale[h][c]), -127, 127)   (IEEE fp32 quotient)
  *   value = code * scale[h][c]
- * The attention step reads the codes and attends over the values they stand for; all of
+ * The attention step reads the codes and attends over the values they stand for.  Its
  * scores and weighted sums run on the tensor cores with fp16 operands: the codes exactly,
  * q times the key scales (scaled by a power of two into fp16 range) and the softmax weights
- * rounded to fp16, fp32 accumulation and softmax.  Every row (decode and prefill chunk) runs
- * on the streaming kernel.
+ * rounded to fp16, with fp32 accumulation and softmax; the value scales are applied to the
+ * fp32 sums.  Decode rows stream through the split-KV kernel and prefill chunks run as
+ * 128-row tiles, as for 16-bit pages.
  *   k_scale, v_scale   device fp32 [num_kv_heads][head_dim], 16-byte aligned, > 0
  *   k_cache            device int8 [num_pages][num_kv_heads][16][head_dim]
  *   v_cache            device int8 [num_pages][num_kv_heads][head_dim][16]: within a page
