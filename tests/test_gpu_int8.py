@@ -264,3 +264,23 @@ def test_int8_many_requests_cross_plan_chunks():
     rows = sorted(set(np.random.default_rng(5).choice(T, 300, replace=False).tolist()) | {0, T - 1})
     got = gpu_as_f64(out[torch.as_tensor(rows)])
     assert_close(got, oracle_rows_int8(w, plan, rows), "int8 2500 reqs")
+
+
+def test_int8_bad_pages_set_flags_and_skip():
+    # a page id outside the pool: the append skips that token (nothing else written) and
+    # flags it; attention through the same table flags it too and never faults
+    from paged_kv_cache_token_gb300.scheduler import make_plan
+    plan = make_plan([0, 1], [3, 2], [0, 0], [[0], [7]])   # page 7 outside a 4-page pool
+    scales = np.full((1, 64), 0.05, np.float32)
+    kv = runner.PagedKV(4, 1, 1, 64, 0, k_scale=scales, v_scale=scales)
+    ds = kv.upload(plan)
+    k = torch.full((5, 1, 64), 1.0, dtype=torch.bfloat16, device="cuda")   # code 20
+    kv.append(ds, k, k)
+    assert kv.read_error() & binding.DEVERR_PAGE_RANGE
+    kc = kv.k_cache.cpu().numpy()
+    assert np.all(kc[0, 0, :3] == 20) and np.all(kc[0, 0, 3:] == runner.INT8_SENTINEL)
+    assert np.all(kc[1:] == runner.INT8_SENTINEL)
+    kv.err.zero_()
+    q = torch.zeros((5, 1, 64), dtype=torch.bfloat16, device="cuda")
+    kv.attention(ds, q, 0.125)
+    assert kv.read_error() & binding.DEVERR_PAGE_RANGE
