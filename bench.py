@@ -566,7 +566,10 @@ def main():
             run_reference(args, dist_ctx)
             return
         from paged_kv_cache_token_gb300 import binding, build
-        build.build()
+        # one process per node compiles (ranks share the in-tree build); the rest wait
+        if dist_ctx.local == 0:
+            build.build()
+        dist_ctx.barrier()
         binding.load()
         device = torch.device("cuda", dist_ctx.local if dist_ctx.world > 1 else 0)
         torch.cuda.set_device(device)
