@@ -427,3 +427,27 @@ def test_many_requests_cross_plan_chunks():
     assert kv.read_error() == 0
     rows = _sample_rows(plan, 400)
     assert_close(gpu_as_f64(out[torch.as_tensor(rows)]), oracle_rows(w, plan, rows), "2500 reqs")
+
+
+def test_gqa8_prefill_4k_and_decode_sampled():
+    """Eight query heads per KV head (64/8, d=128, bf16): a 4,096-token one-shot prefill in
+    the pair kernel, then 4 decode steps, sampled rows against the oracle."""
+    w = custom(1400, 64, 8, 128, 0, [(0, 4096, 4)])
+    worst, _, _ = run_all(w, check_rows=lambda p: _sample_rows(p, 32))
+    print("gqa8 worst", worst)
+
+
+def test_fp16_prefill_8k_one_shot_sampled():
+    """The 8,192-token one-shot prefill with fp16 Q/K/V (32/8 heads, d=128)."""
+    w = W.prefill()
+    w.dtype = W.FP16
+    w._cache.clear()
+    worst, _, _ = run_all(w, check_rows=lambda p: _sample_rows(p, 32))
+    print("fp16 prefill worst", worst)
+
+
+def test_d64_decode_long_contexts():
+    """Head dim 64 (16/4 heads, fp16): decode rows over 20k-60k cached tokens, many splits."""
+    w = custom(1500, 16, 4, 64, 1, [(60000, 0, 2), (20000, 0, 2), (33333, 0, 2)])
+    worst, _, _ = run_all(w)
+    assert worst[0] < 2e-2
