@@ -38,6 +38,8 @@ constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kStages = 3;
 constexpr int kMinSplitPages = 4;
 constexpr int kItemsPerWarp = 6;  // target decode items per resident warp
+constexpr int kManySplits = 64;   // rows that may have more splits get a grouped combine
+constexpr int kChunkedCtas = 4096;  // largest grid of the two-pass combine
 
 template <typename T>
 __device__ __forceinline__ T* ws_at(const StepArgs& a, size_t off) {
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
         }
         for (int k = blockIdx.x + gridDim.x * warp; !overflow && k < nreq;
              k += gridDim.x * (kPlanThreads / 32)) {
-            const int rq = base + k, qk = s_q[k], ck = s_c[k];
+            const int qk = s_q[k], ck = s_c[k];
             if (qk >= 1 && qk < a.prefill_min_q) {
                 // rows of this request, 32 at a time: lane i = row r0 + i; warp scan of item
                 // counts, carried from one group of rows to the next
@@ -232,35 +234,39 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
                     const int first = item0 + incl - Hkv * ns;
                     if (row < qk)
                         rows[s_row0[k] + row] = make_int4(s_t0[k] + row, first, ck + row + 1, ns);
-                    for (int i = 0; i < min(32, qk - r0); ++i) {
-                        const unsigned ns_i = __shfl_sync(kFull, ns, i);
-                        const int first_i = __shfl_sync(kFull, first, i);
-                        const int nkv = ck + r0 + i + 1, pages = cdiv(nkv, kPage);
-                        const int t = s_t0[k] + r0 + i;
-                        // balanced splits: the first `rem` splits get one page more than `per`
-                        const int per = pages / static_cast<int>(ns_i);
-                        const int rem = pages - per * static_cast<int>(ns_i);
-                        // lane l writes 16-byte half l of the row's item records, so a warp
-                        // store covers 512 contiguous bytes; item position = slot (splits of
-                        // a (row, head) adjacent)
-                        int4* dst = items + 2 * static_cast<int64_t>(first_i);
-                        for (unsigned h = lane; h < 2 * Hkv * ns_i; h += 32) {
-                            const unsigned e = h >> 1;
-                            const int g = static_cast<int>(e / ns_i);
-                            const int s_ = static_cast<int>(e) - g * static_cast<int>(ns_i);
-                            if (h & 1) {
-                                dst[h] = make_int4(nkv, static_cast<int>(ns_i), rq,
-                                                   first_i + g * static_cast<int>(ns_i));
-                            } else {
-                                const int pb = s_ * per + min(s_, rem);
-                                const int np = per + (s_ < rem ? 1 : 0);
-                                dst[h] = make_int4(t, g | (s_ << 16), pb, np);
-                            }
-                        }
-                    }
                     item0 += __shfl_sync(kFull, incl, 31);
                 }
             }
+        }
+        // item records, one item per thread over the whole grid (a long row has thousands):
+        // the request by binary search over the chunk's first-item offsets (requests without
+        // items share their successor's offset, so the last offset <= e is the owner), then
+        // the row by walking the request's < prefill_min_q rows.  Record 0 = {token,
+        // head | split << 16, first page, pages}, record 1 = {keys, splits, request, slot of
+        // split 0}; the first `rem` splits of a row get one page more than `per`.
+        const int nitems = overflow ? 0 : tot.y;
+        for (int i = blockIdx.x * kPlanThreads + tid; i < nitems; i += gridDim.x * kPlanThreads) {
+            const int e = carry.y + i;
+            int lo = 0, hi = nreq - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_item0[mid] <= e) lo = mid; else hi = mid - 1;
+            }
+            const int k = lo, ck = s_c[k];
+            int local = e - s_item0[k], row = 0, first = s_item0[k], ns = 1;
+            for (;; ++row) {
+                ns = cdiv(ck + row + 1, kPage * sp);
+                if (local < Hkv * ns || row + 1 >= s_q[k]) break;
+                local -= Hkv * ns;
+                first += Hkv * ns;
+            }
+            const int g = local / ns, sidx = local - g * ns;
+            const int nkv = ck + row + 1, pages = cdiv(nkv, kPage);
+            const int per = pages / ns, rem = pages - per * ns;
+            int4* dst = items + 2 * static_cast<int64_t>(e);
+            dst[0] = make_int4(s_t0[k] + row, g | (sidx << 16), sidx * per + min(sidx, rem),
+                               per + (sidx < rem ? 1 : 0));
+            dst[1] = make_int4(nkv, ns, base + k, first + g * ns);
         }
         carry = Int3{carry.x + tot.x, carry.y + tot.y, carry.z + tot.z};
         __syncthreads();
@@ -903,47 +909,55 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 }
 
 // ------------------------------------------------------------------------------------
-// combine: one CTA per (decode row, KV head) with more than one split, one thread per
-// (query head, 4 dims); every split's loads are independent so they overlap:
-//   m* = max_s m_s,  l* = sum_s l_s 2^(m_s - m*),  out = sum_s O_s 2^(m_s - m*) / l*
+// combine.  A row's splits are merged by NG groups of one thread per (query head, 4 dims):
+// group k folds splits first + (k + NG i) stride into a running (M, L, acc) -- the loads of
+// a batch of splits are independent, so they overlap -- and the groups' states are then
+// merged through shared memory:
+//   m* = max_s m_s,  l* = sum_s l_s 2^(m_s - m*),  acc* = sum_s O_s 2^(m_s - m*)
+// (m in log2 units, O unnormalised).  Three launch shapes:
+//   kCombineRow     one CTA per (row, KV head), NG = 1: every row of a step whose rows have
+//                   at most kManySplits splits.
+//   kCombineChunks  CTA (row x KV head, c) merges splits [64c, 64c + 64) into the slot of
+//                   split 64c -- the merged state has the same (m, l, O) form as a split --
+//                   or, for a row with at most 64 splits, writes the row's output.
+//   kCombineParts   one CTA per (row, KV head) with more than 64 splits merges its chunk
+//                   states (stride 64) into the output.
+// The last two serve a long context on few rows, where one CTA per (row, KV head) would
+// read megabytes of partials at a single SM's bandwidth.
 // ------------------------------------------------------------------------------------
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(G * D / 4) combine_kernel(StepArgs a) {
+enum : int { kCombineRow = 0, kCombineChunks = 1, kCombineParts = 2 };
+constexpr int kCombineChunk = 64;
+
+template <typename T, int D, int G, int NG>
+__device__ __forceinline__ void combine_fold(const StepArgs& a, int64_t base, int first,
+                                             int count, int stride, bool to_out, int t, int g,
+                                             float2 (*s_ml)[G * D / 4],
+                                             float4 (*s_acc)[G * D / 4]) {
     using Cv = F16<T>;
-    const int Hkv = a.num_kv_heads;
-    const int d = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
-    // the row records come from the plan, which completed before the decode kernel let this
-    // grid launch: read them before waiting for the decode kernel's partials
-    const int32_t* ctrl = ws_at<const int32_t>(a, a.lay.ctrl);
-    const int nrows = ctrl[2];
-    const int4 row = ws_at<const int4>(a, a.lay.rows)[d];  // {token, first slot, keys, splits}
-    pdl_wait();  // the decode kernel has finished writing the partials
-    if (d >= nrows) return;
-    const int ns = row.w;
-    if (ns <= 1) return;  // finished in place by the decode kernel
-    const int64_t base = row.y + static_cast<int64_t>(g) * ns;
-    const float2* part_ml = ws_at<const float2>(a, a.lay.part_ml);
-    const float* part_o = ws_at<const float>(a, a.lay.part_o);
-    const int j = threadIdx.x / (D / 4), dim = (threadIdx.x % (D / 4)) * 4;
-    // one pass with a running maximum: acc, L rescaled when a split raises it.  Splits are
-    // read in predicated batches of kBatch so all loads of a batch are in flight together.
-    constexpr int kBatch = 8;
+    constexpr int TPG = G * D / 4;              // threads per group
+    constexpr int kBatch = NG > 1 ? 4 : 8;      // splits in flight per thread
+    float2* part_ml = ws_at<float2>(a, a.lay.part_ml);
+    float* part_o = ws_at<float>(a, a.lay.part_o);
+    const int grp = threadIdx.x / TPG, tin = threadIdx.x % TPG;
+    const int j = tin / (D / 4), dim = (tin % (D / 4)) * 4;
+    // one pass with a running maximum: acc, L rescaled when a split raises it
     float M = -1e30f, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ns; s0 += kBatch) {
+    for (int i0 = grp; i0 < count; i0 += NG * kBatch) {
         float2 ml[kBatch];
         float4 o[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            if (s0 + u < ns) {
-                const int64_t slot = base + s0 + u;
+            const int i = i0 + u * NG;
+            if (i < count) {
+                const int64_t slot = base + first + static_cast<int64_t>(i) * stride;
                 ml[u] = part_ml[slot * G + j];
                 o[u] = *reinterpret_cast<const float4*>(part_o + (slot * G + j) * D + dim);
             }
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            if (s0 + u < ns) {
+            if (i0 + u * NG < count) {
                 const float mn = fmaxf(M, ml[u].x);
                 const float c = fast_exp2(M - mn), w = fast_exp2(ml[u].x - mn);
                 M = mn;
@@ -955,12 +969,78 @@ __global__ void __launch_bounds__(G * D / 4) combine_kernel(StepArgs a) {
             }
         }
     }
-    const float inv = 1.f / L;
-    const int t = row.x;
-    uint16_t* out = static_cast<uint16_t*>(a.out) +
-                    (static_cast<int64_t>(t) * a.num_q_heads + g * G + j) * D + dim;
-    *reinterpret_cast<uint2*>(out) =
-        make_uint2(Cv::pack(acc.x * inv, acc.y * inv), Cv::pack(acc.z * inv, acc.w * inv));
+    if constexpr (NG > 1) {
+        s_ml[grp][tin] = make_float2(M, L);
+        s_acc[grp][tin] = acc;
+        __syncthreads();
+        if (grp == 0) {
+            float Ms = M;
+#pragma unroll
+            for (int k = 1; k < NG; ++k) Ms = fmaxf(Ms, s_ml[k][tin].x);
+            L = 0.f;
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < NG; ++k) {
+                const float2 mlk = s_ml[k][tin];
+                const float4 ak = s_acc[k][tin];
+                const float w = fast_exp2(mlk.x - Ms);  // 0 for a group without splits
+                L = fmaf(mlk.y, w, L);
+                acc.x = fmaf(ak.x, w, acc.x);
+                acc.y = fmaf(ak.y, w, acc.y);
+                acc.z = fmaf(ak.z, w, acc.z);
+                acc.w = fmaf(ak.w, w, acc.w);
+            }
+            M = Ms;
+        }
+        __syncthreads();  // shared state read before a next fold overwrites it
+        if (grp != 0) return;
+    }
+    if (to_out) {
+        const float inv = 1.f / L;
+        uint16_t* out = static_cast<uint16_t*>(a.out) +
+                        (static_cast<int64_t>(t) * a.num_q_heads + g * G + j) * D + dim;
+        *reinterpret_cast<uint2*>(out) = make_uint2(Cv::pack(acc.x * inv, acc.y * inv),
+                                                    Cv::pack(acc.z * inv, acc.w * inv));
+    } else {
+        // the chunk's state replaces its first split's: every read of that slot happened
+        // before the barrier above
+        const int64_t slot = base + first;
+        part_ml[slot * G + j] = make_float2(M, L);
+        *reinterpret_cast<float4*>(part_o + (slot * G + j) * D + dim) = acc;
+    }
+}
+
+template <typename T, int D, int G, int NG, int Stage>
+__global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
+    constexpr int TPG = G * D / 4;
+    __shared__ float2 s_ml[NG > 1 ? NG : 1][TPG];
+    __shared__ float4 s_acc[NG > 1 ? NG : 1][TPG];
+    const int Hkv = a.num_kv_heads;
+    const int d = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
+    // the row records come from the plan, which completed before the decode kernel let this
+    // grid launch: read them before waiting for the decode kernel's partials
+    const int32_t* ctrl = ws_at<const int32_t>(a, a.lay.ctrl);
+    const int nrows = ctrl[2];
+    const int4 row = ws_at<const int4>(a, a.lay.rows)[d];  // {token, first slot, keys, splits}
+    pdl_wait();  // the previous grid (decode kernel or chunk pass) has finished its writes
+    if (d >= nrows) return;
+    const int ns = row.w;
+    if (ns <= 1) return;  // finished in place by the decode kernel
+    const int64_t base = row.y + static_cast<int64_t>(g) * ns;
+    if constexpr (Stage == kCombineRow) {
+        combine_fold<T, D, G, NG>(a, base, 0, ns, 1, true, row.x, g, s_ml, s_acc);
+    } else if constexpr (Stage == kCombineChunks) {
+        const int nch = cdiv(ns, kCombineChunk);
+        for (int c = blockIdx.y; c < nch; c += gridDim.y) {  // uniform over the CTA
+            const int first = c * kCombineChunk;
+            combine_fold<T, D, G, NG>(a, base, first, min(kCombineChunk, ns - first), 1,
+                                      nch == 1, row.x, g, s_ml, s_acc);
+        }
+    } else {
+        if (ns <= kCombineChunk) return;  // written by the chunk pass
+        combine_fold<T, D, G, NG>(a, base, 0, cdiv(ns, kCombineChunk), kCombineChunk, true,
+                                  row.x, g, s_ml, s_acc);
+    }
 }
 
 // ------------------------------------------------------------------------------------
@@ -1036,10 +1116,29 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
                    a) != cudaSuccess)
         return PKV_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return PKV_ERR_CUDA;
-    return launch_pdl(combine_kernel<T, D, G>, dim3(std::max(1, a.lay.max_rows * a.num_kv_heads)),
-                      dim3(G * D / 4), 0, stream, a) == cudaSuccess
-               ? PKV_OK
-               : PKV_ERR_CUDA;
+    // rows can have at most ceil(pages / kMinSplitPages) splits.  Past kManySplits the
+    // combine runs in two passes over chunks of splits with NG thread groups per CTA, or --
+    // when rows x heads x chunks would launch mostly idle CTAs -- in one pass per (row, KV
+    // head) with NG groups
+    constexpr int kTpg = G * D / 4, kNg = std::min(8, 1024 / kTpg);
+    const int max_splits = cdiv(cdiv(a.max_context_len + a.max_q_len, kPage), kMinSplitPages);
+    const int rows_heads = std::max(1, a.lay.max_rows * a.num_kv_heads);
+    const int chunks = cdiv(max_splits, kCombineChunk);
+    cudaError_t e;
+    if (max_splits <= kManySplits) {
+        e = launch_pdl(combine_kernel<T, D, G, 1, kCombineRow>, dim3(rows_heads), dim3(kTpg), 0,
+                       stream, a);
+    } else if (static_cast<long long>(rows_heads) * chunks <= kChunkedCtas) {
+        e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineChunks>, dim3(rows_heads, chunks),
+                       dim3(kTpg * kNg), 0, stream, a);
+        if (e == cudaSuccess)
+            e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineParts>, dim3(rows_heads),
+                           dim3(kTpg * kNg), 0, stream, a);
+    } else {
+        e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineRow>, dim3(rows_heads),
+                       dim3(kTpg * kNg), 0, stream, a);
+    }
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 template <typename T, int D>
