@@ -189,11 +189,22 @@ def test_step_staging_bitwise_identical():
 
 def test_long_contexts():
     # maximum-size rows: a decode row over 131,071 cached tokens (8,192 pages, about 900
-    # splits per (row, KV head), so the combine loops over many batches), one over 40,000,
+    # splits per (row, KV head); with up to 45 decode rows possible in this step the combine
+    # runs one CTA of eight thread groups per (row, KV head)), one over 40,000,
     # and a 300-token prefill chunk on a 70,000-token history (about 550 key tiles per query
     # tile); every row is checked against the oracle
     worst, _, _ = run_all(custom(600, 32, 8, 128, 0, [(131071, 0, 1), (40000, 0, 1),
                                                       (70000, 300, 0)]))
+    assert worst[0] < 2e-2
+
+
+def test_long_row_two_pass_combine():
+    # three decode rows, two steps: 131,071 cached keys (about 820 splits of 10 pages: the
+    # combine merges 64-split chunks, then the chunk states), 3,000 keys (under 64 splits:
+    # finished by the chunk pass) and 100 keys (one split: written by the decode kernel).
+    # The long row's second token opens page 8,192.
+    worst, _, _ = run_all(custom(610, 32, 8, 128, 0, [(131071, 0, 2), (3000, 0, 2),
+                                                      (100, 0, 2)]))
     assert worst[0] < 2e-2
 
 
