@@ -208,6 +208,44 @@ def test_long_row_two_pass_combine():
     assert worst[0] < 2e-2
 
 
+def _tile_rows(plan, per_tile, seed=5):
+    """Rows of every 128-row query tile of every request (its first and last row plus
+    per_tile - 2 seeded picks), so each prefill unit of the step is checked."""
+    rng = np.random.default_rng(seed)
+    pick = set()
+    for j in range(plan.num_reqs):
+        o, n = int(plan.q_offsets[j]), int(plan.q_lens[j])
+        for t0 in range(0, n, 128):
+            t1 = min(n, t0 + 128)
+            pick |= {o + t0, o + t1 - 1}
+            pick |= set((o + rng.integers(t0, t1, size=per_tile - 2)).tolist())
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype,specs", [
+    (32, 8, 128, 0, [(12000, 2018, 0)]),
+    (32, 32, 64, 1, [(12000, 2018, 0)]),
+    (32, 4, 128, 0, [(9000, 1024, 0), (14000, 1024, 0), (3000, 0, 1)]),
+])
+def test_prefill_chunks_on_long_contexts(hq, hkv, d, dtype, specs):
+    # 2K-row chunks over 9K-14K cached keys: 256 prefill CTAs of ~100 key tiles each (GQA
+    # head pairs, MHA query-tile pairs, and two requests beside a decode row).  Sampled rows
+    # of every 128-row query tile against the oracle; a second run gives the same bits.
+    w = custom(620 + hkv + d, hq, hkv, d, dtype, specs)
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    out = runner.run_step(kv, w, plan)
+    again = runner.run_step(kv, w, plan)
+    assert kv.read_error() == 0
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    rows = _tile_rows(plan, 6)
+    mx, mean = assert_close(gpu_as_f64(out[torch.as_tensor(rows)]), oracle_rows(w, plan, rows),
+                            "long-context chunk")
+    print("long-context chunk", hq, hkv, d, dtype, "worst", mx, mean)
+
+
 def test_decode_loop_and_graph_bitwise_identical():
     # the MHA-skew workload's 64 decode steps (16 requests, fp16, page boundaries crossed
     # mid-run) as 64 separate steps, as one device-side loop (lengths advanced on the
