@@ -218,48 +218,53 @@ def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
     dist_ctx.barrier()
     torch.cuda.synchronize()
     with clocks:
-        # repeat the timed region so the clock sampler sees >= ~1 s of load
+        # repeat the timed region so the clock sampler sees >= ~1 s of load.  Each round
+        # times `steps` plain steps (the step rate), then `steps` steps with events around
+        # the decode kernel (its per-launch time): an event recorded between two launches
+        # ends their programmatic overlap, so the plain steps carry none.
         reps = 0
         wall0 = time.time()
         while True:
             t0.record(stream)
             for i in range(steps):
+                one_step()
+            t1.record(stream)
+            for i in range(steps):
                 binding.set_kernel_events(0, kstart[i], kstop[i])
                 one_step()
             binding.set_kernel_events(0, None, None)
-            t1.record(stream)
             torch.cuda.synchronize()
             reps += 1
             if time.time() - wall0 > 1.0 or reps >= 50:
                 break
     dist_ctx.barrier()
-    ms_total = t0.elapsed_time(t1)          # last repetition: exactly `steps` steps
+    ms_total = t0.elapsed_time(t1)          # last round's plain steps: exactly `steps`
     ms_kernel = float(np.mean([a.elapsed_time(b) for a, b in zip(kstart, kstop)]))
     ms_step = dist_ctx.max(ms_total / steps)
     assert kv.read_error() == 0
     acct = step_bytes(w, plan)
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region):
-    #      the step's inputs sit packed in pinned host memory; one H2D copy, append +
-    #      attention, one D2H copy of the output
-    stg = runner.StepStaging(kv)
-    stg.stage(plan, qh, kh, vh)
-    h2d, d2h = stg.h2d_bytes, stg.d2h_bytes
+    #      each step's inputs sit packed in pinned host memory; one H2D copy, append +
+    #      attention, one D2H copy of the output.  Two stagings alternate, so step i+1's
+    #      upload and step i-1's download overlap step i's computation.
+    pipe = runner.StepPipeline(kv, stream)
+    for slot in range(2):
+        pipe.stage(slot, plan, qh, kh, vh)
+    h2d, d2h = pipe.stg[0].h2d_bytes, pipe.stg[0].d2h_bytes
 
-    def e2e_step():
-        stg.upload()
-        stg.run(w.scale, stream)
-        stg.download()
-
-    for _ in range(3):
-        e2e_step()
+    for i in range(4):
+        pipe.launch(i % 2, w.scale)
+    pipe.join()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_ctx.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(steps):
-        e2e_step()
+    pipe.start_after(e0)
+    for i in range(steps):
+        pipe.launch(i % 2, w.scale)
+    pipe.join()
     e1.record(stream)
     torch.cuda.synchronize()
     dist_ctx.barrier()
@@ -296,12 +301,15 @@ def time_decode_int8(device, steps, pool_pages=70000):
     kstart = [lib_event() for _ in range(steps)]
     kstop = [lib_event() for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # plain steps for the step rate, then as many with events around the decode kernel
     t0.record(stream)
+    for i in range(steps):
+        one_step()
+    t1.record(stream)
     for i in range(steps):
         binding.set_kernel_events(0, kstart[i], kstop[i])
         one_step()
     binding.set_kernel_events(0, None, None)
-    t1.record(stream)
     torch.cuda.synchronize()
     assert kv.read_error() == 0
     ms_step = t0.elapsed_time(t1) / steps
@@ -340,19 +348,21 @@ def time_prefill(device, reps=5, kv_int8=False):
             kv.attention(ds, q, w.scale, out)          # warm-up
             torch.cuda.synchronize()
             # `reps` identical steps queued back to back between the events, so the host's
-            # launch latency overlaps device work as it does in a stream of steps; the
-            # kernel events bracket the main kernel of the last step
+            # launch latency overlaps device work as it does in a stream of steps; then one
+            # more step with events around its main kernel (kept out of the timed steps: an
+            # event between two launches ends their programmatic overlap)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ka, kb = lib_event(), lib_event()
-            binding.set_kernel_events(0, ka, kb)
-            binding.set_kernel_events(1, ka, kb)
             a.record()
             for _ in range(reps):
                 kv.attention(ds, q, w.scale, out)
             b.record()
-            torch.cuda.synchronize()
+            binding.set_kernel_events(0, ka, kb)
+            binding.set_kernel_events(1, ka, kb)
+            kv.attention(ds, q, w.scale, out)
             binding.set_kernel_events(0, None, None)
             binding.set_kernel_events(1, None, None)
+            torch.cuda.synchronize()
             total_ms += a.elapsed_time(b) / reps
             main_ms += ka.elapsed_time(kb)
         assert kv.read_error() == 0
@@ -623,7 +633,9 @@ def main():
                          "traffic": captured_traffic("decode_kernel")},
             "e2e": {"value": acct["step"] * dist_ctx.world / (r["ms_e2e"] * 1e-3) / 1e9,
                     "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
-                    "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["ms_e2e"]},
+                    "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["ms_e2e"],
+                    "copies": "pinned host buffers; two alternating stagings, so a step's "
+                              "upload and download overlap its neighbours' computation"},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }

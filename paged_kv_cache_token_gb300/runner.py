@@ -235,6 +235,73 @@ class StepStaging:
         self.out_host.copy_(self.out, non_blocking=True)
 
 
+class StepPipeline:
+    """Consecutive steps through two stagings, with the copies on their own streams.
+
+    Step i uses staging i % 2.  Its upload (on the H2D stream) waits only for the last
+    step that read that staging's device inputs, so it runs while the previous step
+    computes; its append + attention (on the compute stream) wait for its upload and for
+    the staging's previous download; its download (on the D2H stream) waits for its own
+    computation and overlaps the next step's.  Every step still moves its whole input up
+    and its whole output down.
+
+    ``stage(slot, ...)`` fills a staging's pinned input buffer (waiting first for that
+    staging's previous upload), ``launch(slot, scale)`` enqueues the step and ``result(slot)``
+    waits for its download and returns the pinned host output, valid until the slot's next
+    ``launch``.
+    """
+
+    def __init__(self, kv: PagedKV, compute_stream=None):
+        self.kv = kv
+        self.stg = [StepStaging(kv), StepStaging(kv)]
+        self.compute = compute_stream or torch.cuda.current_stream(kv.device)
+        self.h2d = torch.cuda.Stream(device=kv.device)
+        self.d2h = torch.cuda.Stream(device=kv.device)
+        self.uploaded = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.downloaded = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+
+    def stage(self, slot: int, plan: StepPlan, q_bits: np.ndarray, k_bits: np.ndarray,
+              v_bits: np.ndarray) -> None:
+        if self.used[slot]:
+            self.uploaded[slot].synchronize()
+        self.stg[slot].stage(plan, q_bits, k_bits, v_bits)
+
+    def start_after(self, event: torch.cuda.Event) -> None:
+        """Order the copy streams after ``event`` (e.g. the start of a timed region)."""
+        self.h2d.wait_event(event)
+        self.d2h.wait_event(event)
+
+    def launch(self, slot: int, scale: float) -> None:
+        s = self.stg[slot]
+        with torch.cuda.stream(self.h2d):
+            if self.used[slot]:
+                self.h2d.wait_event(self.computed[slot])
+            s.upload()
+            self.uploaded[slot].record(self.h2d)
+        self.compute.wait_event(self.uploaded[slot])
+        if self.used[slot]:
+            self.compute.wait_event(self.downloaded[slot])
+        s.run(scale, self.compute)
+        self.computed[slot].record(self.compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.computed[slot])
+            s.download()
+            self.downloaded[slot].record(self.d2h)
+        self.used[slot] = True
+
+    def join(self) -> None:
+        """Make the compute stream wait for every download launched so far."""
+        for slot in range(2):
+            if self.used[slot]:
+                self.compute.wait_event(self.downloaded[slot])
+
+    def result(self, slot: int) -> torch.Tensor:
+        self.downloaded[slot].synchronize()
+        return self.stg[slot].out_host
+
+
 class DecodeLoop:
     """Consecutive steps of one batch run as one device-side sequence.
 

@@ -157,19 +157,22 @@ def test_prefill_chunks_small(hq, hkv, d, dtype):
 
 def test_step_staging_bitwise_identical():
     # the packed one-copy staging (inputs in one pinned buffer, device views into one
-    # device buffer) gives the same output bits and pool bytes as separate uploads, over
-    # decode steps, prefill chunks and mixed steps
+    # device buffer), alone and as the two-staging pipeline whose copies run on their own
+    # streams beside the neighbouring steps, gives the same output bits and pool bytes as
+    # separate uploads, over decode steps, prefill chunks and mixed steps
     w = custom(500, 8, 2, 128, 0, [(40, 0, 3), (0, 70, 1), (300, 0, 2), (0, 20, 2)],
                budget=48)
     results = []
-    for staged in (False, True):
+    for mode in ("separate", "staged", "pipelined"):
         s = scheduler_for(w)
         kv = runner.paged_kv_for(w)
         runner.load_history(kv, w, s.history_plan())
         stg = runner.StepStaging(kv)
+        pipe = runner.StepPipeline(kv)
         outs = []
-        for plan in s.all_steps():
-            if staged:
+        plans = s.all_steps()
+        for i, plan in enumerate(plans):
+            if mode == "staged":
                 stg.stage(plan, *runner.step_host_inputs(w, plan))
                 stg.upload()
                 stg.run(w.scale)
@@ -177,14 +180,23 @@ def test_step_staging_bitwise_identical():
                 torch.cuda.synchronize()
                 # the pinned output buffer is reused by the next step: keep a copy
                 outs.append(runner.tensor_to_bits(stg.out_host).copy())
+            elif mode == "pipelined":
+                pipe.stage(i % 2, plan, *runner.step_host_inputs(w, plan))
+                pipe.launch(i % 2, w.scale)
+                if i > 0:  # the previous step's output, before its staging is reused
+                    outs.append(runner.tensor_to_bits(pipe.result((i - 1) % 2)).copy())
             else:
                 outs.append(runner.tensor_to_bits(runner.run_step(kv, w, plan)))
+        if mode == "pipelined":
+            outs.append(runner.tensor_to_bits(pipe.result((len(plans) - 1) % 2)).copy())
+        torch.cuda.synchronize()
         assert kv.read_error() == 0
         results.append((outs, pool_bits(kv)))
-    assert len(results[0][0]) == len(results[1][0]) > 2
-    for a, b in zip(results[0][0], results[1][0]):
-        assert np.array_equal(a, b)
-    assert all(np.array_equal(a, b) for a, b in zip(results[0][1], results[1][1]))
+    for other in results[1:]:
+        assert len(results[0][0]) == len(other[0]) > 2
+        for a, b in zip(results[0][0], other[0]):
+            assert np.array_equal(a, b)
+        assert all(np.array_equal(a, b) for a, b in zip(results[0][1], other[1]))
 
 
 def test_long_contexts():
