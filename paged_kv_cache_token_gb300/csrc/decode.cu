@@ -17,9 +17,15 @@
 // mma.sync tensor-core contractions (16 tokens x 8 head columns); an online softmax in base-2
 // units keeps (running max, running sum, un-normalised output) per query head; the weighted
 // sum over the page's values runs on the FP32 pipes for 16-bit pages (FFMA2 over V rows)
-// and on the tensor cores for INT8 pages.  A row with one split is normalised and written directly; otherwise each
-// split leaves its partial (m, l, O) in a fixed slot and the combine kernel reduces them:
-// m* = max m_s, l* = sum l_s 2^(m_s - m*), O = sum O_s 2^(m_s - m*) / l*.
+// and on the tensor cores for INT8 pages.  A row with one split is normalised and written
+// directly; otherwise each split leaves its partial (m, l, O) in a fixed slot and the
+// combine kernel reduces them: m* = max m_s, l* = sum l_s 2^(m_s - m*),
+// O = sum O_s 2^(m_s - m*) / l* (in two passes over 64-split chunks for long rows).
+//
+// The plan kernel builds the step's work lists on the device: the split size from the
+// total decode pages, row records by one warp per request, item records one per thread
+// over the whole grid (a single long row has thousands), prefill tile records longest
+// first.
 #include <algorithm>
 #include <climits>
 #include <type_traits>
