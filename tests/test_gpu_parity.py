@@ -10,7 +10,7 @@ from paged_kv_cache_token_gb300 import binding, build, runner
 from paged_kv_cache_token_gb300 import workloads as W
 from paged_kv_cache_token_gb300.scheduler import PagePool, Scheduler, make_plan, scheduler_for
 
-from gpu_common import assert_close, gpu_as_f64, oracle_rows, pool_bits
+from gpu_common import assert_close, gpu_as_f64, oracle_rows, oracle_rows_int8, pool_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -197,6 +197,44 @@ def test_step_staging_bitwise_identical():
         for a, b in zip(results[0][0], other[0]):
             assert np.array_equal(a, b)
         assert all(np.array_equal(a, b) for a, b in zip(results[0][1], other[1]))
+
+
+@pytest.mark.parametrize("kv_int8", [False, True])
+def test_ragged_step_with_idle_requests(kv_int8):
+    # one launch mixing requests that do not advance (q_len 0, with and without cached
+    # keys) with rows on both sides of the decode/prefill switch (15 rows stay on the
+    # streaming path, 16 and 17 take the tensor-core tiles), two-row decodes and a decode
+    # at a page edge: every row against the oracle; no page of an idle request changes
+    specs = [(50, 0, 0), (33, 15, 0), (0, 16, 0), (16, 1, 0), (0, 0, 0), (127, 17, 0),
+             (31, 0, 0), (200, 2, 0)]
+    w = custom(640, 8, 2, 128, 0, specs)
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, kv_int8=kv_int8)
+    runner.load_history(kv, w, s.history_plan())
+    step = s.next_step()
+    got = {int(r): j for j, r in enumerate(step.rids)}
+    rids, q_lens, ctx, tables = [], [], [], []
+    for r, spec in enumerate(specs):
+        rids.append(r)
+        if r in got:
+            j = got[r]
+            q_lens.append(int(step.q_lens[j]))
+            ctx.append(int(step.context_lens[j]))
+            tables.append([p for p in step.block_table[j].tolist() if p >= 0])
+        else:
+            q_lens.append(0)
+            ctx.append(spec[0])
+            tables.append(list(s.reqs[r].pages))
+    assert q_lens == [0, 15, 16, 1, 0, 17, 0, 2]
+    plan = make_plan(rids, q_lens, ctx, tables)
+    idle_pages = [p for r in (0, 6) for p in tables[r]]
+    before = [b[idle_pages].copy() for b in pool_bits(kv)]
+    out = runner.run_step(kv, w, plan)
+    assert kv.read_error() == 0
+    assert all(np.array_equal(b[idle_pages], a) for b, a in zip(pool_bits(kv), before))
+    ref = oracle_rows_int8(w, plan) if kv_int8 else oracle_rows(w, plan)
+    assert out.shape[0] == sum(q_lens)
+    assert_close(gpu_as_f64(out), ref, "ragged step")
 
 
 def test_long_contexts():
