@@ -920,16 +920,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 // a batch of splits are independent, so they overlap -- and the groups' states are then
 // merged through shared memory:
 //   m* = max_s m_s,  l* = sum_s l_s 2^(m_s - m*),  acc* = sum_s O_s 2^(m_s - m*)
-// (m in log2 units, O unnormalised).  Three launch shapes:
-//   kCombineRow     one CTA per (row, KV head), NG = 1: every row of a step whose rows have
-//                   at most kManySplits splits.
+// (m in log2 units, O unnormalised).  The launch shapes:
+//   kCombineRow     one CTA per (row, KV head): NG = 1 when no row can have more than
+//                   kManySplits splits; NG groups when rows can be long but there are too
+//                   many of them for the chunked form.
 //   kCombineChunks  CTA (row x KV head, c) merges splits [64c, 64c + 64) into the slot of
 //                   split 64c -- the merged state has the same (m, l, O) form as a split --
 //                   or, for a row with at most 64 splits, writes the row's output.
 //   kCombineParts   one CTA per (row, KV head) with more than 64 splits merges its chunk
 //                   states (stride 64) into the output.
-// The last two serve a long context on few rows, where one CTA per (row, KV head) would
-// read megabytes of partials at a single SM's bandwidth.
+// The chunked pair serves a long context on few rows, where one CTA per (row, KV head)
+// would read megabytes of partials at a single SM's bandwidth.
 // ------------------------------------------------------------------------------------
 enum : int { kCombineRow = 0, kCombineChunks = 1, kCombineParts = 2 };
 constexpr int kCombineChunk = 64;
@@ -1036,6 +1037,8 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
     if constexpr (Stage == kCombineRow) {
         combine_fold<T, D, G, NG>(a, base, 0, ns, 1, true, row.x, g, s_ml, s_acc);
     } else if constexpr (Stage == kCombineChunks) {
+        // the in-place chunk write relies on the barrier between the groups' reads and it
+        static_assert(NG > 1, "the chunk pass needs more than one thread group");
         const int nch = cdiv(ns, kCombineChunk);
         for (int c = blockIdx.y; c < nch; c += gridDim.y) {  // uniform over the CTA
             const int first = c * kCombineChunk;
