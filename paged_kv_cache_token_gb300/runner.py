@@ -1,7 +1,13 @@
 """Device-side driver for a sequence of steps: page pools, per-step metadata upload and
 the two C-ABI calls (append, then attention), all through :mod:`binding`.
 
-This is host plumbing around the library (allocation, copies, stream), the same thing a
+* :class:`PagedKV` -- the page pools (16-bit or INT8), the error flag and the workspace;
+* :class:`StepStaging` -- a step's inputs packed into one pinned buffer, one copy each way;
+* :class:`StepPipeline` -- two stagings alternating, copies on their own streams, so a
+  step's transfers overlap its neighbours' computation;
+* :class:`DecodeLoop` -- consecutive decode steps advanced on the device, one CUDA graph.
+
+This is host plumbing around the library (allocation, copies, streams), the same thing a
 serving engine does around its attention backend.  It holds no attention arithmetic.
 """
 from __future__ import annotations
