@@ -59,7 +59,8 @@ typedef enum { PKV_BF16 = 0, PKV_FP16 = 1 } pkv_dtype;
 typedef enum {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARG = -1,     /* null pointer, negative size, page_size != 16, ... */
-    PKV_ERR_UNSUPPORTED = -2,     /* head_dim not 64/128, Hq % Hkv != 0, group > 8, dtype */
+    PKV_ERR_UNSUPPORTED = -2,     /* head_dim not 64/128, Hq % Hkv != 0, group > 8, dtype,
+                                     a pool of 2^31 or more (page, KV head, token) rows */
     PKV_ERR_CAPACITY = -3,        /* max_context_len + max_q_len beyond the block table */
     PKV_ERR_WORKSPACE = -4,       /* workspace NULL or smaller than required */
     PKV_ERR_CUDA = -5,            /* a CUDA runtime call or launch failed */
@@ -89,7 +90,7 @@ typedef struct {
     int32_t num_kv_heads;        /* Hkv, Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8} */
     int32_t head_dim;            /* D in {64, 128} */
     int32_t page_size;           /* must be 16 */
-    int32_t num_pages;           /* pages in each pool */
+    int32_t num_pages;           /* pages in each pool; num_pages * Hkv * 16 < 2^31 */
     int32_t max_pages_per_req;   /* block_table row stride */
     int32_t total_q_tokens;      /* T = sum of q_lens */
     int32_t max_q_len;

@@ -51,6 +51,10 @@ int check_desc(const pkv_step_desc* d) {
     if (static_cast<int64_t>(d->num_pages) * d->num_kv_heads * 16 * d->head_dim >
         (int64_t(1) << 40))
         return PKV_ERR_INVALID_ARG;
+    // the prefill's tensor maps address pool rows (page x KV head x 16 tokens) with 32-bit
+    // coordinates
+    if (static_cast<int64_t>(d->num_pages) * d->num_kv_heads * 16 > INT_MAX)
+        return PKV_ERR_UNSUPPORTED;
     if (d->num_reqs > 0 &&
         (!d->q_lens || !d->q_offsets || !d->context_lens || !d->block_table))
         return PKV_ERR_INVALID_ARG;

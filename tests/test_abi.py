@@ -61,6 +61,7 @@ def _desc(**kw):
     (dict(num_reqs=0, total_q_tokens=5), -1),
     (dict(max_q_len=100, total_q_tokens=100), -3),  # 100 tokens > 4 pages x 16
     (dict(q_lens=None), -1),
+    (dict(num_pages=1 << 26), -2),             # 2^26 pages x 2 heads x 16 = 2^31 pool rows
 ])
 def test_host_validation_rejects_before_launch(lib, kw, code):
     d = _desc(**kw)
