@@ -1023,32 +1023,33 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
     __shared__ float2 s_ml[NG > 1 ? NG : 1][TPG];
     __shared__ float4 s_acc[NG > 1 ? NG : 1][TPG];
     const int Hkv = a.num_kv_heads;
-    const int d = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
-    // the row records come from the plan, which completed before the decode kernel let this
-    // grid launch: read them before waiting for the decode kernel's partials
     const int32_t* ctrl = ws_at<const int32_t>(a, a.lay.ctrl);
-    const int nrows = ctrl[2];
-    const int4 row = ws_at<const int4>(a, a.lay.rows)[d];  // {token, first slot, keys, splits}
+    const int4* rows = ws_at<const int4>(a, a.lay.rows);  // {token, first slot, keys, splits}
     pdl_wait();  // the previous grid (decode kernel or chunk pass) has finished its writes
-    if (d >= nrows) return;
-    const int ns = row.w;
-    if (ns <= 1) return;  // finished in place by the decode kernel
-    const int64_t base = row.y + static_cast<int64_t>(g) * ns;
-    if constexpr (Stage == kCombineRow) {
-        combine_fold<T, D, G, NG>(a, base, 0, ns, 1, true, row.x, g, s_ml, s_acc);
-    } else if constexpr (Stage == kCombineChunks) {
-        // the in-place chunk write relies on the barrier between the groups' reads and it
-        static_assert(NG > 1, "the chunk pass needs more than one thread group");
-        const int nch = cdiv(ns, kCombineChunk);
-        for (int c = blockIdx.y; c < nch; c += gridDim.y) {  // uniform over the CTA
-            const int first = c * kCombineChunk;
-            combine_fold<T, D, G, NG>(a, base, first, min(kCombineChunk, ns - first), 1,
-                                      nch == 1, row.x, g, s_ml, s_acc);
+    // the grid is capped from host bounds; CTAs walk the step's actual (row, KV head) pairs
+    const int nrh = ctrl[2] * Hkv;
+    for (int rh = blockIdx.x; rh < nrh; rh += gridDim.x) {  // uniform over the CTA
+        const int d = rh / Hkv, g = rh % Hkv;
+        const int4 row = rows[d];
+        const int ns = row.w;
+        if (ns <= 1) continue;  // finished in place by the decode kernel
+        const int64_t base = row.y + static_cast<int64_t>(g) * ns;
+        if constexpr (Stage == kCombineRow) {
+            combine_fold<T, D, G, NG>(a, base, 0, ns, 1, true, row.x, g, s_ml, s_acc);
+        } else if constexpr (Stage == kCombineChunks) {
+            // the in-place chunk write relies on the barrier between the groups' reads and it
+            static_assert(NG > 1, "the chunk pass needs more than one thread group");
+            const int nch = cdiv(ns, kCombineChunk);
+            for (int c = blockIdx.y; c < nch; c += gridDim.y) {  // uniform over the CTA
+                const int first = c * kCombineChunk;
+                combine_fold<T, D, G, NG>(a, base, first, min(kCombineChunk, ns - first), 1,
+                                          nch == 1, row.x, g, s_ml, s_acc);
+            }
+        } else {
+            if (ns <= kCombineChunk) continue;  // written by the chunk pass
+            combine_fold<T, D, G, NG>(a, base, 0, cdiv(ns, kCombineChunk), kCombineChunk,
+                                      true, row.x, g, s_ml, s_acc);
         }
-    } else {
-        if (ns <= kCombineChunk) return;  // written by the chunk pass
-        combine_fold<T, D, G, NG>(a, base, 0, cdiv(ns, kCombineChunk), kCombineChunk, true,
-                                  row.x, g, s_ml, s_acc);
     }
 }
 
@@ -1132,19 +1133,22 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
     constexpr int kTpg = G * D / 4, kNg = std::min(8, 1024 / kTpg);
     const int max_splits = cdiv(cdiv(a.max_context_len + a.max_q_len, kPage), kMinSplitPages);
     const int rows_heads = std::max(1, a.lay.max_rows * a.num_kv_heads);
+    // grids capped near a full wave: a host bound on rows can be far above the step's rows
+    const int cap_small = std::min(rows_heads, 16 * a.num_sms);  // 128-thread CTAs
+    const int cap_big = std::min(rows_heads, 2 * a.num_sms);     // up to 1,024 threads
     const int chunks = cdiv(max_splits, kCombineChunk);
     cudaError_t e;
     if (max_splits <= kManySplits) {
-        e = launch_pdl(combine_kernel<T, D, G, 1, kCombineRow>, dim3(rows_heads), dim3(kTpg), 0,
+        e = launch_pdl(combine_kernel<T, D, G, 1, kCombineRow>, dim3(cap_small), dim3(kTpg), 0,
                        stream, a);
     } else if (static_cast<long long>(rows_heads) * chunks <= kChunkedCtas) {
-        e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineChunks>, dim3(rows_heads, chunks),
+        e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineChunks>, dim3(cap_big, chunks),
                        dim3(kTpg * kNg), 0, stream, a);
         if (e == cudaSuccess)
-            e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineParts>, dim3(rows_heads),
+            e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineParts>, dim3(cap_big),
                            dim3(kTpg * kNg), 0, stream, a);
     } else {
-        e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineRow>, dim3(rows_heads),
+        e = launch_pdl(combine_kernel<T, D, G, kNg, kCombineRow>, dim3(cap_big),
                        dim3(kTpg * kNg), 0, stream, a);
     }
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
