@@ -28,7 +28,7 @@ DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16}
 EXPORTED = ("pkv_kv_append", "pkv_advance_context", "pkv_attention_workspace_bytes",
             "pkv_paged_attention_step", "pkv_kv_append_int8",
             "pkv_attention_workspace_bytes_int8", "pkv_paged_attention_step_int8",
-            "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
+            "pkv_paged_attention_step_static_ws", "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
             "pkv_version")
 
 
@@ -82,6 +82,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_attention_step_int8.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V,
                                                   ctypes.c_float, V, sz, V, V]
     lib.pkv_paged_attention_step_int8.restype = ctypes.c_int
+    lib.pkv_paged_attention_step_static_ws.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V,
+                                                       ctypes.c_float, V, V]
+    lib.pkv_paged_attention_step_static_ws.restype = ctypes.c_int
     lib.pkv_read_device_error.argtypes = [V, ctypes.POINTER(ctypes.c_int32), V]
     lib.pkv_read_device_error.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -203,13 +206,9 @@ def paged_attention_step_static_ws(desc: StepDesc, q, k_cache, v_cache, out, sca
                                    err=None, stream=None, check: bool = True) -> int:
     """The attention step with the library's built-in scratch array instead of a caller
     workspace (for callers that cannot allocate device memory at call time)."""
-    lib = load()
-    fn = lib.pkv_paged_attention_step_static_ws
-    fn.argtypes = [ctypes.POINTER(StepDesc), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                   ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
-    rc = fn(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), float(scale),
-            _ptr(err), _stream(stream))
+    rc = load().pkv_paged_attention_step_static_ws(ctypes.byref(desc), _ptr(q), _ptr(k_cache),
+                                                   _ptr(v_cache), _ptr(out), float(scale),
+                                                   _ptr(err), _stream(stream))
     if check and rc != OK:
         raise PkvError("pkv_paged_attention_step_static_ws", rc)
     return rc

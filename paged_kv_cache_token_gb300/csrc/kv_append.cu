@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
     const int tok0 = blockIdx.x * kTokPerBlock;
     if (tok0 >= qlen) return;
     if (__ldg(a.q_offsets + r + 1) - start != qlen || ctx < 0 || qlen > a.max_q_len ||
-        start + qlen > a.total_q_tokens) {
+        start < 0 || start + qlen > a.total_q_tokens) {
         if (threadIdx.x == 0) set_error(a.err, PKV_DEVERR_TOKENS);
         return;
     }
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendArgs a) {
     const int tok0 = blockIdx.x * kTokPerBlock;
     if (tok0 >= qlen) return;
     if (__ldg(a.q_offsets + r + 1) - start != qlen || ctx < 0 || qlen > a.max_q_len ||
-        start + qlen > a.total_q_tokens) {
+        start < 0 || start + qlen > a.total_q_tokens) {
         if (threadIdx.x == 0) set_error(a.err, PKV_DEVERR_TOKENS);
         return;
     }

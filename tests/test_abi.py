@@ -71,6 +71,10 @@ def test_host_validation_rejects_before_launch(lib, kw, code):
                                       None)
     assert rc == code
     assert lib.pkv_attention_workspace_bytes(ctypes.byref(d)) == 0
+    # the built-in-scratch entry point reports description errors the same way
+    rc = lib.pkv_paged_attention_step_static_ws(ctypes.byref(d), None, None, None, None, 1.0,
+                                                None, None)
+    assert rc == code
 
 
 @pytest.mark.parametrize("kw,code", [

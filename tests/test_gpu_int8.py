@@ -284,3 +284,26 @@ def test_int8_bad_pages_set_flags_and_skip():
     q = torch.zeros((5, 1, 64), dtype=torch.bfloat16, device="cuda")
     kv.attention(ds, q, 0.125)
     assert kv.read_error() & binding.DEVERR_PAGE_RANGE
+
+
+def test_int8_append_negative_offsets_flagged_and_skipped():
+    # request 1 starts at token row -1 with a length that matches its offsets: refused like
+    # request 0, whose length disagrees; no code or slot id is written
+    from paged_kv_cache_token_gb300.scheduler import make_plan
+    plan = make_plan([0, 1], [1, 1], [0, 0], [[0], [1]])
+    sc = np.full((1, 64), 0.03, np.float32)
+    kv = runner.PagedKV(4, 1, 1, 64, 0, k_scale=sc, v_scale=sc)
+    ds = kv.upload(plan)
+    qo = torch.tensor([0, -1, 0], dtype=torch.int32, device="cuda")
+    desc = binding.make_desc(num_reqs=2, num_q_heads=1, num_kv_heads=1, head_dim=64,
+                             num_pages=4, max_pages_per_req=plan.max_pages, total_q_tokens=2,
+                             max_q_len=1, max_context_len=0, dtype=0, q_lens=ds.tensors[0],
+                             q_offsets=qo, context_lens=ds.tensors[2],
+                             block_table=ds.tensors[3])
+    k = torch.ones((2, 1, 64), dtype=torch.bfloat16, device="cuda")
+    slots = torch.full((2,), -7, dtype=torch.int64, device="cuda")
+    kv.append_desc(desc, k, k, slots)
+    assert kv.read_error() & binding.DEVERR_TOKENS
+    assert bool((kv.k_cache == runner.INT8_SENTINEL).all())
+    assert bool((kv.v_cache == runner.INT8_SENTINEL).all())
+    assert slots.cpu().tolist() == [-7, -7]

@@ -115,6 +115,28 @@ def test_append_bad_page_sets_flag_and_skips():
     assert np.all(gk[1:] == 0xFFFF)
 
 
+def test_append_negative_offsets_flagged_and_skipped():
+    # q_offsets = [0, -1, 0]: request 0's length disagrees with its offsets, and request 1
+    # starts at token row -1 although its own length (1) matches.  Both must be refused:
+    # the flag gets the token bit and no page slot or slot id changes.
+    plan = make_plan([0, 1], [1, 1], [0, 0], [[0], [1]])
+    kv = runner.PagedKV(4, 1, 1, 64, 0)
+    ds = kv.upload(plan)
+    qo = torch.tensor([0, -1, 0], dtype=torch.int32, device="cuda")
+    desc = binding.make_desc(num_reqs=2, num_q_heads=1, num_kv_heads=1, head_dim=64,
+                             num_pages=4, max_pages_per_req=plan.max_pages, total_q_tokens=2,
+                             max_q_len=1, max_context_len=0, dtype=0, q_lens=ds.tensors[0],
+                             q_offsets=qo, context_lens=ds.tensors[2],
+                             block_table=ds.tensors[3])
+    k = torch.zeros((2, 1, 64), dtype=torch.bfloat16, device="cuda")
+    slots = torch.full((2,), -7, dtype=torch.int64, device="cuda")
+    kv.append_desc(desc, k, k, slots)
+    assert kv.read_error() & binding.DEVERR_TOKENS
+    gk, gv = pool_bits(kv)
+    assert np.all(gk == 0xFFFF) and np.all(gv == 0xFFFF)
+    assert slots.cpu().tolist() == [-7, -7]
+
+
 # ------------------------------------------------------------------------------ attention
 def test_tiny_all_steps():
     run_all(W.tiny())

@@ -89,17 +89,32 @@ def test_static_workspace_repeated_call_same_step():
     assert kv.read_error() == 0
 
 
-def test_static_workspace_rejects_steps_beyond_its_size():
-    # 4,096 decode rows over 100,000-token contexts need more split-KV scratch than the
-    # 16 MiB array holds: refused on the host before anything is launched
+def _big_desc(num_pages):
+    # 4,096 decode rows over 100,000-token contexts: the split-KV scratch this needs does
+    # not depend on the pool size, only on the rows, heads and context lengths
     n, ctx = 4096, 100_000
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     desc = binding.make_desc(num_reqs=n, num_q_heads=32, num_kv_heads=8, head_dim=128,
-                             num_pages=n * (ctx // 16 + 1), max_pages_per_req=ctx // 16 + 1,
+                             num_pages=num_pages, max_pages_per_req=ctx // 16 + 1,
                              total_q_tokens=n, max_q_len=1, max_context_len=ctx, dtype=W.BF16,
                              q_lens=dummy, q_offsets=dummy, context_lens=dummy,
                              block_table=dummy)
+    return desc, dummy
+
+
+def test_static_workspace_rejects_steps_beyond_its_size():
+    # more scratch than the 16 MiB array holds: refused on the host, nothing launched
+    desc, dummy = _big_desc(num_pages=1024)
     assert binding.attention_workspace_bytes(desc) > binding.STATIC_WORKSPACE_BYTES
     rc = binding.paged_attention_step_static_ws(desc, dummy, dummy, dummy, dummy, 1.0,
                                                 check=False)
-    assert rc == -4  # PKV_ERR_WORKSPACE, nothing launched
+    assert rc == -4  # PKV_ERR_WORKSPACE
+
+
+def test_static_workspace_passes_description_errors_through():
+    # a pool of 2^31 (page, KV head, token) rows is not supported by either entry point
+    desc, dummy = _big_desc(num_pages=1 << 24)
+    assert binding.attention_workspace_bytes(desc) == 0
+    rc = binding.paged_attention_step_static_ws(desc, dummy, dummy, dummy, dummy, 1.0,
+                                                check=False)
+    assert rc == -2  # PKV_ERR_UNSUPPORTED
