@@ -240,6 +240,15 @@ def test_int8_decode_loop_graph_bitwise_identical():
     assert kv.read_error() == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(kv.k_cache, ref_pool[0]) and torch.equal(kv.v_cache, ref_pool[1])
+    for i in (0, 31, 63):  # the replayed steps against the oracle directly
+        assert_close(gpu_as_f64(out[i]), oracle_rows_int8(w, plans[i]), "graph step %d" % i)
+    # the device loop launched call by call, against the oracle too
+    s, kv = fresh()
+    out = runner.DecodeLoop(kv, w, plans).run()
+    torch.cuda.synchronize()
+    assert kv.read_error() == 0
+    for i in (0, 31, 63):
+        assert_close(gpu_as_f64(out[i]), oracle_rows_int8(w, plans[i]), "loop step %d" % i)
 
 
 def test_int8_mha_prefill_tile_pairs():
