@@ -200,10 +200,22 @@ def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
                       device=device)
     ws = kv.workspace(ds.desc)
     stream = torch.cuda.current_stream()
+    # a second, disjoint copy of the pools: consecutive steps alternate between the two, so
+    # no step finds the previous step's K/V (613 MB, about 5x L2) in L2 -- the same effect as
+    # flushing L2 between steps, without a flush kernel inside the timed region
+    kv2 = runner.PagedKV(kv.num_pages, kv.hq, kv.hkv, kv.d, kv.dtype_code, device,
+                         fill_sentinel=False)
+    kv2.k_cache.copy_(kv.k_cache)
+    kv2.v_cache.copy_(kv.v_cache)
+    kv2.err = kv.err
+    pools = (kv, kv2)
+    parity = [0]
 
     def one_step():
-        binding.kv_append(ds.desc, k_new, v_new, kv.k_cache, kv.v_cache, None, kv.err, stream)
-        binding.paged_attention_step(ds.desc, q, kv.k_cache, kv.v_cache, out, w.scale, ws,
+        p = pools[parity[0]]
+        parity[0] ^= 1
+        binding.kv_append(ds.desc, k_new, v_new, p.k_cache, p.v_cache, None, kv.err, stream)
+        binding.paged_attention_step(ds.desc, q, p.k_cache, p.v_cache, out, w.scale, ws,
                                      kv.err, stream)
 
     for _ in range(max(3, warmup)):
@@ -245,32 +257,47 @@ def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
     acct = step_bytes(w, plan)
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region):
-    #      each step's inputs sit packed in pinned host memory; one H2D copy, append +
-    #      attention, one D2H copy of the output.  Two stagings alternate, so step i+1's
-    #      upload and step i-1's download overlap step i's computation.
-    pipe = runner.StepPipeline(kv, stream)
+    #      each step's inputs sit in pinned host memory; one H2D copy, append + attention,
+    #      one D2H copy of the output.  Two stagings alternate (and with them the two pools),
+    #      so step i+1's upload and step i-1's download overlap step i's computation.  A
+    #      second run also packs every step's inputs from the caller's numpy arrays into the
+    #      pinned buffer inside the timed region (host time the GPU waits for when the host
+    #      is slower than the step).
+    pipe = runner.StepPipeline(kv, stream, kv_alt=kv2)
     for slot in range(2):
         pipe.stage(slot, plan, qh, kh, vh)
     h2d, d2h = pipe.stg[0].h2d_bytes, pipe.stg[0].d2h_bytes
-
     for i in range(4):
         pipe.launch(i % 2, w.scale)
     pipe.join()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dist_ctx.barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    pipe.start_after(e0)
-    for i in range(steps):
-        pipe.launch(i % 2, w.scale)
-    pipe.join()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    dist_ctx.barrier()
-    ms_e2e = dist_ctx.max(e0.elapsed_time(e1) / steps)
+
+    def e2e_run(pack):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        pack_s = 0.0
+        e0.record(stream)
+        pipe.start_after(e0)
+        for i in range(steps):
+            if pack:
+                h0 = time.perf_counter()
+                pipe.stage(i % 2, plan, qh, kh, vh)
+                pack_s += time.perf_counter() - h0
+            pipe.launch(i % 2, w.scale)
+        pipe.join()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist_ctx.barrier()
+        return dist_ctx.max(e0.elapsed_time(e1) / steps), pack_s * 1e3 / steps
+
+    ms_e2e, _ = e2e_run(False)
+    ms_e2e_pack, host_pack_ms = e2e_run(True)
+    assert kv.read_error() == 0
+    del kv2, pipe
     return dict(w=w, plan=plan, acct=acct, ms_step=ms_step, ms_kernel=ms_kernel, ms_e2e=ms_e2e,
-                h2d=h2d, d2h=d2h, clocks=clocks.summary(), launches=4 * steps)
+                h2d=h2d, d2h=d2h, clocks=clocks.summary(), launches=4 * steps,
+                host_pack_ms=host_pack_ms, ms_e2e_pack=ms_e2e_pack)
 
 
 def time_decode_int8(device, steps, pool_pages=70000):
@@ -464,6 +491,54 @@ def time_decode_loop(device, reps=5):
     return res
 
 
+def time_decode_loop_layers(device, n_layers=4, reps=5):
+    """The MHA-skew workload's 64 decode steps over ``n_layers`` layers, each layer with its
+    own page pools (one layer's cache is ~93 MB, so four of them do not fit in the 129 MB
+    L2): per step, every layer's append + attention, then the lengths advance on the device;
+    the whole sequence is one CUDA graph, so per-layer steps read their K/V from HBM.  Timed
+    twice: every layer planning its own step (pkv_paged_attention_step), and one plan per
+    step shared by the layers (pkv_plan_attention + pkv_paged_attention_run)."""
+    from paged_kv_cache_token_gb300 import runner
+    w = W.mha_skew()
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, device=device, fill_sentinel=False)
+    runner.load_history(kv, w, s.history_plan())
+    plans = s.all_steps()
+    nbytes = sum(step_bytes(w, p)["step"] for p in plans)
+    extra = []
+    for _ in range(n_layers - 1):
+        p = runner.PagedKV(kv.num_pages, kv.hq, kv.hkv, kv.d, kv.dtype_code, device,
+                           fill_sentinel=False)
+        p.k_cache.copy_(kv.k_cache)
+        p.v_cache.copy_(kv.v_cache)
+        p.err = kv.err
+        extra.append((p, w))
+    stream = torch.cuda.current_stream()
+    res = {"layers": n_layers, "steps": len(plans), "bytes_per_layer_step": nbytes / len(plans)}
+    for name, shared in (("plan_per_layer", False), ("shared_plan", True)):
+        loop = runner.DecodeLoop(kv, w, plans, layers=extra, shared_plan=shared)
+        loop.capture()
+        for _ in range(2):
+            loop.replay()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            loop.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b))
+        ms = float(np.median(t))
+        res[name] = {"us_per_layer_step": ms * 1e3 / (len(plans) * n_layers),
+                     "GBps": nbytes * n_layers / (ms * 1e-3) / 1e9}
+        del loop
+    assert kv.read_error() == 0
+    del extra, kv
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------------------ oracle arm
 def oracle_decode_sample(n_req, min_seconds=0.0):
     """Time the fp64 oracle on the first n_req decode rows of the decode workload (all 32
@@ -605,7 +680,8 @@ def main():
             return
         if args.only == "decode-loop":
             if dist_ctx.rank == 0:
-                print(json.dumps({"decode_loop": time_decode_loop(device)}))
+                print(json.dumps({"decode_loop": time_decode_loop(device),
+                                  "layers_from_hbm": time_decode_loop_layers(device)}))
             return
         r = time_decode(device, args.steps, args.warmup, dist_ctx, args.pool_pages)
         acct = r["acct"]
@@ -622,8 +698,10 @@ def main():
                                    "%d-page permuted pool (kv_append + paged_attention_step)"
                                    % args.pool_pages,
                        "kv_bytes_per_step": acct["kv"], "step_bytes": acct["step"],
-                       "l2": "inputs larger than L2: %.0f MB K/V read per step vs 129 MB L2"
-                             % (acct["kv"] / 1e6),
+                       "l2": "steps alternate between two disjoint page pools: each step's "
+                             "%.0f MB of K/V was last read two steps (1.2 GB of K/V) earlier, "
+                             "vs 129 MB of L2" % (acct["kv"] / 1e6),
+                       "l2_flush": True,
                        "parallelism": "independent replica per GPU" if dist_ctx.world > 1
                        else "1 GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -634,8 +712,18 @@ def main():
             "e2e": {"value": acct["step"] * dist_ctx.world / (r["ms_e2e"] * 1e-3) / 1e9,
                     "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["ms_e2e"],
-                    "copies": "pinned host buffers; two alternating stagings, so a step's "
-                              "upload and download overlap its neighbours' computation"},
+                    "copies": "inputs already packed in pinned host buffers; one H2D copy and "
+                              "one D2H copy of the output per step; two alternating stagings, "
+                              "so a step's upload and download overlap its neighbours' "
+                              "computation",
+                    "with_host_pack": {
+                        "value": acct["step"] * dist_ctx.world / (r["ms_e2e_pack"] * 1e-3) / 1e9,
+                        "unit": "GB/s", "ms_per_step": r["ms_e2e_pack"],
+                        "host_pack_ms": r["host_pack_ms"],
+                        "note": "the same loop with every step's inputs also packed from the "
+                                "caller's numpy arrays into the pinned buffer inside the "
+                                "timed region (host-bound when packing plus launch exceed the "
+                                "GPU step)"}},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
@@ -666,6 +754,13 @@ def main():
                         "in L2, so GB/s here is not an HBM rate; the comparison is between "
                         "launch modes" % (dl["bytes_per_step"] / 1e6),
                 **dl}
+            ml = time_decode_loop_layers(device)
+            line["decode_loop"]["layers_from_hbm"] = {
+                "workload": "the same 64 steps over %d layers with separate page pools (%.0f MB "
+                            "of cache in all, above L2), all layers' append + attention in one "
+                            "CUDA graph" % (ml["layers"], ml["layers"] *
+                                            ml["bytes_per_layer_step"] / 1e6),
+                **ml, "frac_of_hbm": ml["shared_plan"]["GBps"] / hbm}
         if not args.no_prefill and dist_ctx.rank == 0:
             mx = time_mixed(device)
             line["mixed_step"] = {

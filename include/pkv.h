@@ -162,6 +162,33 @@ PKV_API int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, c
                              size_t workspace_bytes, int32_t* dev_err_flag, void* stream);
 
 /*
+ * pkv_plan_attention, pkv_paged_attention_run -- the attention step in two halves, so that
+ * one plan serves every layer of a model step.  The step's work list (decode rows, split-KV
+ * items, prefill tiles) depends only on the lengths and the block table, which every layer
+ * of a step shares (niuwancheng.cn "11. Chunked prefill and unified scheduling": the step's
+ * token budget is divided among requests once per step); the K/V pools, Q and the output
+ * are per layer.  pkv_paged_attention_step(...) is exactly pkv_plan_attention followed by
+ * pkv_paged_attention_run on the same stream.
+ *   pkv_plan_attention   validates the lengths on the device (as the full step does) and
+ *                        writes the work list into `workspace`; q, pools and output are not
+ *                        touched.
+ *   pkv_paged_attention_run(_int8)   the attention kernels over the plan in `workspace`:
+ *                        same arguments and results as pkv_paged_attention_step(_int8).
+ *                        The plan must come from pkv_plan_attention (or a full step) with the
+ *                        same host integers and unchanged device arrays, enqueued earlier on
+ *                        the same stream into the same workspace, with no other plan into it
+ *                        since; any number of runs may follow one plan.  The plan is the same
+ *                        for 16-bit and INT8 pools.
+ * Errors: those of pkv_paged_attention_step (the plan call does not check q, pools, out).
+ */
+PKV_API int pkv_plan_attention(const pkv_step_desc* desc, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_err_flag, void* stream);
+PKV_API int pkv_paged_attention_run(const pkv_step_desc* desc, const void* q,
+                                    const void* k_cache, const void* v_cache, void* out,
+                                    float scale, void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_err_flag, void* stream);
+
+/*
  * pkv_paged_attention_step_static_ws -- the same attention step as
  * pkv_paged_attention_step, for callers that cannot allocate device memory when they call
  * it.  Examples are code that runs from a plugin or callback that must not synchronise the
@@ -214,6 +241,13 @@ PKV_API int pkv_kv_append_int8(const pkv_step_desc* desc, const void* k_new, con
                                int8_t* v_cache, int64_t* slot_mapping_out,
                                int32_t* dev_err_flag, void* stream);
 PKV_API size_t pkv_attention_workspace_bytes_int8(const pkv_step_desc* desc);
+/* the run half over INT8 pools (see pkv_plan_attention) */
+PKV_API int pkv_paged_attention_run_int8(const pkv_step_desc* desc, const void* q,
+                                         const int8_t* k_cache, const int8_t* v_cache,
+                                         const float* k_scale, const float* v_scale,
+                                         void* out, float scale, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_err_flag,
+                                         void* stream);
 PKV_API int pkv_paged_attention_step_int8(const pkv_step_desc* desc, const void* q,
                                           const int8_t* k_cache, const int8_t* v_cache,
                                           const float* k_scale, const float* v_scale,

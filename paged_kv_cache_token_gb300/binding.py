@@ -28,7 +28,8 @@ DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16}
 EXPORTED = ("pkv_kv_append", "pkv_advance_context", "pkv_attention_workspace_bytes",
             "pkv_paged_attention_step", "pkv_kv_append_int8",
             "pkv_attention_workspace_bytes_int8", "pkv_paged_attention_step_int8",
-            "pkv_paged_attention_step_static_ws", "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
+            "pkv_paged_attention_step_static_ws", "pkv_plan_attention",
+            "pkv_paged_attention_run", "pkv_paged_attention_run_int8", "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
             "pkv_version")
 
 
@@ -82,6 +83,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_attention_step_int8.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V,
                                                   ctypes.c_float, V, sz, V, V]
     lib.pkv_paged_attention_step_int8.restype = ctypes.c_int
+    lib.pkv_plan_attention.argtypes = [ctypes.POINTER(StepDesc), V, sz, V, V]
+    lib.pkv_plan_attention.restype = ctypes.c_int
+    lib.pkv_paged_attention_run.argtypes = lib.pkv_paged_attention_step.argtypes
+    lib.pkv_paged_attention_run.restype = ctypes.c_int
+    lib.pkv_paged_attention_run_int8.argtypes = lib.pkv_paged_attention_step_int8.argtypes
+    lib.pkv_paged_attention_run_int8.restype = ctypes.c_int
     lib.pkv_paged_attention_step_static_ws.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V,
                                                        ctypes.c_float, V, V]
     lib.pkv_paged_attention_step_static_ws.restype = ctypes.c_int
@@ -165,6 +172,46 @@ def paged_attention_step(desc: StepDesc, q, k_cache, v_cache, out, scale: float,
                                          nbytes, _ptr(err), _stream(stream))
     if check and rc != OK:
         raise PkvError("pkv_paged_attention_step", rc)
+    return rc
+
+
+def plan_attention(desc: StepDesc, workspace, err=None, stream=None, check: bool = True,
+                   workspace_bytes: Optional[int] = None) -> int:
+    """The plan half of the attention step: the step's work list into ``workspace``."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None \
+        else workspace_bytes
+    rc = load().pkv_plan_attention(ctypes.byref(desc), _ptr(workspace), nbytes, _ptr(err),
+                                   _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_plan_attention", rc)
+    return rc
+
+
+def paged_attention_run(desc: StepDesc, q, k_cache, v_cache, out, scale: float, workspace,
+                        err=None, stream=None, check: bool = True,
+                        workspace_bytes: Optional[int] = None) -> int:
+    """The run half: attention over the plan already in ``workspace`` (another layer)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None \
+        else workspace_bytes
+    rc = load().pkv_paged_attention_run(ctypes.byref(desc), _ptr(q), _ptr(k_cache),
+                                        _ptr(v_cache), _ptr(out), float(scale), _ptr(workspace),
+                                        nbytes, _ptr(err), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_paged_attention_run", rc)
+    return rc
+
+
+def paged_attention_run_int8(desc: StepDesc, q, k_cache, v_cache, k_scale, v_scale, out,
+                             scale: float, workspace, err=None, stream=None, check: bool = True,
+                             workspace_bytes: Optional[int] = None) -> int:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None \
+        else workspace_bytes
+    rc = load().pkv_paged_attention_run_int8(ctypes.byref(desc), _ptr(q), _ptr(k_cache),
+                                             _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                             _ptr(out), float(scale), _ptr(workspace), nbytes,
+                                             _ptr(err), _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_paged_attention_run_int8", rc)
     return rc
 
 

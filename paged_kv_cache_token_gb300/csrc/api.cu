@@ -181,19 +181,26 @@ size_t pkv_attention_workspace_bytes_int8(const pkv_step_desc* desc) {
 
 namespace {
 
+// What one attention call launches: the plan and the attention kernels (a whole step), the
+// plan alone, or the attention kernels over a plan already in the workspace.
+enum class Phase { kPlanAndRun, kPlanOnly, kRunOnly };
+
 int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache,
                    const void* v_cache, void* out, float scale, void* workspace,
                    size_t workspace_bytes, int32_t* dev_err_flag, void* stream,
-                   const float* k_scale, const float* v_scale) {
+                   const float* k_scale, const float* v_scale,
+                   Phase phase = Phase::kPlanAndRun) {
     int rc = check_desc(desc);
     if (rc != PKV_OK) return rc;
     if (desc->total_q_tokens == 0) return PKV_OK;
-    if (!q || !k_cache || !v_cache || !out) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-        return PKV_ERR_INVALID_ARG;
     const bool int8 = k_scale != nullptr;
-    if (int8 && (!v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
-        return PKV_ERR_INVALID_ARG;
+    if (phase != Phase::kPlanOnly) {
+        if (!q || !k_cache || !v_cache || !out) return PKV_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+            return PKV_ERR_INVALID_ARG;
+        if (int8 && (!v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+            return PKV_ERR_INVALID_ARG;
+    }
     const int sms = num_sms_current_device();
     if (sms <= 0) return PKV_ERR_CUDA;
     const pkv::WorkspaceLayout lay = layout_for(desc, sms, int8);
@@ -230,9 +237,18 @@ int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((rc = pkv::launch_plan(a, s)) != PKV_OK) return rc;
+    // with both paths possible the prefill goes first and the decode fills the SMs its last
+    // wave leaves idle
+    a.overlap = lay.max_tiles > 0 && lay.max_items > 0 ? 1 : 0;
+    a.plan_wait_first = phase == Phase::kPlanOnly ? 1 : 0;
+    a.plan_ready = phase == Phase::kRunOnly ? 1 : 0;
+    if (phase != Phase::kRunOnly && (rc = pkv::launch_plan(a, s)) != PKV_OK) return rc;
+    if (phase == Phase::kPlanOnly) return PKV_OK;
+    if (a.overlap &&
+        (rc = pkv::launch_prefill(a, s, g_events[1][0], g_events[1][1])) != PKV_OK)
+        return rc;
     if ((rc = pkv::launch_decode(a, s, g_events[0][0], g_events[0][1])) != PKV_OK) return rc;
-    if (lay.max_tiles > 0 &&
+    if (!a.overlap && lay.max_tiles > 0 &&
         (rc = pkv::launch_prefill(a, s, g_events[1][0], g_events[1][1])) != PKV_OK)
         return rc;
     return PKV_OK;
@@ -257,6 +273,30 @@ int pkv_paged_attention_step_int8(const pkv_step_desc* desc, const void* q,
     if (!k_scale) return PKV_ERR_INVALID_ARG;
     return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
                           dev_err_flag, stream, k_scale, v_scale);
+}
+
+int pkv_plan_attention(const pkv_step_desc* desc, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_err_flag, void* stream) {
+    return attention_impl(desc, nullptr, nullptr, nullptr, nullptr, 1.f, workspace,
+                          workspace_bytes, dev_err_flag, stream, nullptr, nullptr,
+                          Phase::kPlanOnly);
+}
+
+int pkv_paged_attention_run(const pkv_step_desc* desc, const void* q, const void* k_cache,
+                            const void* v_cache, void* out, float scale, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_err_flag, void* stream) {
+    return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                          dev_err_flag, stream, nullptr, nullptr, Phase::kRunOnly);
+}
+
+int pkv_paged_attention_run_int8(const pkv_step_desc* desc, const void* q,
+                                 const int8_t* k_cache, const int8_t* v_cache,
+                                 const float* k_scale, const float* v_scale, void* out,
+                                 float scale, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_err_flag, void* stream) {
+    if (!k_scale) return PKV_ERR_INVALID_ARG;
+    return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                          dev_err_flag, stream, k_scale, v_scale, Phase::kRunOnly);
 }
 
 int pkv_set_kernel_events(int which, void* start, void* stop) {

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
         s_sum = 0;
         s_bad = 0;
     }
+    if (a.plan_wait_first) pdl_wait();
     __syncthreads();
 
     // ---- pass A: validity and the decode page total (sets the split size).  The lengths of
@@ -403,11 +404,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         fence_barrier_init();
     }
     __syncwarp();
-    pdl_wait();     // the plan (and through it this step's kv_append) has completed
-    pdl_trigger();  // the combine may be scheduled; it waits for this grid to finish
+    // The plan must be complete before the work list is read, and this step's kv_append
+    // before the pages are.  Behind a prefill grid both completed before any prefill CTA
+    // passed its own wait, and this grid launched only after every prefill CTA had started.
+    // Over a plan made by an earlier call the plan completed before this step's kv_append
+    // started, so only the pages wait (below).  Otherwise the plan is this grid's
+    // predecessor and completes after the kv_append.
+    if (!a.overlap && !a.plan_ready) pdl_wait();
 
     int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
     const int num_items = ctrl[1];
+    const int nwarps = static_cast<int>(gridDim.x) * kDecWarps;  // workers in the grid
     const int4* items = ws_at<const int4>(a, a.lay.items);
     float2* part_ml = ws_at<float2>(a, a.lay.part_ml);
     float* part_o = ws_at<float>(a, a.lay.part_o);
@@ -480,13 +487,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     };
     auto claim = [&]() {  // lane 0 holds the claimed index; read it with __shfl_sync later
         int idx = 0;
-        if (lane == 0) idx = atomicAdd(&ctrl[0], 1);
+        if (lane == 0) idx = atomicAdd(&ctrl[0], 1) + 2 * nwarps;
         return idx;
     };
 
-    // prime the pipeline
-    const int i0 = __shfl_sync(kFull, claim(), 0);
-    const int i1 = __shfl_sync(kFull, claim(), 0);
+    // prime the pipeline: a warp's first two items are fixed by its index (no queue round
+    // trip before the first copy); later ones come from the queue, numbered after them
+    const int i0 = static_cast<int>(blockIdx.x) * kDecWarps + warp;
+    const int i1 = i0 + nwarps;
     int4 ra, rb;
     load_record(i0, ra, rb);
     DecItem cur = resolve(i0, ra, rb);
@@ -503,6 +511,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     int4 p2a, p2b;
     load_record(p2_idx, p2a, p2b);
     int p3_lane0 = claim();
+    // over an earlier plan: the pages of this step's kv_append are final only now
+    if (!a.overlap && a.plan_ready) pdl_wait();
+    pdl_trigger();  // the combine may be scheduled; it waits for this grid to finish
     uint32_t issued = 0, consumed = 0;  // ring counters
     bool aborted = false;
     int ic = 0;          // pages of `cur` issued so far
@@ -912,6 +923,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         mbar_wait_warp(&bars[consumed % kNst], (consumed / kNst) & 1);
         ++consumed;
     }
+    // behind a prefill grid: finish only after it, so the combine and the next step still
+    // follow the whole step
+    if (a.overlap) pdl_wait();
 }
 
 // ------------------------------------------------------------------------------------
@@ -920,15 +934,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 // a batch of splits are independent, so they overlap -- and the groups' states are then
 // merged through shared memory:
 //   m* = max_s m_s,  l* = sum_s l_s 2^(m_s - m*),  acc* = sum_s O_s 2^(m_s - m*)
-// (m in log2 units, O unnormalised).  The launch shapes:
-//   kCombineRow     one CTA per (row, KV head): NG = 1 when no row can have more than
+// (m in log2 units, O unnormalised).  A (row, KV head) pair is one CTA's unit of work; the
+// grids are capped near a full wave (the host only knows a bound on the rows) and each CTA
+// walks the step's actual pairs with a grid stride.  The launch shapes:
+//   kCombineRow     a pair per CTA turn: NG = 1 when no row can have more than
 //                   kManySplits splits; NG groups when rows can be long but there are too
 //                   many of them for the chunked form.
-//   kCombineChunks  CTA (row x KV head, c) merges splits [64c, 64c + 64) into the slot of
-//                   split 64c -- the merged state has the same (m, l, O) form as a split --
-//                   or, for a row with at most 64 splits, writes the row's output.
-//   kCombineParts   one CTA per (row, KV head) with more than 64 splits merges its chunk
-//                   states (stride 64) into the output.
+//   kCombineChunks  turn (pair, c) merges splits [64c, 64c + 64) into the slot of split
+//                   64c -- the merged state has the same (m, l, O) form as a split -- or, for
+//                   a row with at most 64 splits, writes the row's output.
+//   kCombineParts   a pair with more than 64 splits per CTA turn: merges its chunk states
+//                   (stride 64) into the output.
 // The chunked pair serves a long context on few rows, where one CTA per (row, KV head)
 // would read megabytes of partials at a single SM's bandwidth.
 // ------------------------------------------------------------------------------------
@@ -1023,9 +1039,13 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
     __shared__ float2 s_ml[NG > 1 ? NG : 1][TPG];
     __shared__ float4 s_acc[NG > 1 ? NG : 1][TPG];
     const int Hkv = a.num_kv_heads;
-    const int32_t* ctrl = ws_at<const int32_t>(a, a.lay.ctrl);
+    int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
     const int4* rows = ws_at<const int4>(a, a.lay.rows);  // {token, first slot, keys, splits}
     pdl_wait();  // the previous grid (decode kernel or chunk pass) has finished its writes
+    // the decode grid has completed, so nothing claims work items any more: rewind the queue
+    // so the next attention call over the same plan (another layer) starts from item 0
+    if (Stage != kCombineParts && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        ctrl[0] = 0;
     // the grid is capped from host bounds; CTAs walk the step's actual (row, KV head) pairs
     const int nrh = ctrl[2] * Hkv;
     for (int rh = blockIdx.x; rh < nrh; rh += gridDim.x) {  // uniform over the CTA

@@ -61,6 +61,18 @@ struct StepArgs {
     int heads_per_tile; // query heads per prefill tile (2 when a KV group has an even size)
     int32_t* err;
     int kv_int8;        // K/V pools hold INT8 codes with per-channel scales
+    // the prefill grid runs before the decode grid of this step: the prefill lets the decode
+    // launch once its CTAs have all started, and the decode waits for it at its end
+    int overlap;
+    // the plan waits for the preceding kernel before it reads the lengths: set when the plan
+    // is launched on its own (pkv_plan_attention), where that kernel may be the one that
+    // wrote them (pkv_advance_context); a full step's plan follows kv_append instead, which
+    // waited for that writer before letting the plan start
+    int plan_wait_first;
+    // the work list in the workspace was planned before this call (pkv_paged_attention_run):
+    // the decode kernel may read it before its dependency wait, which then only guards the
+    // pages this step's kv_append wrote
+    int plan_ready;
     const float* k_scale;  // [Hkv][D], INT8 pools only
     const float* v_scale;
 };

@@ -73,7 +73,8 @@ prefill_pair_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q,
     constexpr uint32_t kIdescS = tc::idesc_f16(kAB, 0, kBM, kBN);
     constexpr uint32_t kIdescO = tc::idesc_f16(kAB, 1, kBM, D);
 
-    pdl_wait();  // plan, kv_append and the decode kernel of this step have completed
+    pdl_wait();  // the plan and kv_append (and the decode kernel, if it ran first) completed
+    if (a.overlap) pdl_trigger();  // the decode grid may launch once every CTA has started
     const int32_t* ctrl = reinterpret_cast<const int32_t*>(a.ws + a.lay.ctrl);
     if (static_cast<int>(blockIdx.x) >= ctrl[9]) return;
 

@@ -124,6 +124,16 @@ class PagedKV:
             binding.paged_attention_step(desc, q, self.k_cache, self.v_cache, out, scale, ws,
                                          self.err, stream)
 
+    def run_desc(self, desc, q, out, scale: float, ws, stream=None) -> None:
+        """The attention kernels over the plan already in ``ws`` (see
+        binding.plan_attention): one more layer of a planned step."""
+        if self.kv_int8:
+            binding.paged_attention_run_int8(desc, q, self.k_cache, self.v_cache, self.k_scale,
+                                             self.v_scale, out, scale, ws, self.err, stream)
+        else:
+            binding.paged_attention_run(desc, q, self.k_cache, self.v_cache, out, scale, ws,
+                                        self.err, stream)
+
     def append(self, ds: DeviceStep, k_new: torch.Tensor, v_new: torch.Tensor,
                slot_mapping: Optional[torch.Tensor] = None, stream=None) -> None:
         self.append_desc(ds.desc, k_new, v_new, slot_mapping, stream)
@@ -185,20 +195,33 @@ class StepStaging:
 
     def stage(self, plan: StepPlan, q_bits: np.ndarray, k_bits: np.ndarray,
               v_bits: np.ndarray) -> None:
-        """Write a step's inputs (16-bit patterns and metadata) into the pinned buffer."""
+        """Write a step's inputs (16-bit patterns and metadata) into the pinned buffer.  The
+        layout, the device views and the step description depend only on the step's shape
+        (tokens, requests, block-table width); while it repeats they are reused and staging
+        is just the byte copies."""
+        kv = self.kv
+        key = (plan.total_q_tokens, plan.num_reqs, plan.max_pages, plan.max_q_len,
+               plan.max_context_len)
+        if getattr(self, "_key", None) != key:
+            self._prepare(plan)
+            self._key = key
+        src = (q_bits, k_bits, v_bits, plan.q_lens, plan.q_offsets, plan.context_lens,
+               plan.block_table)
+        for dst, a in zip(self._host_views, src):
+            np.copyto(dst, a.reshape(dst.shape), casting="no")
+        self.plan = plan
+
+    def _prepare(self, plan: StepPlan) -> None:
         kv = self.kv
         offs, total = self._layout(plan)
         out_bytes = self._up(plan.total_q_tokens * kv.hq * kv.d * 2)
         self._ensure(total, out_bytes)
         h = self._host.numpy()
-        src = {"q": q_bits, "k": k_bits, "v": v_bits, "q_lens": plan.q_lens,
-               "q_offsets": plan.q_offsets, "context_lens": plan.context_lens,
-               "block_table": plan.block_table}
-        for name, (off, nbytes) in offs.items():
-            a = np.ascontiguousarray(src[name])
-            assert a.nbytes == nbytes, (name, a.nbytes, nbytes)
-            h[off:off + nbytes] = a.reshape(-1).view(np.uint8)
-        self.plan, self.offs, self.total = plan, offs, total
+        kinds = {"q": np.uint16, "k": np.uint16, "v": np.uint16, "q_lens": np.int32,
+                 "q_offsets": np.int32, "context_lens": np.int32, "block_table": np.int32}
+        self._host_views = [h[off:off + nbytes].view(kinds[name])
+                            for name, (off, nbytes) in offs.items()]
+        self.offs, self.total = offs, total
         T = plan.total_q_tokens
         d = self._dev
         view = lambda name, dt, shape: d[offs[name][0]:offs[name][0] + offs[name][1]].view(dt) \
@@ -217,6 +240,7 @@ class StepStaging:
         self.out = self._out_dev[:T * kv.hq * kv.d * 2].view(kv.dtype).view(T, kv.hq, kv.d)
         self.out_host = self._out_host[:T * kv.hq * kv.d * 2].view(kv.dtype) \
             .view(T, kv.hq, kv.d)
+        self._ws = kv.workspace(self.desc)
 
     @property
     def h2d_bytes(self) -> int:
@@ -233,8 +257,7 @@ class StepStaging:
     def run(self, scale: float, stream=None) -> None:
         """kv_append then the attention step, on the staged device views."""
         self.kv.append_desc(self.desc, self.k_new, self.v_new, None, stream)
-        self.kv.attention_desc(self.desc, self.q, self.out, scale,
-                               self.kv.workspace(self.desc), stream)
+        self.kv.attention_desc(self.desc, self.q, self.out, scale, self._ws, stream)
 
     def download(self) -> None:
         """Device -> host copy of the step's output on the current stream."""
@@ -257,9 +280,11 @@ class StepPipeline:
     ``launch``.
     """
 
-    def __init__(self, kv: PagedKV, compute_stream=None):
+    def __init__(self, kv: PagedKV, compute_stream=None, kv_alt: Optional[PagedKV] = None):
+        """``kv_alt``: a second set of pools for the odd steps (e.g. another layer's cache);
+        by default both stagings use ``kv``."""
         self.kv = kv
-        self.stg = [StepStaging(kv), StepStaging(kv)]
+        self.stg = [StepStaging(kv), StepStaging(kv_alt if kv_alt is not None else kv)]
         self.compute = compute_stream or torch.cuda.current_stream(kv.device)
         self.h2d = torch.cuda.Stream(device=kv.device)
         self.d2h = torch.cuda.Stream(device=kv.device)
@@ -317,9 +342,15 @@ class DecodeLoop:
     K_new, V_new are staged on the device up front and each step's output has its own slot.
     ``capture`` records the whole sequence in one CUDA graph (the lengths are reset at its
     start, so it can be replayed); ``replay`` then runs all steps with one launch.
+
+    ``layers``: more layers of the same model step, each a ``(PagedKV, workload)`` with its
+    own pools and its own values for the same requests and pages; every step runs each
+    layer's append + attention in turn.  With ``shared_plan`` a step plans once
+    (pkv_plan_attention) and every layer runs over that plan (pkv_paged_attention_run)
+    instead of planning again.  ``outs[l]`` holds layer l's outputs, ``out`` layer 0's.
     """
 
-    def __init__(self, kv: PagedKV, workload, plans):
+    def __init__(self, kv: PagedKV, workload, plans, layers=(), shared_plan: bool = False):
         if not plans:
             raise ValueError("no steps")
         p0, pl = plans[0], plans[-1]
@@ -332,12 +363,20 @@ class DecodeLoop:
                 if not np.array_equal(p.block_table[r, :n], pl.block_table[r, :n]):
                     raise ValueError("block tables of the steps disagree")
         self.kv, self.scale, self.steps = kv, workload.scale, len(plans)
+        self.shared_plan = shared_plan
+        self.layers = [(kv, workload)] + list(layers)
         dev = kv.device
-        ins = [step_host_inputs(workload, p) for p in plans]
-        stack = lambda i: bits_to_tensor(np.stack([x[i] for x in ins]), workload.dtype, dev)
-        self.q, self.k_new, self.v_new = stack(0), stack(1), stack(2)
         T = p0.total_q_tokens
-        self.out = torch.empty((self.steps, T, kv.hq, kv.d), dtype=kv.dtype, device=dev)
+        self.io = []
+        for lkv, lw in self.layers:
+            if (lkv.hq, lkv.hkv, lkv.d, lkv.num_pages) != (kv.hq, kv.hkv, kv.d, kv.num_pages):
+                raise ValueError("layers must share the pool geometry")
+            ins = [step_host_inputs(lw, p) for p in plans]
+            stack = lambda i: bits_to_tensor(np.stack([x[i] for x in ins]), lw.dtype, dev)
+            out = torch.empty((self.steps, T, kv.hq, kv.d), dtype=kv.dtype, device=dev)
+            self.io.append((stack(0), stack(1), stack(2), out))
+        self.q, self.k_new, self.v_new, self.out = self.io[0]
+        self.outs = [x[3] for x in self.io]
         self.q_lens = torch.from_numpy(p0.q_lens).to(dev)
         self.q_offsets = torch.from_numpy(p0.q_offsets).to(dev)
         self.ctx0 = torch.from_numpy(p0.context_lens).to(dev)
@@ -353,11 +392,16 @@ class DecodeLoop:
         self.graph = None
 
     def _body(self, stream=None) -> None:
-        kv = self.kv
         self.ctx.copy_(self.ctx0, non_blocking=True)
         for s in range(self.steps):
-            kv.append_desc(self.desc, self.k_new[s], self.v_new[s], None, stream)
-            kv.attention_desc(self.desc, self.q[s], self.out[s], self.scale, self.ws, stream)
+            if self.shared_plan:
+                binding.plan_attention(self.desc, self.ws, self.kv.err, stream)
+            for (lkv, _), (q, k_new, v_new, out) in zip(self.layers, self.io):
+                lkv.append_desc(self.desc, k_new[s], v_new[s], None, stream)
+                if self.shared_plan:
+                    lkv.run_desc(self.desc, q[s], out[s], self.scale, self.ws, stream)
+                else:
+                    lkv.attention_desc(self.desc, q[s], out[s], self.scale, self.ws, stream)
             binding.advance_context(self.desc, self.ctx, stream)
 
     def run(self) -> torch.Tensor:

@@ -71,7 +71,11 @@ def test_host_validation_rejects_before_launch(lib, kw, code):
                                       None)
     assert rc == code
     assert lib.pkv_attention_workspace_bytes(ctypes.byref(d)) == 0
-    # the built-in-scratch entry point reports description errors the same way
+    # the plan and run halves and the built-in-scratch entry point report description
+    # errors the same way
+    assert lib.pkv_plan_attention(ctypes.byref(d), None, 0, None, None) == code
+    assert lib.pkv_paged_attention_run(ctypes.byref(d), None, None, None, None, 1.0, None, 0,
+                                       None, None) == code
     rc = lib.pkv_paged_attention_step_static_ws(ctypes.byref(d), None, None, None, None, 1.0,
                                                 None, None)
     assert rc == code
@@ -140,3 +144,18 @@ def test_empty_step_is_a_no_op(lib):
 def test_read_device_error_rejects_null(lib):
     v = ctypes.c_int32(0)
     assert lib.pkv_read_device_error(None, ctypes.byref(v), None) == -1
+
+
+def test_plan_and_run_argument_checks(lib):
+    d = _desc()
+    t = ctypes.c_void_p(0x1000)
+    # the run needs the tensors (checked before any device query)
+    assert lib.pkv_paged_attention_run(ctypes.byref(d), None, None, None, None, 1.0, t, 1 << 30,
+                                       None, None) == -1
+    assert lib.pkv_paged_attention_run_int8(ctypes.byref(d), t, t, t, None, t, t, 1.0, t,
+                                            1 << 30, None, None) == -1
+    e = _desc(num_reqs=0, total_q_tokens=0, max_q_len=0, max_context_len=0, q_lens=None,
+              q_offsets=None, context_lens=None, block_table=None)
+    assert lib.pkv_plan_attention(ctypes.byref(e), None, 0, None, None) == 0
+    assert lib.pkv_paged_attention_run(ctypes.byref(e), None, None, None, None, 1.0, None, 0,
+                                       None, None) == 0

@@ -316,3 +316,35 @@ def test_int8_append_negative_offsets_flagged_and_skipped():
     assert bool((kv.k_cache == runner.INT8_SENTINEL).all())
     assert bool((kv.v_cache == runner.INT8_SENTINEL).all())
     assert slots.cpu().tolist() == [-7, -7]
+
+
+def _first_step(w):
+    """The first step after the workload's cached history is loaded."""
+    s = scheduler_for(w)
+    s.history_plan()
+    return s.next_step()
+
+
+def test_int8_shared_plan_two_layers():
+    # INT8 pools: one plan, two layers' runs (pkv_paged_attention_run_int8), each layer
+    # against the oracle over its own codes
+    import dataclasses
+    specs = [(2000, 0, 1), (0, 300, 0), (100, 0, 1)]
+    w0 = custom(1700, 32, 8, 128, 0, specs)
+    w1 = dataclasses.replace(w0, index=w0.index + 100, _cache={})
+    plan = _first_step(w0)
+    pools = []
+    for lw in (w0, w1):
+        kv = runner.paged_kv_for(lw, kv_int8=True)
+        runner.load_history(kv, lw, scheduler_for(lw).history_plan())
+        pools.append(kv)
+    ds = pools[0].upload(plan)
+    ws = pools[0].workspace(ds.desc)
+    binding.plan_attention(ds.desc, ws, pools[0].err)
+    for kv, lw in zip(pools, (w0, w1)):
+        q, k, v = runner.step_host_inputs(lw, plan)
+        kv.append(ds, runner.bits_to_tensor(k, 0), runner.bits_to_tensor(v, 0))
+        out = torch.empty((plan.total_q_tokens, 32, 128), dtype=torch.bfloat16, device="cuda")
+        kv.run_desc(ds.desc, runner.bits_to_tensor(q, 0), out, lw.scale, ws)
+        assert kv.read_error() == 0
+        assert_close(gpu_as_f64(out), oracle_rows_int8(lw, plan), "int8 planned layer")

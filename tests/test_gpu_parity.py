@@ -355,6 +355,93 @@ def test_decode_loop_and_graph_bitwise_identical():
             assert_close(gpu_as_f64(out[i]), oracle_rows(w, plans[i]), "%s step %d" % (mode, i))
 
 
+def _layer_of(w, layer):
+    """Layer ``layer`` of a model step over workload ``w``: the same requests, lengths and
+    pages, its own Q/K/V values (another seed)."""
+    import dataclasses
+    return dataclasses.replace(w, index=w.index + 100 * layer, _cache={})
+
+
+def test_shared_plan_layers_match_per_layer_steps_and_oracle():
+    # two layers of the MHA-skew run's 64 decode steps: one plan per step shared by both
+    # layers (pkv_plan_attention + pkv_paged_attention_run) gives the same bits as every
+    # layer planning its own step, and both layers match the oracle
+    w0 = W.mha_skew()
+    w1 = _layer_of(w0, 1)
+
+    def fresh():
+        pools = []
+        for lw in (w0, w1):
+            kv = runner.paged_kv_for(lw)
+            runner.load_history(kv, lw, scheduler_for(lw).history_plan())
+            pools.append(kv)
+        return pools
+
+    s = scheduler_for(w0)
+    s.history_plan()
+    plans = s.all_steps()
+    outs = {}
+    for shared in (False, True):
+        kv0, kv1 = fresh()
+        kv1.err = kv0.err
+        loop = runner.DecodeLoop(kv0, w0, plans, layers=[(kv1, w1)], shared_plan=shared)
+        if shared:
+            loop.capture()
+            loop.replay()
+        else:
+            loop.run()
+        torch.cuda.synchronize()
+        assert kv0.read_error() == 0
+        outs[shared] = [o.clone() for o in loop.outs]
+    for a, b in zip(outs[False], outs[True]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for lw, o in zip((w0, w1), outs[True]):
+        for i in (0, 31, 63):
+            assert_close(gpu_as_f64(o[i]), oracle_rows(lw, plans[i]), "layer step %d" % i)
+
+
+def _first_step(w):
+    """The first step after the workload's cached history is loaded."""
+    s = scheduler_for(w)
+    s.history_plan()
+    return s.next_step()
+
+
+def test_shared_plan_mixed_step_two_layers():
+    # a step with decode rows and prefill chunks (both kernels, prefill first): plan once,
+    # then two layers' append + run; each layer's output equals a full step on its pools
+    specs = [(3000, 0, 1), (0, 700, 0), (40, 0, 1), (900, 300, 0), (5, 0, 1)]
+    w0 = custom(1600, 32, 8, 128, 0, specs)
+    w1 = _layer_of(w0, 1)
+    full, planned = [], []
+    for mode in ("full", "planned"):
+        pools = []
+        for lw in (w0, w1):
+            kv = runner.paged_kv_for(lw)
+            runner.load_history(kv, lw, scheduler_for(lw).history_plan())
+            pools.append(kv)
+        plan = _first_step(w0)
+        assert plan.max_q_len >= 16 and int((plan.q_lens == 1).sum()) == 3
+        ds = pools[0].upload(plan)
+        ws = pools[0].workspace(ds.desc)
+        if mode == "planned":
+            binding.plan_attention(ds.desc, ws, pools[0].err)
+        for kv, lw in zip(pools, (w0, w1)):
+            q, k, v = runner.step_host_inputs(lw, plan)
+            kv.append(ds, runner.bits_to_tensor(k, 0), runner.bits_to_tensor(v, 0))
+            out = torch.empty((plan.total_q_tokens, 32, 128), dtype=torch.bfloat16, device="cuda")
+            qd = runner.bits_to_tensor(q, 0)
+            if mode == "planned":
+                kv.run_desc(ds.desc, qd, out, lw.scale, ws)
+            else:
+                kv.attention_desc(ds.desc, qd, out, lw.scale, ws)
+            (full if mode == "full" else planned).append(out)
+            assert kv.read_error() == 0
+    for a, b in zip(full, planned):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert_close(gpu_as_f64(planned[1]), oracle_rows(w1, plan), "planned layer 1")
+
+
 def test_prefix_cache_reuse_matches_oracle():
     # prefix caching (hotelren.com/news/6181127 §4.3) through the native planner: requests
     # sharing a 100-token system prompt reuse the full prompt blocks the first one already
