@@ -256,6 +256,25 @@ PKV_API int pkv_paged_attention_step_int8(const pkv_step_desc* desc, const void*
                                           void* stream);
 
 /*
+ * pkv_copy_pages -- copy whole pages, K and V, from src_pages[i] to dst_pages[i] for
+ * i < num_copies: every KV head's 16 slots, bit for bit.  This is the copy-on-write of a
+ * page several requests share (include/pkv_sched.h, pkv_sched_fork) before one of them
+ * appends into it; enqueue it before that step's pkv_kv_append.  hotelren.com/news/6181127
+ * §4.3: cached K/V reused across requests, memory managed by page.
+ *   desc             only num_kv_heads, head_dim, page_size, num_pages and dtype are read
+ *   src_pages,
+ *   dst_pages        device int32 [num_copies]; a destination must not be a source or
+ *                    appear twice
+ *   k_cache, v_cache the pools: 16-bit (kv_int8 = 0) or INT8 (kv_int8 = 1); a page is the
+ *                    same contiguous block of every pool either way
+ * A page id outside the pool sets PKV_DEVERR_PAGE_RANGE and that copy is skipped.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.  num_copies == 0 is a no-op returning PKV_OK.
+ */
+PKV_API int pkv_copy_pages(const pkv_step_desc* desc, const int32_t* src_pages,
+                           const int32_t* dst_pages, int32_t num_copies, void* k_cache,
+                           void* v_cache, int kv_int8, int32_t* dev_err_flag, void* stream);
+
+/*
  * pkv_read_device_error -- synchronise `stream`, copy *dev_err_flag (device) to
  * *host_value and return PKV_OK when it is zero, PKV_ERR_DEVICE when not, PKV_ERR_CUDA
  * when the copy fails.  The only synchronising entry point.

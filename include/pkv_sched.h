@@ -32,10 +32,16 @@ typedef struct pkv_scheduler pkv_scheduler;  /* opaque */
  *        max_pages_per_req   row stride of block_table (pass it as the step
  *                            description's max_pages_per_req)
  *        rids .. block_table host arrays of those capacities
+ *        max_copies          capacity of copy_src, copy_dst (may be 0 with NULL arrays
+ *                            when no request is ever forked)
  *   out: num_reqs            requests in the step, in launch order
  *        total_q_tokens      sum of q_lens
  *        max_q_len, max_context_len
  *        pages_used          longest block-table row of the step (<= max_pages_per_req)
+ *        num_copies          page copies the step needs before its kv_append (copy-on-write
+ *                            of pages shared after pkv_sched_fork): copy page copy_src[i]
+ *                            to copy_dst[i] with pkv_copy_pages; the block table already
+ *                            names the copies
  * block_table row i holds request i's physical pages, -1 past its last page.
  */
 typedef struct {
@@ -51,6 +57,10 @@ typedef struct {
     int32_t max_q_len;
     int32_t max_context_len;
     int32_t pages_used;
+    int32_t max_copies;
+    int32_t* copy_src;
+    int32_t* copy_dst;
+    int32_t num_copies;
 } pkv_plan;
 
 /*
@@ -124,7 +134,8 @@ PKV_API int32_t pkv_sched_free_pages(const pkv_scheduler* s);
  *  - Shared blocks are reference-counted.  A request's release returns its references;
  *    blocks nobody uses stay cached and are evicted least-recently-used first, block by
  *    block, only when the free list is empty.
- *  - Shared pages are always full, so no step ever writes into one.
+ *  - Registered blocks are always full, so no step ever writes into one (pages shared by
+ *    pkv_sched_fork, which may be partly filled, are copied on write instead).
  */
 
 /*
@@ -134,6 +145,22 @@ PKV_API int32_t pkv_sched_free_pages(const pkv_scheduler* s);
  */
 PKV_API int pkv_sched_add_prompt(pkv_scheduler* s, int32_t rid, const int32_t* tokens,
                                  int32_t n_prompt, int32_t decodes);
+
+/*
+ * pkv_sched_fork -- append request `rid` that continues from everything request
+ * `parent_rid` has cached so far (its prompt must be complete) with `decodes` generated
+ * tokens of its own: parallel samples or beams of one prompt.  The child shares all of the
+ * parent's pages, a partly filled last page included; every shared page counts its holders
+ * (hotelren.com/news/6181127 §4.3: reused K/V, memory managed by page).  Copy-on-write: when
+ * a step is about to write a request's next token into a page that already holds tokens and
+ * that another request also holds, the planner gives the request a fresh page, names it in
+ * the block table and lists the copy (old page -> fresh page) in the plan; the last holder
+ * of a page writes into it in place.  Releasing a request drops its hold on every page; a
+ * page returns to the free list with its last holder.  Errors: INVALID_ARG (unknown parent,
+ * parent still prefilling or without cached tokens, rid already used), CAPACITY (out of
+ * memory).
+ */
+PKV_API int pkv_sched_fork(pkv_scheduler* s, int32_t parent_rid, int32_t rid, int32_t decodes);
 
 /* Registered blocks: all of them, and those no request uses (evictable).  -1 for NULL. */
 PKV_API int32_t pkv_sched_cached_blocks(const pkv_scheduler* s);

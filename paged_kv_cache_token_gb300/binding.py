@@ -29,7 +29,8 @@ EXPORTED = ("pkv_kv_append", "pkv_advance_context", "pkv_attention_workspace_byt
             "pkv_paged_attention_step", "pkv_kv_append_int8",
             "pkv_attention_workspace_bytes_int8", "pkv_paged_attention_step_int8",
             "pkv_paged_attention_step_static_ws", "pkv_plan_attention",
-            "pkv_paged_attention_run", "pkv_paged_attention_run_int8", "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
+            "pkv_paged_attention_run", "pkv_paged_attention_run_int8", "pkv_copy_pages",
+            "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
             "pkv_version")
 
 
@@ -83,6 +84,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_attention_step_int8.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V,
                                                   ctypes.c_float, V, sz, V, V]
     lib.pkv_paged_attention_step_int8.restype = ctypes.c_int
+    lib.pkv_copy_pages.argtypes = [ctypes.POINTER(StepDesc), V, V, ctypes.c_int32, V, V,
+                                   ctypes.c_int, V, V]
+    lib.pkv_copy_pages.restype = ctypes.c_int
     lib.pkv_plan_attention.argtypes = [ctypes.POINTER(StepDesc), V, sz, V, V]
     lib.pkv_plan_attention.restype = ctypes.c_int
     lib.pkv_paged_attention_run.argtypes = lib.pkv_paged_attention_step.argtypes
@@ -172,6 +176,18 @@ def paged_attention_step(desc: StepDesc, q, k_cache, v_cache, out, scale: float,
                                          nbytes, _ptr(err), _stream(stream))
     if check and rc != OK:
         raise PkvError("pkv_paged_attention_step", rc)
+    return rc
+
+
+def copy_pages(desc: StepDesc, src_pages, dst_pages, k_cache, v_cache, kv_int8: bool = False,
+               err=None, stream=None, check: bool = True) -> int:
+    """Copy whole pages src_pages[i] -> dst_pages[i] (int32 CUDA tensors) in both pools."""
+    n = int(src_pages.numel())
+    rc = load().pkv_copy_pages(ctypes.byref(desc), _ptr(src_pages), _ptr(dst_pages), n,
+                               _ptr(k_cache), _ptr(v_cache), 1 if kv_int8 else 0, _ptr(err),
+                               _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_copy_pages", rc)
     return rc
 
 

@@ -153,6 +153,28 @@ int pkv_kv_append_int8(const pkv_step_desc* desc, const void* k_new, const void*
                           stream, k_scale, v_scale);
 }
 
+int pkv_copy_pages(const pkv_step_desc* desc, const int32_t* src_pages,
+                   const int32_t* dst_pages, int32_t num_copies, void* k_cache, void* v_cache,
+                   int kv_int8, int32_t* dev_err_flag, void* stream) {
+    if (!desc || num_copies < 0) return PKV_ERR_INVALID_ARG;
+    if (desc->page_size != PKV_PAGE_SIZE || desc->num_pages <= 0 || desc->num_kv_heads <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (desc->dtype != PKV_BF16 && desc->dtype != PKV_FP16) return PKV_ERR_UNSUPPORTED;
+    if (desc->head_dim != 64 && desc->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (kv_int8 != 0 && kv_int8 != 1) return PKV_ERR_INVALID_ARG;
+    if (num_copies == 0) return PKV_OK;
+    if (!src_pages || !dst_pages || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(src_pages) & 3u) ||
+        (reinterpret_cast<uintptr_t>(dst_pages) & 3u))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t page_bytes = static_cast<int64_t>(desc->num_kv_heads) * PKV_PAGE_SIZE *
+                               desc->head_dim * (kv_int8 ? 1 : 2);
+    return pkv::launch_copy_pages(src_pages, dst_pages, num_copies, page_bytes, desc->num_pages,
+                                  k_cache, v_cache, dev_err_flag,
+                                  static_cast<cudaStream_t>(stream));
+}
+
 int pkv_advance_context(const pkv_step_desc* desc, int32_t* context_lens, void* stream) {
     const int rc = check_desc(desc);
     if (rc != PKV_OK) return rc;

@@ -10,6 +10,8 @@
 // V, 16 bytes per lane, so each row moves as full 128-byte transactions.  The destination
 // comes from the block table.  Bad device data sets a flag bit and skips the copy; nothing
 // traps.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -190,6 +192,52 @@ int launch_advance_context(const int32_t* q_lens, int32_t* context_lens, int num
     if (num_reqs == 0) return PKV_OK;
     return launch_pdl(advance_context_kernel, dim3(cdiv(num_reqs, 256)), dim3(256), 0, stream,
                       q_lens, context_lens, num_reqs) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+// Copy-on-write of shared pages: page src[i] -> dst[i], K and V, every KV head, bit for bit
+// (a page is one contiguous block of page_bytes in each pool, for 16-bit and INT8 pools
+// alike).  grid.x = copy, grid.y = slice of the page; 16 bytes per thread and load.
+__global__ void __launch_bounds__(256) copy_pages_kernel(const int32_t* src, const int32_t* dst,
+                                                         int n, int64_t page_bytes,
+                                                         int num_pages, uint8_t* k_cache,
+                                                         uint8_t* v_cache, int32_t* err) {
+    // earlier kernels on the stream (the previous step) may still read the destination,
+    // a page that was free before this step
+    pdl_wait();
+    pdl_trigger();
+    const int c = blockIdx.x;
+    if (c >= n) return;
+    const int s = __ldg(src + c), d = __ldg(dst + c);
+    if (s < 0 || s >= num_pages || d < 0 || d >= num_pages) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) set_error(err, PKV_DEVERR_PAGE_RANGE);
+        return;
+    }
+    if (s == d) return;
+    const int64_t words = page_bytes / 16;
+    const uint4* ks = reinterpret_cast<const uint4*>(k_cache + s * page_bytes);
+    const uint4* vs = reinterpret_cast<const uint4*>(v_cache + s * page_bytes);
+    uint4* kd = reinterpret_cast<uint4*>(k_cache + d * page_bytes);
+    uint4* vd = reinterpret_cast<uint4*>(v_cache + d * page_bytes);
+    for (int64_t w = blockIdx.y * blockDim.x + threadIdx.x; w < words;
+         w += static_cast<int64_t>(gridDim.y) * blockDim.x) {
+        const uint4 kw = ks[w], vw = vs[w];
+        kd[w] = kw;
+        vd[w] = vw;
+    }
+}
+
+int launch_copy_pages(const int32_t* src, const int32_t* dst, int n, int64_t page_bytes,
+                      int num_pages, void* k_cache, void* v_cache, int32_t* err,
+                      cudaStream_t stream) {
+    if (n <= 0) return PKV_OK;
+    const int64_t words = page_bytes / 16;
+    const int slices = static_cast<int>(std::min<int64_t>(8, (words + 255) / 256));
+    const dim3 grid(n, slices);
+    return launch_pdl(copy_pages_kernel, grid, dim3(256), 0, stream, src, dst, n, page_bytes,
+                      num_pages, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
+                      err) == cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
 }

@@ -105,6 +105,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 int launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 int launch_kv_append_int8(const AppendArgs& a, cudaStream_t stream);
+int launch_copy_pages(const int32_t* src, const int32_t* dst, int n, int64_t page_bytes,
+                      int num_pages, void* k_cache, void* v_cache, int32_t* err,
+                      cudaStream_t stream);
 int launch_advance_context(const int32_t* q_lens, int32_t* context_lens, int num_reqs,
                            cudaStream_t stream);
 int launch_plan(const StepArgs& a, cudaStream_t stream);

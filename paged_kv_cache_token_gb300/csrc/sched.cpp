@@ -92,6 +92,23 @@ struct pkv_scheduler {
     std::unordered_map<int32_t, size_t> index;
     std::unordered_map<uint64_t, Block> blocks;  // shared prompt blocks by key
     std::list<uint64_t> lru;                      // unreferenced blocks, least recent first
+    // pages outside the block registry held by more than one request (after a fork), with
+    // their number of holders; a page absent here has one holder
+    std::unordered_map<int32_t, int32_t> holders;
+
+    int32_t holders_of(int32_t page) const {
+        const auto it = holders.find(page);
+        return it == holders.end() ? 1 : it->second;
+    }
+    // one holder lets go of a private page: the last one returns it to the free list
+    void drop_page(int32_t page) {
+        const auto it = holders.find(page);
+        if (it == holders.end()) {
+            free_list.push_back(page);
+        } else if (--it->second <= 1) {
+            holders.erase(it);
+        }
+    }
 
     int64_t available() const {
         return static_cast<int64_t>(free_list.size()) + static_cast<int64_t>(lru.size());
@@ -170,8 +187,34 @@ struct pkv_scheduler {
             max_ctx = std::max(max_ctx, r.computed);
         }
         if (total_q > INT32_MAX || max_ctx > INT32_MAX) return PKV_ERR_CAPACITY;
-        if (need > available()) return PKV_ERR_NO_PAGES;
+        const int64_t copies = copy_on_write_pages(picks).size();
+        if (copies > 0 && (out->max_copies < copies || !out->copy_src || !out->copy_dst))
+            return PKV_ERR_CAPACITY;
+        if (need + copies > available()) return PKV_ERR_NO_PAGES;
         return PKV_OK;
+    }
+
+    // Copy-on-write: the picks (in order) whose first new token lands in a page that
+    // already holds tokens and that another request also holds.  A request about to write
+    // into a shared page gets a copy of it first; the holders left keep the original, and
+    // the last of them writes into it in place.  Returns, per such pick, its index in
+    // `picks` (the holder counts as they will be when the pick is reached).
+    std::vector<size_t> copy_on_write_pages(const std::vector<Pick>& picks) const {
+        std::vector<size_t> cow;
+        std::unordered_map<int32_t, int32_t> left;  // holders still on a page in this step
+        for (size_t k = 0; k < picks.size(); ++k) {
+            const Pick& p = picks[k];
+            const Req& r = reqs[p.i];
+            if (p.n <= 0 || r.computed % kPage == 0) continue;  // starts a fresh page
+            const int32_t page = r.pages[static_cast<size_t>(r.computed / kPage)];
+            auto it = left.find(page);
+            if (it == left.end()) it = left.emplace(page, holders_of(page)).first;
+            if (it->second > 1) {
+                cow.push_back(k);
+                --it->second;
+            }
+        }
+        return cow;
     }
 
     // Check, then take the step's pages (in pick order, as the step reaches them one
@@ -186,7 +229,20 @@ struct pkv_scheduler {
             max_ctx = std::max(max_ctx, history ? int64_t{0} : reqs[p.i].computed);
             pages_used = std::max(pages_used, p.pages_after);
         }
+        const std::vector<size_t> cow = history ? std::vector<size_t>() :
+                                                   copy_on_write_pages(picks);
         // nothing can fail from here on
+        out->num_copies = 0;
+        for (size_t k : cow) {
+            Req& r = reqs[picks[k].i];
+            int32_t& slot = r.pages[static_cast<size_t>(r.computed / kPage)];
+            const int32_t fresh = take_page();
+            out->copy_src[out->num_copies] = slot;
+            out->copy_dst[out->num_copies] = fresh;
+            ++out->num_copies;
+            drop_page(slot);  // another request still holds the original
+            slot = fresh;
+        }
         const int64_t stride = out->max_pages_per_req;
         int32_t off = 0;
         for (size_t k = 0; k < picks.size(); ++k) {
@@ -359,7 +415,7 @@ int pkv_sched_release(pkv_scheduler* s, int32_t rid) {
         for (size_t i = 0; i < r.pages.size(); ++i) {
             const uint64_t key = i < r.block_of.size() ? r.block_of[i] : 0;
             if (key == 0) {
-                s->free_list.push_back(r.pages[i]);
+                s->drop_page(r.pages[i]);
                 continue;
             }
             Block& blk = s->blocks.at(key);
@@ -416,6 +472,51 @@ int pkv_sched_add_prompt(pkv_scheduler* s, int32_t rid, const int32_t* tokens,
         for (Block* blk : hit)  // nothing can fail any more: take the references
             if (blk->refs++ == 0) s->lru.erase(blk->lru);
         return static_cast<int>(hit.size() * kPage);
+    } catch (...) {
+        return PKV_ERR_CAPACITY;
+    }
+}
+
+int pkv_sched_fork(pkv_scheduler* s, int32_t parent_rid, int32_t rid, int32_t decodes) {
+    if (!s || decodes < 0 || s->index.count(rid)) return PKV_ERR_INVALID_ARG;
+    const auto it = s->index.find(parent_rid);
+    if (it == s->index.end()) return PKV_ERR_INVALID_ARG;
+    const Req& parent = s->reqs[it->second];
+    if (parent.computed <= 0 || parent.computed < parent.prompt_end ||
+        parent.history_pending)
+        return PKV_ERR_INVALID_ARG;
+    try {
+        Req r;
+        r.rid = rid;
+        r.history = 0;
+        r.computed = parent.computed;
+        r.prompt_end = parent.computed;
+        r.total = parent.computed + decodes;
+        r.begun = true;
+        r.pages.assign(parent.pages.begin(),
+                       parent.pages.begin() + static_cast<std::ptrdiff_t>(pages_for(r.computed)));
+        r.block_of.assign(parent.block_of.begin(),
+                          parent.block_of.begin() + static_cast<std::ptrdiff_t>(r.pages.size()));
+        // reserve every container insertion before the first reference is taken
+        s->holders.reserve(s->holders.size() + r.pages.size());
+        s->reqs.push_back(std::move(r));
+        try {
+            s->index[rid] = s->reqs.size() - 1;
+        } catch (...) {
+            s->reqs.pop_back();
+            throw;
+        }
+        const Req& child = s->reqs.back();  // nothing can fail any more: take references
+        for (size_t i = 0; i < child.pages.size(); ++i) {
+            const uint64_t key = child.block_of[i];
+            if (key != 0) {
+                Block& blk = s->blocks.at(key);
+                if (blk.refs++ == 0) s->lru.erase(blk.lru);
+            } else {
+                s->holders[child.pages[i]] = s->holders_of(child.pages[i]) + 1;
+            }
+        }
+        return PKV_OK;
     } catch (...) {
         return PKV_ERR_CAPACITY;
     }

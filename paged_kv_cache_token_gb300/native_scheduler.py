@@ -27,7 +27,8 @@ class _Plan(ctypes.Structure):
                 ("q_offsets", _I32P), ("block_table", _I32P),
                 ("num_reqs", ctypes.c_int32), ("total_q_tokens", ctypes.c_int32),
                 ("max_q_len", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
-                ("pages_used", ctypes.c_int32)]
+                ("pages_used", ctypes.c_int32), ("max_copies", ctypes.c_int32),
+                ("copy_src", _I32P), ("copy_dst", _I32P), ("num_copies", ctypes.c_int32)]
 
 
 def _lib():
@@ -51,6 +52,8 @@ def _lib():
         lib.pkv_sched_add_prompt.argtypes = [V, ctypes.c_int32, V, ctypes.c_int32,
                                              ctypes.c_int32]
         lib.pkv_sched_add_prompt.restype = ctypes.c_int
+        lib.pkv_sched_fork.argtypes = [V, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+        lib.pkv_sched_fork.restype = ctypes.c_int
         lib.pkv_sched_sort_by_length.argtypes = [V]
         lib.pkv_sched_sort_by_length.restype = ctypes.c_int
         for fn in (lib.pkv_sched_cached_blocks, lib.pkv_sched_evictable_blocks):
@@ -72,6 +75,7 @@ class NativeScheduler:
         if not self._h:
             raise ValueError("bad scheduler arguments")
         self._interleave = interleave_history
+        self._total = {}
         self.max_reqs = 0
         self.max_pages = 1
         for r in requests:
@@ -87,7 +91,8 @@ class NativeScheduler:
         if rc != binding.OK:
             raise binding.PkvError("pkv_sched_add_request", rc)
         self.max_reqs += 1
-        self.max_pages = max(self.max_pages, -(-(history + prompt + decodes) // 16))
+        self._total[rid] = history + prompt + decodes
+        self.max_pages = max(self.max_pages, -(-self._total[rid] // 16))
 
     def add_prompt(self, rid: int, tokens, decodes: int) -> int:
         """Add a request with known prompt token ids (prefix caching); returns the number
@@ -98,8 +103,20 @@ class NativeScheduler:
         if rc < 0:
             raise binding.PkvError("pkv_sched_add_prompt", rc)
         self.max_reqs += 1
-        self.max_pages = max(self.max_pages, -(-(len(t) + decodes) // 16))
+        self._total[rid] = len(t) + decodes
+        self.max_pages = max(self.max_pages, -(-self._total[rid] // 16))
         return rc
+
+    def fork(self, parent_rid: int, rid: int, decodes: int) -> None:
+        """Add request ``rid`` continuing from everything ``parent_rid`` has cached, with
+        ``decodes`` generated tokens of its own; pages are shared and copied on write."""
+        rc = self._lib.pkv_sched_fork(self._h, parent_rid, rid, decodes)
+        if rc != binding.OK:
+            raise binding.PkvError("pkv_sched_fork", rc)
+        self.max_reqs += 1
+        # the child holds at most the parent's whole sequence plus its own tokens
+        self._total[rid] = self._total[parent_rid] + decodes
+        self.max_pages = max(self.max_pages, -(-self._total[rid] // 16))
 
     def sort_by_length(self) -> None:
         """Order the requests whose prompt has not started by the prompt tokens still to
@@ -121,18 +138,22 @@ class NativeScheduler:
         arr = {n: np.zeros(R + (n == "q_offsets"), np.int32)
                for n in ("rids", "q_lens", "context_lens", "q_offsets")}
         bt = np.zeros(R * P, np.int32)
+        C = R  # at most one page copy per request and step
+        cp = np.zeros((2, C), np.int32)
         ptr = lambda a: a.ctypes.data_as(_I32P)
         plan = _Plan(R, P, ptr(arr["rids"]), ptr(arr["q_lens"]), ptr(arr["context_lens"]),
-                     ptr(arr["q_offsets"]), ptr(bt), 0, 0, 0, 0, 0)
+                     ptr(arr["q_offsets"]), ptr(bt), 0, 0, 0, 0, 0, C, ptr(cp[0]), ptr(cp[1]),
+                     0)
         rc = fn(self._h, *args, ctypes.byref(plan))
         if rc < 0:
             raise binding.PkvError(fn.__name__, rc)
         if rc == 0:
             return None
         n, w = plan.num_reqs, max(1, plan.pages_used)
+        copies = np.ascontiguousarray(cp[:, :plan.num_copies].T) if plan.num_copies else None
         return StepPlan([int(x) for x in arr["rids"][:n]], arr["q_lens"][:n].copy(),
                         arr["context_lens"][:n].copy(), arr["q_offsets"][:n + 1].copy(),
-                        np.ascontiguousarray(bt.reshape(R, P)[:n, :w]))
+                        np.ascontiguousarray(bt.reshape(R, P)[:n, :w]), copies)
 
     def history_plan(self) -> Optional[StepPlan]:
         return self._call(self._lib.pkv_sched_history_plan, 1 if self._interleave else 0)

@@ -134,6 +134,15 @@ class PagedKV:
             binding.paged_attention_run(desc, q, self.k_cache, self.v_cache, out, scale, ws,
                                         self.err, stream)
 
+    def copy_pages(self, ds: DeviceStep, stream=None) -> None:
+        """The step's copy-on-write page copies (plan.copies), before its kv_append."""
+        c = ds.plan.copies
+        if c is None or len(c) == 0:
+            return
+        cd = torch.from_numpy(np.ascontiguousarray(c.T)).to(self.device)
+        binding.copy_pages(ds.desc, cd[0], cd[1], self.k_cache, self.v_cache, self.kv_int8,
+                           self.err, stream)
+
     def append(self, ds: DeviceStep, k_new: torch.Tensor, v_new: torch.Tensor,
                slot_mapping: Optional[torch.Tensor] = None, stream=None) -> None:
         self.append_desc(ds.desc, k_new, v_new, slot_mapping, stream)
@@ -463,5 +472,6 @@ def load_history(kv: PagedKV, workload, plan: Optional[StepPlan]) -> None:
 def run_step(kv: PagedKV, workload, plan: StepPlan) -> torch.Tensor:
     q, k, v = step_host_inputs(workload, plan)
     ds = kv.upload(plan)
+    kv.copy_pages(ds)
     kv.append(ds, bits_to_tensor(k, workload.dtype), bits_to_tensor(v, workload.dtype))
     return kv.attention(ds, bits_to_tensor(q, workload.dtype), workload.scale)

@@ -81,6 +81,9 @@ class StepPlan:
     context_lens: np.ndarray   # int32 [B]
     q_offsets: np.ndarray      # int32 [B+1]
     block_table: np.ndarray    # int32 [B, max_pages]
+    # page copies to run before the step's kv_append (copy-on-write of shared pages):
+    # int32 [n, 2] rows (source page, destination page), or None
+    copies: Optional[np.ndarray] = None
 
     @property
     def num_reqs(self) -> int:

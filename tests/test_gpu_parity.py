@@ -497,6 +497,82 @@ def test_prefix_cache_reuse_matches_oracle():
             assert np.array_equal(vc[page, :, p_ % 16], v[p_]), (r, p_)
 
 
+def test_forked_requests_copy_the_shared_partial_page_on_write():
+    # parallel samples of one prompt (pkv_sched_fork): a 100-token prompt leaves 4 tokens in
+    # its 7th page; two forks share every page with it, and the three then decode 20 tokens
+    # each, diverging inside that page.  The first writers get copies of the shared page
+    # (pkv_copy_pages before the step's append), the last holder writes in place.  Every row
+    # must match the oracle over the request's own sequence (the shared 100 prompt tokens,
+    # then its own tokens), and every slot of every request's pages must hold its K/V.
+    from paged_kv_cache_token_gb300.native_scheduler import NativeScheduler
+    hq, hkv, d, P, n_dec = 8, 2, 128, 100, 20
+    rng = np.random.default_rng(31)
+    draw = lambda *shape: runner.tensor_to_bits(
+        torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16))
+    kp, vp, qp = draw(P, hkv, d), draw(P, hkv, d), draw(P, hq, d)
+    specs = [W.RequestSpec(r, 0, P, n_dec) for r in range(3)]
+    pages = 3 * -(-(P + n_dec) // 16) + 4
+    w = W.Workload(910, "fork", hq, hkv, d, 0, specs, np.arange(pages, dtype=np.int32), pages)
+    for r in range(3):
+        k = np.concatenate([kp, draw(n_dec, hkv, d)])
+        v = np.concatenate([vp, draw(n_dec, hkv, d)])
+        w._cache[("kv", r)] = (k, v)
+        w._cache[("q", r)] = np.concatenate([qp, draw(n_dec, hq, d)])
+    s = NativeScheduler([], w.page_order, 256)
+    s.add_request(0, 0, P, n_dec)
+    kv = runner.paged_kv_for(w)
+    plan = s.next_step()                      # the prompt, one chunk
+    out = runner.run_step(kv, w, plan)
+    assert_close(gpu_as_f64(out), oracle_rows(w, plan), "prompt")
+    s.fork(0, 1, n_dec)
+    s.fork(0, 2, n_dec)
+    tables, copied = {}, 0
+    while True:
+        plan = s.next_step()
+        if plan is None:
+            break
+        copied += 0 if plan.copies is None else len(plan.copies)
+        out = runner.run_step(kv, w, plan)
+        assert kv.read_error() == 0
+        assert_close(gpu_as_f64(out), oracle_rows(w, plan), "forked decode step")
+        for j, rid in enumerate(plan.rids):
+            tables[rid] = plan.block_table[j].copy()
+    assert copied == 2
+    assert len({int(tables[r][6]) for r in range(3)}) == 3    # the partial page diverged
+    assert len({tuple(tables[r][:6]) for r in range(3)}) == 1  # full pages still shared
+    kc, vc = pool_bits(kv)
+    for r in range(3):
+        k, v = w.kv(r)
+        for pos in range(P + n_dec):
+            page = tables[r][pos // 16]
+            assert np.array_equal(kc[page, :, pos % 16], k[pos]), (r, pos)
+            assert np.array_equal(vc[page, :, pos % 16], v[pos]), (r, pos)
+
+
+def test_copy_pages_bit_exact_and_bad_ids_flagged():
+    # whole-page copies in both pool kinds, bit for bit; an out-of-range id is flagged and
+    # its copy skipped
+    for kv_int8 in (False, True):
+        sc = np.full((4, 64), 0.03, np.float32) if kv_int8 else None
+        kv = runner.PagedKV(10, 8, 4, 64, 1, k_scale=sc, v_scale=sc)
+        g = torch.Generator(device="cuda").manual_seed(3)
+        kb, vb = kv.k_cache.view(torch.uint8), kv.v_cache.view(torch.uint8)
+        for t in (kb, vb):
+            t.copy_(torch.randint(0, 256, t.shape, generator=g, device="cuda",
+                                  dtype=torch.uint8))
+        k0, v0 = kb.clone(), vb.clone()
+        plan = make_plan([0], [1], [0], [[0]])
+        ds = kv.upload(plan)
+        src = torch.tensor([1, 4, 7, 2], dtype=torch.int32, device="cuda")
+        dst = torch.tensor([5, 9, 0, 12], dtype=torch.int32, device="cuda")  # 12: out of pool
+        binding.copy_pages(ds.desc, src, dst, kv.k_cache, kv.v_cache, kv_int8, kv.err)
+        assert kv.read_error() & binding.DEVERR_PAGE_RANGE
+        ek, ev = k0.clone(), v0.clone()
+        for a, b in ((1, 5), (4, 9), (7, 0)):
+            ek[b], ev[b] = k0[a], v0[a]
+        assert torch.equal(kb, ek) and torch.equal(vb, ev)
+
+
 def test_block_table_permutation_bitwise_identical():
     base = custom(400, 32, 8, 128, 0, [(c, 0, 1) for c in (50, 700, 2100, 16)])
     outs = []

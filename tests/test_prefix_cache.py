@@ -122,3 +122,76 @@ def test_referenced_blocks_are_never_evicted():
         s.next_step()
     assert e.value.status == -7
     assert s.cached_blocks == 2
+
+
+# ------------------------------------------------------------------ fork + copy-on-write
+def test_fork_shares_pages_and_copies_the_partial_page_on_first_write():
+    # A's 100-token prompt fills 6 pages and 4 slots of a 7th; B and C fork from it and all
+    # three decode: the first two to write into the shared 7th page get copies of it, the
+    # last holder writes in place; the full pages stay shared
+    s = planner(pages=40)
+    s.add_request(0, 0, 100, 3)
+    p = s.next_step()
+    a_pages = list(p.block_table[0][:7])
+    s.fork(0, 1, 3)
+    s.fork(0, 2, 3)
+    p = s.next_step()
+    assert list(p.rids) == [0, 1, 2] and list(p.context_lens) == [100, 100, 100]
+    assert p.copies is not None and p.copies.shape == (2, 2)
+    assert list(p.copies[:, 0]) == [a_pages[6], a_pages[6]]
+    fresh = list(p.copies[:, 1])
+    assert len(set(fresh)) == 2 and not set(fresh) & set(a_pages)
+    for i in range(3):
+        assert list(p.block_table[i][:6]) == a_pages[:6]     # full pages still shared
+    assert [p.block_table[i][6] for i in range(3)] == fresh + [a_pages[6]]
+    p = s.next_step()                                        # no shared partial page left
+    assert p.copies is None
+
+
+def test_fork_at_a_page_boundary_needs_no_copy_and_release_returns_every_page():
+    s = planner(pages=40)
+    s.add_request(0, 0, 96, 2)                               # exactly 6 pages
+    s.next_step()
+    s.fork(0, 1, 2)
+    free0 = s.num_free
+    p = s.next_step()                                        # both start page 7: fresh pages
+    assert p.copies is None
+    assert p.block_table[0][6] != p.block_table[1][6]
+    assert s.num_free == free0 - 2
+    s.next_step()
+    assert s.next_step() is None
+    s.release(0)                                             # shared pages stay with 1
+    assert s.num_free == free0 - 2 + 1
+    s.release(1)
+    assert s.num_free == 40
+
+
+def test_fork_release_order_and_copy_capacity():
+    s = planner(pages=12)
+    s.add_request(0, 0, 40, 1)                               # 2 full pages + 8 slots
+    s.next_step()
+    for c in (1, 2, 3):
+        s.fork(0, c, 1)
+    p = s.next_step()                                        # 3 copies of page 3
+    assert p.copies.shape == (3, 2)
+    assert s.next_step() is None
+    for r in (2, 0, 3, 1):
+        s.release(r)
+    assert s.num_free == 12                                  # every page back exactly once
+
+
+def test_fork_errors_and_no_pages_leaves_state():
+    s = planner(pages=4)
+    s.add_request(0, 0, 20, 2)
+    with pytest.raises(binding.PkvError):
+        s.fork(0, 1, 1)                                      # parent still prefilling
+    s.next_step()                                            # 20 tokens: 2 pages
+    with pytest.raises(binding.PkvError):
+        s.fork(7, 1, 1)                                      # unknown parent
+    s.fork(0, 1, 4)
+    s.fork(0, 2, 4)
+    s.fork(0, 3, 4)
+    # 4 requests write into the shared 2nd page: 3 copies, but only 2 pages are free
+    with pytest.raises(binding.PkvError):
+        s.next_step()
+    assert s.num_free == 2                                  # nothing was taken
