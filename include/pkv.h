@@ -195,7 +195,7 @@ PKV_API int pkv_paged_attention_run(const pkv_step_desc* desc, const void* q,
  * device (cudaMalloc and cudaFree can synchronise it), and runtimes that hand out all
  * device memory once at start-up and allow no allocation afterwards.  This entry point
  * allocates nothing: its scratch (the work list and split-KV partial results) lives in a
- * fixed array compiled into the library, PKV_STATIC_WORKSPACE_BYTES (16 MiB) on every GPU
+ * fixed array compiled into the library, PKV_STATIC_WORKSPACE_BYTES (32 MiB) on every GPU
  * that loads the library, held until the process exits.  The pages have no counterpart to
  * this call; it only changes where the scratch memory comes from.
  *   Arguments and results are those of pkv_paged_attention_step without the workspace.
@@ -209,7 +209,7 @@ PKV_API int pkv_paged_attention_run(const pkv_step_desc* desc, const void* q,
  *   that overlap on the GPU -- on different streams, or from several host threads without
  *   ordering -- race on the array: issue them in order on one stream.
  */
-#define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
+#define PKV_STATIC_WORKSPACE_BYTES (32u << 20)
 PKV_API int pkv_paged_attention_step_static_ws(const pkv_step_desc* desc, const void* q,
                                                const void* k_cache, const void* v_cache,
                                                void* out, float scale, int32_t* dev_err_flag,

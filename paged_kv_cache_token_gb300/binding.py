@@ -262,7 +262,7 @@ def paged_attention_step_int8(desc: StepDesc, q, k_cache, v_cache, k_scale, v_sc
     return rc
 
 
-STATIC_WORKSPACE_BYTES = 16 << 20
+STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 def paged_attention_step_static_ws(desc: StepDesc, q, k_cache, v_cache, out, scale: float,

@@ -1,7 +1,9 @@
 // C ABI of libpkv.so: argument checks on the host, then kernel launches on the caller's
 // stream.  Declarations and the contract of every entry point are in include/pkv.h.
 #include <algorithm>
+#include <atomic>
 #include <climits>
+#include <random>
 #include <cstdint>
 
 #include "launch.h"
@@ -64,6 +66,21 @@ int check_desc(const pkv_step_desc* d) {
 // Requests with at least this many new tokens take the tensor-core prefill path (128-row
 // query tiles); shorter multi-token requests run row by row on the streaming path.
 int prefill_min_q() { return 16; }
+
+// Tags of attention calls (see StepArgs::epoch): 40-bit values, never 0, from a start chosen
+// at random per process so that a workspace's earlier contents are unlikely to hold one.
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> counter{[] {
+        std::random_device rd;
+        return (static_cast<unsigned long long>(rd()) << 20) ^ rd();
+    }()};
+    const unsigned long long kMask = (1ull << 40) - 1;
+    unsigned long long e;
+    do {
+        e = counter.fetch_add(1, std::memory_order_relaxed) & kMask;
+    } while (e == 0);
+    return e;
+}
 
 thread_local cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
 
@@ -264,7 +281,11 @@ int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache
     a.overlap = lay.max_tiles > 0 && lay.max_items > 0 ? 1 : 0;
     a.plan_wait_first = phase == Phase::kPlanOnly ? 1 : 0;
     a.plan_ready = phase == Phase::kRunOnly ? 1 : 0;
-    if (phase != Phase::kRunOnly && (rc = pkv::launch_plan(a, s)) != PKV_OK) return rc;
+    a.self_plan = lay.self_plan;
+    a.epoch = a.self_plan ? next_epoch() : 0;
+    // a self-planned step has nothing to plan ahead: its decode kernel plans for itself
+    if (phase != Phase::kRunOnly && !a.self_plan && (rc = pkv::launch_plan(a, s)) != PKV_OK)
+        return rc;
     if (phase == Phase::kPlanOnly) return PKV_OK;
     if (a.overlap &&
         (rc = pkv::launch_prefill(a, s, g_events[1][0], g_events[1][1])) != PKV_OK)

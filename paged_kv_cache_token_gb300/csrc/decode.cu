@@ -46,6 +46,9 @@ constexpr int kMinSplitPages = 4;
 constexpr int kItemsPerWarp = 6;  // target decode items per resident warp
 constexpr int kManySplits = 64;   // rows that may have more splits get a grouped combine
 constexpr int kChunkedCtas = 4096;  // largest grid of the two-pass combine
+constexpr int kDecMaxCtasPerSm = 3;  // decode CTAs an SM can hold (INT8 pages)
+constexpr int kMinChunkPages = 4;    // smallest dynamic chunk of a self-planned step
+constexpr int kSlotsPerWarp = 6;     // partial slots a self-planned step may use per warp
 
 template <typename T>
 __device__ __forceinline__ T* ws_at(const StepArgs& a, size_t off) {
@@ -279,9 +282,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(StepArgs a) {
         __syncthreads();
     }
     // the plan ran alongside this step's kv_append; finish only after it (so a kernel that
-    // waits for the plan also sees the appended K/V), then let the attention kernels start
+    // waits for the plan also sees the appended K/V), then let the attention kernels start.
+    // A plan launched on its own does not let the next kernel start early: a run over it
+    // reads the work list before its own wait, so the list must be complete when that
+    // kernel launches.
     pdl_wait();
-    pdl_trigger();
+    if (!a.plan_wait_first) pdl_trigger();
     if (tid == 0 && blockIdx.x == 0) {
         if (overflow) set_error(a.err, PKV_DEVERR_TOKENS);  // host maxima were wrong
         ctrl[0] = 0;
@@ -370,6 +376,53 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     return y;
 }
 
+// Units of a self-planned step: nw static units of `static_pages` pages (the fraction
+// num / den of the total, rounded down), then chunks of `chunk_pages` pages.  Every unit has
+// two partial slots, so the chunks are no smaller than the workspace's slots allow.
+// Measured on the decode batches (A/B in one process): 16-bit pages do best with 3/4 static
+// and chunks of at least 4 pages (the warps' streaming rates differ by about +-8%, and the
+// chunks even out the tail); INT8 pages with everything static (a piece's setup -- q times
+// the key scales -- costs too much for small chunks), the remainder only in chunks.
+struct SelfPlanUnits { int static_pages, chunk_pages, chunks; };
+__device__ __forceinline__ SelfPlanUnits self_plan_units(int total, int nw, int slots, int num,
+                                                         int den) {
+    SelfPlanUnits u;
+    u.static_pages = static_cast<int>(static_cast<int64_t>(total) * num /
+                                      (static_cast<int64_t>(den) * nw));
+    const int dyn = total - nw * u.static_pages;
+    const int max_chunks = max(1, slots / 2 - nw);
+    u.chunk_pages = max(kMinChunkPages, cdiv(dyn, max_chunks));
+    u.chunks = cdiv(dyn, u.chunk_pages);
+    return u;
+}
+
+// The chunk counter of a self-planned step is one 64-bit word: the call's epoch (40 bits,
+// from the host, never 0) above a 24-bit count, so the workspace needs no initialisation.
+// Every CTA tries once, in its prologue, to move the word from an earlier call's epoch (or
+// 0, where the combine parks it) to this call's with a zero count; claims, long after, are
+// then single atomic adds.
+__device__ __forceinline__ void install_epoch(unsigned long long* ctr, unsigned long long epoch) {
+    const unsigned long long cur = atomicAdd(ctr, 0ull);
+    if ((cur >> 24) != epoch) atomicCAS(ctr, cur, epoch << 24);
+}
+// The chunk a claim got: `old` is the word an atomic add of 1 returned.  A claim that still
+// found another epoch (no CTA's install had landed) moves the word itself, taking chunk 0,
+// or claims again once another thread has; bounded: after kWaitLimit failed swaps it gives
+// up (no more chunks) and sets PKV_DEVERR_TIMEOUT.
+__device__ __forceinline__ int claimed_chunk(unsigned long long* ctr, unsigned long long old,
+                                             unsigned long long epoch, int32_t* err) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if ((old >> 24) == epoch) return static_cast<int>(old & 0xffffffull);
+        const unsigned long long expected = old + 1;  // the word after this thread's add
+        const unsigned long long prev = atomicCAS(ctr, expected, (epoch << 24) | 1ull);
+        if (prev == expected) return 0;
+        // another thread moved or bumped the word: claim again on its current value
+        old = (prev >> 24) == epoch ? atomicAdd(ctr, 1ull) : prev - 1;
+    }
+    set_error(err, PKV_DEVERR_TIMEOUT);
+    return INT_MAX;
+}
+
 // One work item as a warp sees it.
 struct DecItem {
     int idx;        // queue position; >= count when none
@@ -404,21 +457,102 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         fence_barrier_init();
     }
     __syncwarp();
+    const int nwarps = static_cast<int>(gridDim.x) * kDecWarps;  // workers in the grid
+    const int gw = static_cast<int>(blockIdx.x) * kDecWarps + warp;
+    const int Hkv = a.num_kv_heads, Hq = a.num_q_heads;
+
+    // ---- self-planned steps (every request advances by at most one token, few requests):
+    //      the CTA plans the step itself from the lengths, before its dependency wait (they
+    //      were final before this step's kv_append started).  The work is the sequence of
+    //      (request, KV head) segments of the requests' pages, in request order -- request
+    //      r's head g covers pages [seg0[r] + g P_r, seg0[r] + (g + 1) P_r) with P_r its
+    //      pages.  A share of the T pages is cut into nw equal static units, one per warp;
+    //      the rest into small chunks that warps take from a counter once their own unit is
+    //      done, which evens out the warps' different streaming rates (self_plan_units).
+    //      A warp's pieces are the segments a unit meets; a piece that is not a whole
+    //      segment leaves a partial in slot 2u (the unit's first piece) or 2u + 1 (its
+    //      last).  No work records and no separate plan launch.
+    __shared__ int s_seg0[kSelfPlanMaxReqs + 1];
+    __shared__ int s_tok[kSelfPlanMaxReqs];
+    __shared__ int s_keys[kSelfPlanMaxReqs];
+    __shared__ int s_wsum[kDecWarps];
+    __shared__ int s_bad;
+    int sp_total = 0, sp_nw = 0, sp_static = 0, sp_chunk = 1, sp_chunks = 0, sp_unit = -1;
+    int range_start = 0, range_end = 0;  // the unit this warp works through (T < 2^30)
+    if (a.self_plan) {
+        const int tid = threadIdx.x;
+        if (tid == 0)
+            s_bad = (a.q_offsets[0] != 0 || a.q_offsets[a.num_reqs] != a.total_q_tokens) ? 1 : 0;
+        __syncthreads();
+        // request tid + 128 k of the first / second half: its segments' total pages
+        int pages[2] = {0, 0};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = tid + k * kDecThreads;
+            if (r < a.num_reqs) {
+                const ReqLens L = load_request(a, r);
+                if (!L.ok) atomicOr(&s_bad, 1);
+                s_tok[r] = L.t0;
+                s_keys[r] = L.c + 1;
+                pages[k] = (L.ok && L.q == 1) ? cdiv(L.c + 1, kPage) * Hkv : 0;
+            }
+        }
+        // exclusive scan over requests 0..255 in order: the first half, then the second
+        int run = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            int incl = pages[k];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) s_wsum[warp] = incl;
+            __syncthreads();
+            int before = run;
+            for (int w = 0; w < warp; ++w) before += s_wsum[w];
+            int half = 0;
+            for (int w = 0; w < kDecWarps; ++w) half += s_wsum[w];
+            const int r = tid + k * kDecThreads;
+            if (r < a.num_reqs) s_seg0[r] = before + incl - pages[k];
+            run += half;
+            __syncthreads();
+        }
+        if (tid == 0) s_seg0[a.num_reqs] = run;
+        __syncthreads();
+        if (tid == 0)
+            install_epoch(reinterpret_cast<unsigned long long*>(
+                              ws_at<int32_t>(a, a.lay.ctrl) + 10), a.epoch);
+        sp_total = s_bad ? 0 : run;
+        // two partial slots per working warp, within the workspace's slots (a third of them
+        // at most; the rest serve the chunks)
+        sp_nw = min(min(nwarps, sp_total), a.lay.max_items / kSlotsPerWarp);
+        if (sp_nw > 0) {
+            const SelfPlanUnits u = self_plan_units(sp_total, sp_nw, a.lay.max_items,
+                                                    Q8 ? 1 : 3, Q8 ? 1 : 4);
+            sp_static = u.static_pages;
+            sp_chunk = u.chunk_pages;
+            sp_chunks = u.chunks;
+            if (gw < sp_nw) {
+                range_start = gw * sp_static;
+                range_end = range_start + sp_static;
+                sp_unit = gw;
+            }
+        }
+    }
     // The plan must be complete before the work list is read, and this step's kv_append
     // before the pages are.  Behind a prefill grid both completed before any prefill CTA
     // passed its own wait, and this grid launched only after every prefill CTA had started.
     // Over a plan made by an earlier call the plan completed before this step's kv_append
     // started, so only the pages wait (below).  Otherwise the plan is this grid's
     // predecessor and completes after the kv_append.
-    if (!a.overlap && !a.plan_ready) pdl_wait();
+    if (!a.overlap && !a.plan_ready && !a.self_plan) pdl_wait();
 
     int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
-    const int num_items = ctrl[1];
-    const int nwarps = static_cast<int>(gridDim.x) * kDecWarps;  // workers in the grid
+    const int num_items = a.self_plan ? 0 : ctrl[1];
     const int4* items = ws_at<const int4>(a, a.lay.items);
     float2* part_ml = ws_at<float2>(a, a.lay.part_ml);
     float* part_o = ws_at<float>(a, a.lay.part_o);
-    const int Hkv = a.num_kv_heads, Hq = a.num_q_heads;
     const uint8_t* kc = static_cast<const uint8_t*>(a.k_cache);
     const uint8_t* vc = static_cast<const uint8_t*>(a.v_cache);
     // K/V pages are read once per step: evict them first so the split partials written
@@ -490,30 +624,117 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         if (lane == 0) idx = atomicAdd(&ctrl[0], 1) + 2 * nwarps;
         return idx;
     };
+    // self-planned steps: the piece of this warp's range that starts at flattened page `pos`
+    auto make_piece = [&](int pos) {
+        DecItem it{};
+        it.ns = 1;
+        if (pos >= range_end) return it;  // np = 0: none
+        const int p = pos;
+        int lo = 0, hi = a.num_reqs - 1;  // last request whose segments start at or before p
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_seg0[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        const int r = lo, per = cdiv(s_keys[r], kPage);
+        const int g = (p - s_seg0[r]) / per;
+        const int seg = s_seg0[r] + g * per;
+        const int end = min(seg + per, range_end);
+        it.t = s_tok[r];
+        it.g = g;
+        it.pb = p - seg;
+        it.np = end - p;
+        it.nkv = s_keys[r];
+        it.r = r;
+        it.ns = (p == seg && end == seg + per) ? 1 : 2;  // a whole segment writes its row
+        it.base = 2 * sp_unit + (pos == range_start ? 0 : 1);  // unit's first / last piece
+        it.s = 0;
+        return it;
+    };
+    int sp_pos = range_start;  // self-planned: where the warp's next piece starts
+    unsigned long long* chunk_ctr = reinterpret_cast<unsigned long long*>(ctrl + 10);
+    // a chunk claim is issued when a unit's last piece is made and read one piece later, so
+    // the atomic's round trip overlaps the streaming (lane 0 holds the returned word)
+    unsigned long long claim_word = 0;
+    bool claim_pending = false;
+    auto issue_claim = [&]() {
+        if (lane == 0) claim_word = atomicAdd(chunk_ctr, 1ull);
+        claim_pending = true;
+    };
+    auto next_piece = [&]() {
+        if (sp_pos >= range_end && sp_unit >= 0) {
+            // this unit is done: take the chunk claimed for it (lane 0, the warp follows)
+            if (!claim_pending) issue_claim();
+            int k = 0;
+            if (lane == 0) k = claimed_chunk(chunk_ctr, claim_word, a.epoch, a.err);
+            k = __shfl_sync(kFull, k, 0);
+            claim_pending = false;
+            if (k < sp_chunks) {
+                sp_unit = sp_nw + k;
+                range_start = sp_nw * sp_static + k * sp_chunk;
+                range_end = min(range_start + sp_chunk, sp_total);
+                sp_pos = range_start;
+            } else {
+                sp_unit = -1;
+                range_end = range_start = sp_pos;
+            }
+        }
+        const DecItem it = make_piece(sp_pos);
+        sp_pos += it.np;
+        if (it.np > 0 && sp_pos >= range_end && !claim_pending) issue_claim();
+        return it;
+    };
 
     // prime the pipeline: a warp's first two items are fixed by its index (no queue round
     // trip before the first copy); later ones come from the queue, numbered after them
-    const int i0 = static_cast<int>(blockIdx.x) * kDecWarps + warp;
+    const int i0 = gw;
     const int i1 = i0 + nwarps;
     int4 ra, rb;
-    load_record(i0, ra, rb);
-    DecItem cur = resolve(i0, ra, rb);
-    load_record(i1, ra, rb);
-    DecItem nxt = resolve(i1, ra, rb);
+    DecItem cur, nxt;
+    if (a.self_plan) {
+        cur = next_piece();
+        nxt = next_piece();
+    } else {
+        load_record(i0, ra, rb);
+        cur = resolve(i0, ra, rb);
+        load_record(i1, ra, rb);
+        nxt = resolve(i1, ra, rb);
+    }
     int cur_win = load_window(cur, 0), cur_win_base = 0;
     int nxt_win = load_window(nxt, 0);
+    // Over an earlier plan only the work list (written by a plan that completed before this
+    // grid launched) and the block table were read so far.  The preceding kernel may still
+    // be writing anything else -- the pages of this step's kv_append, or, when it is the
+    // previous layer's combine, the queue counter it rewinds -- so the queue and q wait.
+    if (!a.overlap && (a.plan_ready || a.self_plan)) pdl_wait();
+    pdl_trigger();  // the combine may be scheduled; it waits for this grid to finish
+    if (a.self_plan && blockIdx.x == 0) {
+        // what the combine needs: per request {token, first segment page, keys, pages per
+        // head}, the totals (every earlier kernel has completed: the workspace is free)
+        int4* rec = ws_at<int4>(a, a.lay.req_info);
+        for (int r = threadIdx.x; r < a.num_reqs; r += kDecThreads)
+            rec[r] = make_int4(s_tok[r], s_seg0[r], s_keys[r],
+                               (s_seg0[r + 1] - s_seg0[r]) / Hkv);
+        if (threadIdx.x == 0) {
+            if (s_bad) set_error(a.err, PKV_DEVERR_TOKENS);
+            ctrl[1] = sp_total;
+            ctrl[2] = s_bad ? 0 : a.num_reqs;
+            ctrl[4] = sp_nw;
+            ctrl[5] = sp_static;
+            ctrl[6] = sp_chunk;
+        }
+    }
     // the next item's q is prefetched when the registers allow (not for 8 x 128-dim heads)
     constexpr bool kPrefetchQ = NQ <= 8;
     uint4 q_cur[NQ], q_nxt[kPrefetchQ ? NQ : 1];
     load_q(cur, q_cur);
     if constexpr (kPrefetchQ) load_q(nxt, q_nxt);
-    int p2_idx = __shfl_sync(kFull, claim(), 0);
+    int p2_idx = 0, p3_lane0 = 0;
     int4 p2a, p2b;
-    load_record(p2_idx, p2a, p2b);
-    int p3_lane0 = claim();
-    // over an earlier plan: the pages of this step's kv_append are final only now
-    if (!a.overlap && a.plan_ready) pdl_wait();
-    pdl_trigger();  // the combine may be scheduled; it waits for this grid to finish
+    if (!a.self_plan) {
+        p2_idx = __shfl_sync(kFull, claim(), 0);
+        load_record(p2_idx, p2a, p2b);
+        p3_lane0 = claim();
+    }
     uint32_t issued = 0, consumed = 0;  // ring counters
     bool aborted = false;
     int ic = 0;          // pages of `cur` issued so far
@@ -906,12 +1127,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         }
         ic = in_nxt;
         in_nxt = 0;
-        nxt = resolve(p2_idx, p2a, p2b);
+        if (a.self_plan) {
+            nxt = next_piece();
+        } else {
+            nxt = resolve(p2_idx, p2a, p2b);
+        }
         nxt_win = load_window(nxt, 0);
         if constexpr (kPrefetchQ) load_q(nxt, q_nxt);
-        p2_idx = __shfl_sync(kFull, p3_lane0, 0);
-        load_record(p2_idx, p2a, p2b);
-        p3_lane0 = claim();
+        if (!a.self_plan) {
+            p2_idx = __shfl_sync(kFull, p3_lane0, 0);
+            load_record(p2_idx, p2a, p2b);
+            p3_lane0 = claim();
+        }
         while (issued - consumed < static_cast<uint32_t>(kNst)) {
             const uint32_t before = issued;
             issue_one();
@@ -951,9 +1178,26 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 enum : int { kCombineRow = 0, kCombineChunks = 1, kCombineParts = 2 };
 constexpr int kCombineChunk = 64;
 
-template <typename T, int D, int G, int NG>
-__device__ __forceinline__ void combine_fold(const StepArgs& a, int64_t base, int first,
-                                             int count, int stride, bool to_out, int t, int g,
+// Slots of a (row, KV head)'s splits: base + first + i * stride.
+struct SlotRun {
+    int64_t base;
+    int first, stride;
+    __device__ int64_t operator()(int i) const {
+        return base + first + static_cast<int64_t>(i) * stride;
+    }
+};
+// Slots of a self-planned segment's pieces (see combine_pieces_kernel): slot0 for the
+// first, then consecutive slots from next.
+struct SlotPieces {
+    int64_t slot0, next, stride;
+    __device__ int64_t operator()(int i) const {
+        return i == 0 ? slot0 : next + (i - 1) * stride;
+    }
+};
+
+template <typename T, int D, int G, int NG, typename SlotFn>
+__device__ __forceinline__ void combine_fold(const StepArgs& a, SlotFn slot_of, int count,
+                                             bool to_out, int t, int g,
                                              float2 (*s_ml)[G * D / 4],
                                              float4 (*s_acc)[G * D / 4]) {
     using Cv = F16<T>;
@@ -973,7 +1217,7 @@ __device__ __forceinline__ void combine_fold(const StepArgs& a, int64_t base, in
         for (int u = 0; u < kBatch; ++u) {
             const int i = i0 + u * NG;
             if (i < count) {
-                const int64_t slot = base + first + static_cast<int64_t>(i) * stride;
+                const int64_t slot = slot_of(i);
                 ml[u] = part_ml[slot * G + j];
                 o[u] = *reinterpret_cast<const float4*>(part_o + (slot * G + j) * D + dim);
             }
@@ -1027,7 +1271,7 @@ __device__ __forceinline__ void combine_fold(const StepArgs& a, int64_t base, in
     } else {
         // the chunk's state replaces its first split's: every read of that slot happened
         // before the barrier above
-        const int64_t slot = base + first;
+        const int64_t slot = slot_of(0);
         part_ml[slot * G + j] = make_float2(M, L);
         *reinterpret_cast<float4*>(part_o + (slot * G + j) * D + dim) = acc;
     }
@@ -1042,6 +1286,9 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
     int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
     const int4* rows = ws_at<const int4>(a, a.lay.rows);  // {token, first slot, keys, splits}
     pdl_wait();  // the previous grid (decode kernel or chunk pass) has finished its writes
+    // the next kernel on the stream may be scheduled now; it waits for this grid to finish
+    // before it touches memory
+    pdl_trigger();
     // the decode grid has completed, so nothing claims work items any more: rewind the queue
     // so the next attention call over the same plan (another layer) starts from item 0
     if (Stage != kCombineParts && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
@@ -1055,21 +1302,64 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
         if (ns <= 1) continue;  // finished in place by the decode kernel
         const int64_t base = row.y + static_cast<int64_t>(g) * ns;
         if constexpr (Stage == kCombineRow) {
-            combine_fold<T, D, G, NG>(a, base, 0, ns, 1, true, row.x, g, s_ml, s_acc);
+            combine_fold<T, D, G, NG>(a, SlotRun{base, 0, 1}, ns, true, row.x, g, s_ml, s_acc);
         } else if constexpr (Stage == kCombineChunks) {
             // the in-place chunk write relies on the barrier between the groups' reads and it
             static_assert(NG > 1, "the chunk pass needs more than one thread group");
             const int nch = cdiv(ns, kCombineChunk);
             for (int c = blockIdx.y; c < nch; c += gridDim.y) {  // uniform over the CTA
                 const int first = c * kCombineChunk;
-                combine_fold<T, D, G, NG>(a, base, first, min(kCombineChunk, ns - first), 1,
-                                          nch == 1, row.x, g, s_ml, s_acc);
+                combine_fold<T, D, G, NG>(a, SlotRun{base, first, 1},
+                                          min(kCombineChunk, ns - first), nch == 1, row.x, g,
+                                          s_ml, s_acc);
             }
         } else {
             if (ns <= kCombineChunk) continue;  // written by the chunk pass
-            combine_fold<T, D, G, NG>(a, base, 0, cdiv(ns, kCombineChunk), kCombineChunk,
-                                      true, row.x, g, s_ml, s_acc);
+            combine_fold<T, D, G, NG>(a, SlotRun{base, 0, kCombineChunk},
+                                      cdiv(ns, kCombineChunk), true, row.x, g, s_ml, s_acc);
         }
+    }
+}
+
+// Combine of a self-planned step.  Segment (request r, KV head g) covers flattened pages
+// [b, e) with b = seg0[r] + g P_r, e = b + P_r.  Unit u starts at u S (u < nw, S static
+// pages per warp) or nw S + (u - nw) C (chunks of C pages), so the segment meets units
+// u1 = unit(b) .. u2 = unit(e - 1).  One unit (u1 == u2) wrote the row itself.  Otherwise
+// the pieces are u1's first piece (slot 2 u1) when the unit starts exactly at b, else its
+// last (slot 2 u1 + 1), then the first piece of each later unit (slot 2 u).  NG thread
+// groups of a CTA share a pair's pieces, so even a segment that spans hundreds of units
+// (one dominant long row) is folded in a few rounds of loads.
+template <typename T, int D, int G, int NG>
+__global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_kernel(StepArgs a) {
+    constexpr int TPG = G * D / 4;
+    __shared__ float2 s_ml[NG > 1 ? NG : 1][TPG];
+    __shared__ float4 s_acc[NG > 1 ? NG : 1][TPG];
+    const int Hkv = a.num_kv_heads;
+    int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
+    const int4* rec = ws_at<const int4>(a, a.lay.req_info);  // {token, seg0, keys, pages}
+    pdl_wait();  // the decode grid has completed
+    // park the chunk counter at epoch 0, which no call uses, so the next call starts afresh;
+    // before the next kernel may launch, since a decode kernel can claim before its wait
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        atomicExch(reinterpret_cast<unsigned long long*>(ctrl + 10), 0ull);
+    __syncthreads();
+    pdl_trigger();
+    const int nreq = ctrl[2], nw = ctrl[4];
+    const int64_t S = ctrl[5], C = ctrl[6], D0 = static_cast<int64_t>(nw) * S;
+    auto unit = [&](int64_t p) -> int64_t { return p < D0 ? p / S : nw + (p - D0) / C; };
+    auto unit_start = [&](int64_t u) -> int64_t { return u < nw ? u * S : D0 + (u - nw) * C; };
+    for (int rh = blockIdx.x; rh < nreq * Hkv; rh += gridDim.x) {  // uniform over the CTA
+        const int r = rh / Hkv, g = rh % Hkv;
+        const int4 rr = rec[r];
+        const int per = rr.w;
+        if (per == 0) continue;
+        const int64_t b = static_cast<int64_t>(rr.y) + static_cast<int64_t>(g) * per;
+        const int64_t e = b + per;
+        const int64_t u1 = unit(b), u2 = unit(e - 1);
+        if (u1 == u2) continue;
+        const SlotPieces slots{2 * u1 + (unit_start(u1) == b ? 0 : 1), 2 * (u1 + 1), 2};
+        combine_fold<T, D, G, NG>(a, slots, static_cast<int>(u2 - u1 + 1), true, rr.x, g,
+                                  s_ml, s_acc);
     }
 }
 
@@ -1098,6 +1388,14 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
                              ((row_pages + kMinSplitPages - 1) / kMinSplitPages);
     const long long by_target = L.target_items + static_cast<long long>(L.max_rows) * num_kv_heads;
     L.max_items = L.max_rows ? static_cast<int>(std::min(by_len, by_target)) : 0;
+    // every request advances by at most one token and there are few requests: the decode
+    // kernel plans the step itself, with two partial slots per warp
+    const long long seg_pages = static_cast<long long>(num_reqs) * num_kv_heads *
+                                ((static_cast<long long>(max_context_len) + kPage) / kPage);
+    L.self_plan = L.max_rows > 0 && max_q_len <= 1 && num_reqs <= kSelfPlanMaxReqs &&
+                  seg_pages < INT_MAX / 2;
+    if (L.self_plan)
+        L.max_items = std::max(L.max_items, kSlotsPerWarp * kDecWarps * kDecMaxCtasPerSm * num_sms);
     const int prefill_reqs = max_q_len >= prefill_min_q
                                  ? std::min(num_reqs, total_q_tokens / std::max(1, prefill_min_q))
                                  : 0;
@@ -1158,7 +1456,11 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
     const int cap_big = std::min(rows_heads, 2 * a.num_sms);     // up to 1,024 threads
     const int chunks = cdiv(max_splits, kCombineChunk);
     cudaError_t e;
-    if (max_splits <= kManySplits) {
+    if (a.self_plan) {
+        const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
+        e = launch_pdl(combine_pieces_kernel<T, D, G, kNg>, dim3(std::min(pairs, 2 * a.num_sms)),
+                       dim3(kTpg * kNg), 0, stream, a);
+    } else if (max_splits <= kManySplits) {
         e = launch_pdl(combine_kernel<T, D, G, 1, kCombineRow>, dim3(cap_small), dim3(kTpg), 0,
                        stream, a);
     } else if (static_cast<long long>(rows_heads) * chunks <= kChunkedCtas) {

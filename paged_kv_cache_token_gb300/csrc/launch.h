@@ -37,10 +37,17 @@ struct AppendArgs {
 //   tiles     int4[max_tiles]  prefill tiles {request, q tile, query head (pair), 0}
 //   part_ml   float2[max_items * G]      per slot (running max in log2 units, sum)
 //   part_o    float[max_items * G * D]   per slot un-normalised outputs
+//   (a self-planned step -- self_plan below -- uses req_info for {token, first segment
+//   page, keys, pages per head} of every request, ctrl[1] / [2] / [4] for the total pages,
+//   the requests and the warps sharing them, and two partial slots per decode warp)
 struct WorkspaceLayout {
     size_t ctrl, req_info, rows, items, tiles, part_ml, part_o, total;
     int max_rows, max_items, max_tiles, target_items;
+    int self_plan;  // every request advances by <= 1 token, at most kSelfPlanMaxReqs of them
 };
+
+// requests a decode CTA plans for itself (one int per request in three shared arrays)
+constexpr int kSelfPlanMaxReqs = 256;
 
 struct StepArgs {
     int num_reqs, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages;
@@ -70,9 +77,16 @@ struct StepArgs {
     // waited for that writer before letting the plan start
     int plan_wait_first;
     // the work list in the workspace was planned before this call (pkv_paged_attention_run):
-    // the decode kernel may read it before its dependency wait, which then only guards the
-    // pages this step's kv_append wrote
+    // the decode kernel may read it (and the block table) before its dependency wait.  The
+    // plan kernel of pkv_plan_attention never lets its successor launch before it completes,
+    // so the list is complete by the time any later kernel launches.
     int plan_ready;
+    // the decode kernel plans the step itself (WorkspaceLayout::self_plan): no plan launch
+    int self_plan;
+    // this call's tag for the self-planned step's chunk counter: 40 bits, never 0, a new
+    // value for every call (a CUDA graph replays the captured values; the combine parks the
+    // counter at 0 after every call, so a replayed tag still starts afresh)
+    unsigned long long epoch;
     const float* k_scale;  // [Hkv][D], INT8 pools only
     const float* v_scale;
 };

@@ -105,7 +105,10 @@ prefill_q8_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_q) {
     constexpr uint32_t kIdescO = tc::idesc_f16(0, 0, kBM, D);   // B = V^T, K-major
 
     pdl_wait();  // the plan and kv_append (and the decode kernel, if it ran first) completed
-    if (a.overlap) pdl_trigger();  // the decode grid may launch once every CTA has started
+    // the next grid (the decode stream of a mixed step, or the next step's first kernel)
+    // may launch once every CTA has started; the decode kernel only waits for this grid at
+    // its end, any other kernel before it touches memory
+    pdl_trigger();
     const int32_t* ctrl = reinterpret_cast<const int32_t*>(a.ws + a.lay.ctrl);
     if (static_cast<int>(blockIdx.x) >= ctrl[9]) return;
 

@@ -103,7 +103,7 @@ def _big_desc(num_pages):
 
 
 def test_static_workspace_rejects_steps_beyond_its_size():
-    # more scratch than the 16 MiB array holds: refused on the host, nothing launched
+    # more scratch than the 32 MiB array holds: refused on the host, nothing launched
     desc, dummy = _big_desc(num_pages=1024)
     assert binding.attention_workspace_bytes(desc) > binding.STATIC_WORKSPACE_BYTES
     rc = binding.paged_attention_step_static_ws(desc, dummy, dummy, dummy, dummy, 1.0,
