@@ -1328,7 +1328,9 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
 // the pieces are u1's first piece (slot 2 u1) when the unit starts exactly at b, else its
 // last (slot 2 u1 + 1), then the first piece of each later unit (slot 2 u).  NG thread
 // groups of a CTA share a pair's pieces, so even a segment that spans hundreds of units
-// (one dominant long row) is folded in a few rounds of loads.
+// (one dominant long row, or one cut into many chunks) is folded in a few rounds of loads.
+// Used for 16-bit pages, whose chunked tail gives many pairs dozens of pieces (measured
+// faster than the per-group form below for them).
 template <typename T, int D, int G, int NG>
 __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_kernel(StepArgs a) {
     constexpr int TPG = G * D / 4;
@@ -1360,6 +1362,108 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_kernel(StepArgs
         const SlotPieces slots{2 * u1 + (unit_start(u1) == b ? 0 : 1), 2 * (u1 + 1), 2};
         combine_fold<T, D, G, NG>(a, slots, static_cast<int>(u2 - u1 + 1), true, rr.x, g,
                                   s_ml, s_acc);
+    }
+}
+
+// The same combine for steps whose pairs mostly have few pieces (INT8 pages, whose units are
+// static but for a remainder): the CTA's NG thread groups take NG pairs at a time (pairs
+// blockIdx.x + k gridDim.x, so pairs of neighbouring requests land in different CTAs); a
+// group folds a pair of at most kSmallPieces pieces on its own, in one round of loads, and
+// the pairs with more (a long segment) are then folded by all groups together.
+constexpr int kSmallPieces = 8;
+struct PairPieces {
+    int count;        // pieces (<= 1: the decode kernel wrote the row)
+    int token, g;
+    SlotPieces slots;
+};
+template <typename T, int D, int G, int NG>
+__global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_solo_kernel(StepArgs a) {
+    using Cv = F16<T>;
+    constexpr int TPG = G * D / 4;
+    __shared__ float2 s_ml[NG > 1 ? NG : 1][TPG];
+    __shared__ float4 s_acc[NG > 1 ? NG : 1][TPG];
+    __shared__ int s_big[NG], s_nbig;
+    const int Hkv = a.num_kv_heads;
+    int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
+    const int4* rec = ws_at<const int4>(a, a.lay.req_info);  // {token, seg0, keys, pages}
+    const float2* part_ml = ws_at<const float2>(a, a.lay.part_ml);
+    const float* part_o = ws_at<const float>(a, a.lay.part_o);
+    pdl_wait();  // the decode grid has completed
+    // park the chunk counter at epoch 0, which no call uses, so the next call starts afresh;
+    // before the next kernel may launch, since a decode kernel can claim before its wait
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        atomicExch(reinterpret_cast<unsigned long long*>(ctrl + 10), 0ull);
+    __syncthreads();
+    pdl_trigger();
+    const int nreq = ctrl[2], nw = ctrl[4];
+    const int64_t S = ctrl[5], C = ctrl[6], D0 = static_cast<int64_t>(nw) * S;
+    auto unit = [&](int64_t p) -> int64_t { return p < D0 ? p / S : nw + (p - D0) / C; };
+    auto unit_start = [&](int64_t u) -> int64_t { return u < nw ? u * S : D0 + (u - nw) * C; };
+    auto pieces_of = [&](int rh) {
+        PairPieces pp{0, 0, 0, {0, 0, 0}};
+        const int r = rh / Hkv, g = rh % Hkv;
+        const int4 rr = rec[r];
+        const int per = rr.w;
+        if (per == 0) return pp;
+        const int64_t b = static_cast<int64_t>(rr.y) + static_cast<int64_t>(g) * per;
+        const int64_t u1 = unit(b), u2 = unit(b + per - 1);
+        pp.count = static_cast<int>(u2 - u1 + 1);
+        pp.token = rr.x;
+        pp.g = g;
+        pp.slots = SlotPieces{2 * u1 + (unit_start(u1) == b ? 0 : 1), 2 * (u1 + 1), 2};
+        return pp;
+    };
+    const int grp = threadIdx.x / TPG, tin = threadIdx.x % TPG;
+    const int j = tin / (D / 4), dim = (tin % (D / 4)) * 4;
+    const int npairs = nreq * Hkv;
+    for (int round = 0; static_cast<int64_t>(round) * gridDim.x * NG < npairs; ++round) {
+        if (threadIdx.x == 0) s_nbig = 0;
+        __syncthreads();
+        const int rh = blockIdx.x + (round * NG + grp) * gridDim.x;
+        if (rh < npairs) {
+            const PairPieces pp = pieces_of(rh);
+            if (pp.count > kSmallPieces) {
+                if (tin == 0) s_big[atomicAdd(&s_nbig, 1)] = rh;
+            } else if (pp.count > 1) {
+                // this group alone: every piece's loads in flight together
+                float2 ml[kSmallPieces];
+                float4 o[kSmallPieces];
+#pragma unroll
+                for (int u = 0; u < kSmallPieces; ++u) {
+                    if (u < pp.count) {
+                        const int64_t slot = pp.slots(u);
+                        ml[u] = part_ml[slot * G + j];
+                        o[u] = *reinterpret_cast<const float4*>(part_o + (slot * G + j) * D + dim);
+                    }
+                }
+                float M = -1e30f, L = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < kSmallPieces; ++u) {
+                    if (u < pp.count) {
+                        const float mn = fmaxf(M, ml[u].x);
+                        const float c = fast_exp2(M - mn), w = fast_exp2(ml[u].x - mn);
+                        M = mn;
+                        L = fmaf(L, c, ml[u].y * w);
+                        acc.x = fmaf(acc.x, c, o[u].x * w);
+                        acc.y = fmaf(acc.y, c, o[u].y * w);
+                        acc.z = fmaf(acc.z, c, o[u].z * w);
+                        acc.w = fmaf(acc.w, c, o[u].w * w);
+                    }
+                }
+                const float inv = 1.f / L;
+                uint16_t* out = static_cast<uint16_t*>(a.out) +
+                                (static_cast<int64_t>(pp.token) * a.num_q_heads + pp.g * G + j) *
+                                    D + dim;
+                *reinterpret_cast<uint2*>(out) = make_uint2(Cv::pack(acc.x * inv, acc.y * inv),
+                                                            Cv::pack(acc.z * inv, acc.w * inv));
+            }
+        }
+        __syncthreads();
+        for (int k = 0; k < s_nbig; ++k) {  // uniform over the CTA
+            const PairPieces pp = pieces_of(s_big[k]);
+            combine_fold<T, D, G, NG>(a, pp.slots, pp.count, true, pp.token, pp.g, s_ml, s_acc);
+        }
     }
 }
 
@@ -1456,7 +1560,13 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
     const int cap_big = std::min(rows_heads, 2 * a.num_sms);     // up to 1,024 threads
     const int chunks = cdiv(max_splits, kCombineChunk);
     cudaError_t e;
-    if (a.self_plan) {
+    if (a.self_plan && Q8) {
+        // one CTA per SM at most, each taking kNg pairs at a time
+        const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
+        e = launch_pdl(combine_pieces_solo_kernel<T, D, G, kNg>,
+                       dim3(std::min(cdiv(pairs, kNg), a.num_sms)), dim3(kTpg * kNg), 0, stream,
+                       a);
+    } else if (a.self_plan) {
         const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
         e = launch_pdl(combine_pieces_kernel<T, D, G, kNg>, dim3(std::min(pairs, 2 * a.num_sms)),
                        dim3(kTpg * kNg), 0, stream, a);
