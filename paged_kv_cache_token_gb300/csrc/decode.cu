@@ -1202,7 +1202,8 @@ __device__ __forceinline__ void combine_fold(const StepArgs& a, SlotFn slot_of, 
                                              float4 (*s_acc)[G * D / 4]) {
     using Cv = F16<T>;
     constexpr int TPG = G * D / 4;              // threads per group
-    constexpr int kBatch = NG > 1 ? 4 : 8;      // splits in flight per thread
+    // splits in flight per thread: 4 when a CTA of 1,024 threads leaves 64 registers each
+    constexpr int kBatch = (NG > 1 && TPG * NG >= 1024) ? 4 : 8;
     float2* part_ml = ws_at<float2>(a, a.lay.part_ml);
     float* part_o = ws_at<float>(a, a.lay.part_o);
     const int grp = threadIdx.x / TPG, tin = threadIdx.x % TPG;
@@ -1567,9 +1568,11 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
                        dim3(std::min(cdiv(pairs, kNg), a.num_sms)), dim3(kTpg * kNg), 0, stream,
                        a);
     } else if (a.self_plan) {
+        // four thread groups per CTA: two CTAs fit an SM, so the grid runs in one wave
+        constexpr int kNg4 = std::min(4, 1024 / kTpg);
         const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
-        e = launch_pdl(combine_pieces_kernel<T, D, G, kNg>, dim3(std::min(pairs, 2 * a.num_sms)),
-                       dim3(kTpg * kNg), 0, stream, a);
+        e = launch_pdl(combine_pieces_kernel<T, D, G, kNg4>, dim3(std::min(pairs, 2 * a.num_sms)),
+                       dim3(kTpg * kNg4), 0, stream, a);
     } else if (max_splits <= kManySplits) {
         e = launch_pdl(combine_kernel<T, D, G, 1, kCombineRow>, dim3(cap_small), dim3(kTpg), 0,
                        stream, a);
