@@ -1561,15 +1561,16 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
     const int cap_big = std::min(rows_heads, 2 * a.num_sms);     // up to 1,024 threads
     const int chunks = cdiv(max_splits, kCombineChunk);
     cudaError_t e;
+    // self-planned steps: at most four thread groups and 512 threads per CTA, so two CTAs
+    // fit an SM
+    constexpr int kNg4 = std::max(1, std::min(4, 512 / kTpg));
     if (a.self_plan && Q8) {
-        // one CTA per SM at most, each taking kNg pairs at a time
+        // one CTA per SM at most, each taking kNg4 pairs at a time
         const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
-        e = launch_pdl(combine_pieces_solo_kernel<T, D, G, kNg>,
-                       dim3(std::min(cdiv(pairs, kNg), a.num_sms)), dim3(kTpg * kNg), 0, stream,
-                       a);
+        e = launch_pdl(combine_pieces_solo_kernel<T, D, G, kNg4>,
+                       dim3(std::min(cdiv(pairs, kNg4), a.num_sms)), dim3(kTpg * kNg4), 0,
+                       stream, a);
     } else if (a.self_plan) {
-        // four thread groups per CTA: two CTAs fit an SM, so the grid runs in one wave
-        constexpr int kNg4 = std::min(4, 1024 / kTpg);
         const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
         e = launch_pdl(combine_pieces_kernel<T, D, G, kNg4>, dim3(std::min(pairs, 2 * a.num_sms)),
                        dim3(kTpg * kNg4), 0, stream, a);
