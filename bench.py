@@ -212,11 +212,12 @@ def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
     parity = [0]
 
     def one_step():
+        # kv_append + paged_attention_step as one call (pkv_append_attention: one fused
+        # decode grid plus the combine for this decode step)
         p = pools[parity[0]]
         parity[0] ^= 1
-        binding.kv_append(ds.desc, k_new, v_new, p.k_cache, p.v_cache, None, kv.err, stream)
-        binding.paged_attention_step(ds.desc, q, p.k_cache, p.v_cache, out, w.scale, ws,
-                                     kv.err, stream)
+        binding.append_attention(ds.desc, k_new, v_new, p.k_cache, p.v_cache, q, out, w.scale,
+                                 ws, None, kv.err, stream)
 
     for _ in range(max(3, warmup)):
         one_step()
@@ -296,7 +297,7 @@ def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
     assert kv.read_error() == 0
     del kv2, pipe
     return dict(w=w, plan=plan, acct=acct, ms_step=ms_step, ms_kernel=ms_kernel, ms_e2e=ms_e2e,
-                h2d=h2d, d2h=d2h, clocks=clocks.summary(), launches=4 * steps,
+                h2d=h2d, d2h=d2h, clocks=clocks.summary(), launches=2 * steps,
                 host_pack_ms=host_pack_ms, ms_e2e_pack=ms_e2e_pack)
 
 
@@ -695,7 +696,8 @@ def main():
             "data": "synthetic",
             "config": {"workload": "decode-only step: 64 requests, cached ctx U[512,4096], 32 q /"
                                    " 8 kv heads, d_head 128, bf16, 16-token pages over a "
-                                   "%d-page permuted pool (kv_append + paged_attention_step)"
+                                   "%d-page permuted pool (kv_append + paged_attention_step "
+                                   "through pkv_append_attention)"
                                    % args.pool_pages,
                        "kv_bytes_per_step": acct["kv"], "step_bytes": acct["step"],
                        "l2": "steps alternate between two disjoint page pools: each step's "

@@ -162,6 +162,21 @@ PKV_API int pkv_paged_attention_step(const pkv_step_desc* desc, const void* q, c
                              size_t workspace_bytes, int32_t* dev_err_flag, void* stream);
 
 /*
+ * pkv_append_attention -- pkv_kv_append followed by pkv_paged_attention_step, in one call
+ * (16-bit pools): arguments, results, slot ids and errors are those of the two calls.  When
+ * every request advances by at most one token (a decode step) and there are at most 256
+ * requests, a single decode grid does both: the warp that streams a (request, KV head)'s
+ * last page first writes the request's new K and V rows into it (hotelren.com/news/6181127
+ * §3.1: append, then attend over all S+t keys), so no separate append launch or dependency
+ * hop sits in the step.  Other steps run the append kernel, then the attention step.  On
+ * inconsistent lengths (PKV_DEVERR_TOKENS) such a decode step appends nothing.
+ */
+PKV_API int pkv_append_attention(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, int64_t* slot_mapping_out,
+                                 const void* q, void* out, float scale, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err_flag, void* stream);
+
+/*
  * pkv_plan_attention, pkv_paged_attention_run -- the attention step in two halves, so that
  * one plan serves every layer of a model step.  The step's work list (decode rows, split-KV
  * items, prefill tiles) depends only on the lengths and the block table, which every layer

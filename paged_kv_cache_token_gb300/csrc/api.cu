@@ -224,11 +224,18 @@ namespace {
 // plan alone, or the attention kernels over a plan already in the workspace.
 enum class Phase { kPlanAndRun, kPlanOnly, kRunOnly };
 
+// New K/V rows for an attention call that appends them itself (pkv_append_attention).
+struct FusedAppend {
+    const void* k_new;
+    const void* v_new;
+    int64_t* slot_mapping;
+};
+
 int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache,
                    const void* v_cache, void* out, float scale, void* workspace,
                    size_t workspace_bytes, int32_t* dev_err_flag, void* stream,
                    const float* k_scale, const float* v_scale,
-                   Phase phase = Phase::kPlanAndRun) {
+                   Phase phase = Phase::kPlanAndRun, const FusedAppend* fused = nullptr) {
     int rc = check_desc(desc);
     if (rc != PKV_OK) return rc;
     if (desc->total_q_tokens == 0) return PKV_OK;
@@ -283,6 +290,12 @@ int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache
     a.plan_ready = phase == Phase::kRunOnly ? 1 : 0;
     a.self_plan = lay.self_plan;
     a.epoch = a.self_plan ? next_epoch() : 0;
+    if (fused) {
+        a.fused_append = 1;
+        a.k_new = fused->k_new;
+        a.v_new = fused->v_new;
+        a.slot_mapping = fused->slot_mapping;
+    }
     // a self-planned step has nothing to plan ahead: its decode kernel plans for itself
     if (phase != Phase::kRunOnly && !a.self_plan && (rc = pkv::launch_plan(a, s)) != PKV_OK)
         return rc;
@@ -316,6 +329,33 @@ int pkv_paged_attention_step_int8(const pkv_step_desc* desc, const void* q,
     if (!k_scale) return PKV_ERR_INVALID_ARG;
     return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
                           dev_err_flag, stream, k_scale, v_scale);
+}
+
+int pkv_append_attention(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                         void* k_cache, void* v_cache, int64_t* slot_mapping_out, const void* q,
+                         void* out, float scale, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_err_flag, void* stream) {
+    int rc = check_desc(desc);
+    if (rc != PKV_OK) return rc;
+    if (desc->total_q_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    if (slot_mapping_out && (reinterpret_cast<uintptr_t>(slot_mapping_out) & 7u))
+        return PKV_ERR_INVALID_ARG;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    if (layout_for(desc, sms).self_plan) {
+        // one decode grid appends and attends (after the argument checks of both calls)
+        if (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache))
+            return PKV_ERR_INVALID_ARG;
+        const FusedAppend f{k_new, v_new, slot_mapping_out};
+        return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                              dev_err_flag, stream, nullptr, nullptr, Phase::kPlanAndRun, &f);
+    }
+    if ((rc = kv_append_impl(desc, k_new, v_new, k_cache, v_cache, slot_mapping_out,
+                             dev_err_flag, stream, nullptr, nullptr)) != PKV_OK)
+        return rc;
+    return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                          dev_err_flag, stream, nullptr, nullptr);
 }
 
 int pkv_plan_attention(const pkv_step_desc* desc, void* workspace, size_t workspace_bytes,

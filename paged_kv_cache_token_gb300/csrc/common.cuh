@@ -99,6 +99,12 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
     return __shfl_sync(kFull, ok, 0) != 0;
 }
 
+// Generic-proxy shared-memory writes of this thread -> ordered before later async-proxy
+// (bulk copy) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- bulk async copy (TMA, 1-D)
 // Global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte aligned) that
 // signals completion on `bar` through the transaction count.

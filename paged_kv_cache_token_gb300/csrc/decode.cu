@@ -585,7 +585,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             rb = make_int4(0, 1, 0, 0);
         }
     };
-    // lane l: physical id of page pb + w + l
+    // lane l: physical id of page pb + w + l (-1 when it is not a valid page: flagged, and
+    // page 0 is copied in its place)
     auto load_window = [&](const DecItem& it, int w) {
         int phys = 0;
         const int i = w + lane;
@@ -595,10 +596,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 phys = __ldg(a.block_table + static_cast<int64_t>(it.r) * a.max_pages + lp);
                 if (phys < 0 || phys >= a.num_pages) {
                     set_error(a.err, PKV_DEVERR_PAGE_RANGE);
-                    phys = 0;
+                    phys = -1;
                 }
             } else {
                 set_error(a.err, PKV_DEVERR_TABLE_RANGE);
+                phys = -1;
             }
         }
         return phys;
@@ -650,6 +652,32 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         it.s = 0;
         return it;
     };
+    // fused append (self-planned 16-bit steps): the warp whose piece holds a segment's last
+    // page loads the request's new K and V rows of that KV head when it makes the piece (16
+    // bytes per lane, keys on the low lanes, values above) and, once that page has landed in
+    // shared memory, writes the row into the page's slot there and into the pool.  No proxy
+    // fence sits before the copies: the copy reads the pool slot before the row is written,
+    // and the row reaches the computation through shared memory.
+    constexpr int kAppLanes = D * 2 / 16;  // 16-byte chunks of one K (or V) row
+    auto load_append = [&](const DecItem& it) {
+        uint4 r = make_uint4(0, 0, 0, 0);
+        if constexpr (!Q8) {
+            if (lane < 2 * kAppLanes) {
+                const bool is_v = lane >= kAppLanes;
+                const int chunk = is_v ? lane - kAppLanes : lane;
+                const uint16_t* sp = static_cast<const uint16_t*>(is_v ? a.v_new : a.k_new) +
+                                     (static_cast<int64_t>(it.t) * Hkv + it.g) * D;
+                r = __ldg(reinterpret_cast<const uint4*>(sp) + chunk);
+            }
+        }
+        return r;
+    };
+    uint4 app_cur = make_uint4(0, 0, 0, 0), app_nxt = app_cur;
+    // whether a piece holds its segment's last page
+    auto holds_last = [&](const DecItem& it) {
+        return it.np > 0 && it.pb + it.np == cdiv(it.nkv, kPage);
+    };
+    bool waited = false;           // the dependency wait has returned
     int sp_pos = range_start;  // self-planned: where the warp's next piece starts
     unsigned long long* chunk_ctr = reinterpret_cast<unsigned long long*>(ctrl + 10);
     // a chunk claim is issued when a unit's last piece is made and read one piece later, so
@@ -681,6 +709,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         const DecItem it = make_piece(sp_pos);
         sp_pos += it.np;
         if (it.np > 0 && sp_pos >= range_end && !claim_pending) issue_claim();
+        if (a.fused_append && waited && holds_last(it)) app_nxt = load_append(it);
         return it;
     };
 
@@ -706,6 +735,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     // be writing anything else -- the pages of this step's kv_append, or, when it is the
     // previous layer's combine, the queue counter it rewinds -- so the queue and q wait.
     if (!a.overlap && (a.plan_ready || a.self_plan)) pdl_wait();
+    waited = true;
+    if (a.fused_append) {  // rows of the two pieces made before the wait
+        if (holds_last(cur)) app_cur = load_append(cur);
+        if (holds_last(nxt)) app_nxt = load_append(nxt);
+    }
     pdl_trigger();  // the combine may be scheduled; it waits for this grid to finish
     if (a.self_plan && blockIdx.x == 0) {
         // what the combine needs: per request {token, first segment page, keys, pages per
@@ -759,7 +793,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         } else {
             return;
         }
-        const int phys = __shfl_sync(kFull, win, lidx);
+        const int phys = max(0, __shfl_sync(kFull, win, lidx));
         if (lane == 0) {
             const int stage = issued % kNst;
             uint8_t* dst = ring + stage * S::kStageBytes;
@@ -983,6 +1017,27 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             const uint8_t* sK = ring + stage * S::kStageBytes;
             const uint8_t* sV = sK + S::kPageBytes;
             const int nvalid = min(kPage, cur.nkv - (cur.pb + i) * kPage);
+            const bool patch = a.fused_append && i == cur.np - 1 && holds_last(cur);
+            if (patch) {
+                // this step's row of the segment's last page: into the staged page (its pool
+                // slot was copied before the row was written) and into the pool
+                const int phys = __shfl_sync(kFull, cur_win, i - cur_win_base);
+                const int slot = (cur.nkv - 1) % kPage;
+                if (phys >= 0 && lane < 2 * kAppLanes) {
+                    const bool is_v = lane >= kAppLanes;
+                    const int chunk = is_v ? lane - kAppLanes : lane;
+                    reinterpret_cast<uint4*>(const_cast<uint8_t*>(is_v ? sV : sK) +
+                                             slot * D * 2)[chunk] = app_cur;
+                    const int64_t dst =
+                        ((static_cast<int64_t>(phys) * Hkv + cur.g) * kPage + slot) * D;
+                    uint16_t* dp = static_cast<uint16_t*>(const_cast<void*>(
+                                       is_v ? a.v_cache : a.k_cache)) + dst;
+                    reinterpret_cast<uint4*>(dp)[chunk] = app_cur;
+                }
+                if (phys >= 0 && lane == 0 && cur.g == 0 && a.slot_mapping)
+                    a.slot_mapping[cur.t] = static_cast<int64_t>(phys) * kPage + slot;
+                __syncwarp();
+            }
             // ---- scores: rows kr0, kr1, chunk m of 8 dims = k-steps 2m, 2m + 1
             float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1066,6 +1121,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
             } else {
                 for (int tok = 0; tok < nvalid; ++tok) pv_token(tok);
             }
+            if (patch) fence_proxy_async_smem();  // the patched stage is refilled by a copy
             __syncwarp();
             issue_one();  // refill the stage just freed
         }
@@ -1117,6 +1173,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
 
         // ---- advance the metadata pipeline; `nxt`'s first pages are already in flight
         cur = nxt;
+        app_cur = app_nxt;
         cur_win = nxt_win;
         cur_win_base = 0;
         if constexpr (kPrefetchQ) {

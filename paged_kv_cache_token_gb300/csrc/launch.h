@@ -87,6 +87,13 @@ struct StepArgs {
     // value for every call (a CUDA graph replays the captured values; the combine parks the
     // counter at 0 after every call, so a replayed tag still starts afresh)
     unsigned long long epoch;
+    // self-planned steps over 16-bit pools may also append the step's new K/V rows
+    // (pkv_append_attention): the warp that reads a (request, KV head)'s last page writes the
+    // request's new row into it first
+    int fused_append;
+    const void* k_new;  // [T][Hkv][D], with fused_append
+    const void* v_new;
+    int64_t* slot_mapping;  // [T] or null, with fused_append
     const float* k_scale;  // [Hkv][D], INT8 pools only
     const float* v_scale;
 };

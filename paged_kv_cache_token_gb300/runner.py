@@ -124,6 +124,17 @@ class PagedKV:
             binding.paged_attention_step(desc, q, self.k_cache, self.v_cache, out, scale, ws,
                                          self.err, stream)
 
+    def append_attention_desc(self, desc, k_new, v_new, q, out, scale: float, ws,
+                              slot_mapping=None, stream=None) -> None:
+        """kv_append then the attention step (16-bit pools in one call, fused into one decode
+        grid for decode steps; INT8 pools as the two calls)."""
+        if self.kv_int8:
+            self.append_desc(desc, k_new, v_new, slot_mapping, stream)
+            self.attention_desc(desc, q, out, scale, ws, stream)
+        else:
+            binding.append_attention(desc, k_new, v_new, self.k_cache, self.v_cache, q, out,
+                                     scale, ws, slot_mapping, self.err, stream)
+
     def run_desc(self, desc, q, out, scale: float, ws, stream=None) -> None:
         """The attention kernels over the plan already in ``ws`` (see
         binding.plan_attention): one more layer of a planned step."""
@@ -264,9 +275,9 @@ class StepStaging:
         self._dev[:self.total].copy_(self._host[:self.total], non_blocking=True)
 
     def run(self, scale: float, stream=None) -> None:
-        """kv_append then the attention step, on the staged device views."""
-        self.kv.append_desc(self.desc, self.k_new, self.v_new, None, stream)
-        self.kv.attention_desc(self.desc, self.q, self.out, scale, self._ws, stream)
+        """kv_append then the attention step (one call), on the staged device views."""
+        self.kv.append_attention_desc(self.desc, self.k_new, self.v_new, self.q, self.out,
+                                      scale, self._ws, None, stream)
 
     def download(self) -> None:
         """Device -> host copy of the step's output on the current stream."""
@@ -345,8 +356,9 @@ class StepPipeline:
 class DecodeLoop:
     """Consecutive steps of one batch run as one device-side sequence.
 
-    Every step is kv_append, the attention step and pkv_advance_context (context_lens +=
-    q_lens), so no metadata crosses from the host between steps; the block table is the
+    Every step is kv_append with the attention step (pkv_append_attention: one fused grid
+    for decode steps) and pkv_advance_context (context_lens += q_lens), so no metadata
+    crosses from the host between steps; the block table is the
     last step's, which already holds every page the earlier steps reach.  Each step's Q,
     K_new, V_new are staged on the device up front and each step's output has its own slot.
     ``capture`` records the whole sequence in one CUDA graph (the lengths are reset at its
@@ -406,11 +418,12 @@ class DecodeLoop:
             if self.shared_plan:
                 binding.plan_attention(self.desc, self.ws, self.kv.err, stream)
             for (lkv, _), (q, k_new, v_new, out) in zip(self.layers, self.io):
-                lkv.append_desc(self.desc, k_new[s], v_new[s], None, stream)
                 if self.shared_plan:
+                    lkv.append_desc(self.desc, k_new[s], v_new[s], None, stream)
                     lkv.run_desc(self.desc, q[s], out[s], self.scale, self.ws, stream)
                 else:
-                    lkv.attention_desc(self.desc, q[s], out[s], self.scale, self.ws, stream)
+                    lkv.append_attention_desc(self.desc, k_new[s], v_new[s], q[s], out[s],
+                                              self.scale, self.ws, None, stream)
             binding.advance_context(self.desc, self.ctx, stream)
 
     def run(self) -> torch.Tensor:
@@ -467,6 +480,18 @@ def load_history(kv: PagedKV, workload, plan: Optional[StepPlan]) -> None:
     _, k, v = step_host_inputs(workload, plan)
     ds = kv.upload(plan)
     kv.append(ds, bits_to_tensor(k, workload.dtype), bits_to_tensor(v, workload.dtype))
+
+
+def run_step_fused(kv: PagedKV, workload, plan: StepPlan, slot_mapping=None) -> torch.Tensor:
+    """As :func:`run_step`, through the one-call pkv_append_attention."""
+    q, k, v = step_host_inputs(workload, plan)
+    ds = kv.upload(plan)
+    kv.copy_pages(ds)
+    out = torch.empty((plan.total_q_tokens, kv.hq, kv.d), dtype=kv.dtype, device=kv.device)
+    kv.append_attention_desc(ds.desc, bits_to_tensor(k, workload.dtype),
+                             bits_to_tensor(v, workload.dtype), bits_to_tensor(q, workload.dtype),
+                             out, workload.scale, kv.workspace(ds.desc), slot_mapping)
+    return out
 
 
 def run_step(kv: PagedKV, workload, plan: StepPlan) -> torch.Tensor:

@@ -71,8 +71,10 @@ def test_host_validation_rejects_before_launch(lib, kw, code):
                                       None)
     assert rc == code
     assert lib.pkv_attention_workspace_bytes(ctypes.byref(d)) == 0
-    # the plan and run halves and the built-in-scratch entry point report description
-    # errors the same way
+    # the plan and run halves, the one-call append + attention and the built-in-scratch
+    # entry point report description errors the same way
+    assert lib.pkv_append_attention(ctypes.byref(d), None, None, None, None, None, None, None,
+                                    1.0, None, 0, None, None) == code
     assert lib.pkv_plan_attention(ctypes.byref(d), None, 0, None, None) == code
     assert lib.pkv_paged_attention_run(ctypes.byref(d), None, None, None, None, 1.0, None, 0,
                                        None, None) == code
@@ -159,3 +161,19 @@ def test_plan_and_run_argument_checks(lib):
     assert lib.pkv_plan_attention(ctypes.byref(e), None, 0, None, None) == 0
     assert lib.pkv_paged_attention_run(ctypes.byref(e), None, None, None, None, 1.0, None, 0,
                                        None, None) == 0
+
+
+def test_append_attention_argument_checks(lib):
+    d = _desc()
+    t, odd = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1008)
+    # new rows missing or misaligned, a misaligned slot-id array (before any device query)
+    assert lib.pkv_append_attention(ctypes.byref(d), None, t, t, t, None, t, t, 1.0, t, 1 << 30,
+                                    None, None) == -1
+    assert lib.pkv_append_attention(ctypes.byref(d), odd, t, t, t, None, t, t, 1.0, t, 1 << 30,
+                                    None, None) == -1
+    assert lib.pkv_append_attention(ctypes.byref(d), t, t, t, t, ctypes.c_void_p(0x1004), t, t,
+                                    1.0, t, 1 << 30, None, None) == -1
+    e = _desc(num_reqs=0, total_q_tokens=0, max_q_len=0, max_context_len=0, q_lens=None,
+              q_offsets=None, context_lens=None, block_table=None)
+    assert lib.pkv_append_attention(ctypes.byref(e), None, None, None, None, None, None, None,
+                                    1.0, None, 0, None, None) == 0

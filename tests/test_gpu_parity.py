@@ -150,6 +150,74 @@ def test_decode_batches(hq, hkv, d, dtype):
     run_all(w)
 
 
+def _steps_both_ways(w):
+    """Every step of w through pkv_append_attention and through the two separate calls, on
+    fresh pools: (outputs, slot ids, pool bits) of each, and the plans."""
+    res = {}
+    for fused in (True, False):
+        s = scheduler_for(w)
+        kv = runner.paged_kv_for(w)
+        runner.load_history(kv, w, s.history_plan())
+        outs, slots, plans = [], [], []
+        for plan in s.all_steps():
+            sl = torch.full((plan.total_q_tokens,), -7, dtype=torch.int64, device="cuda")
+            if fused:
+                out = runner.run_step_fused(kv, w, plan, sl)
+            else:
+                q, k, v = runner.step_host_inputs(w, plan)
+                ds = kv.upload(plan)
+                kv.append(ds, runner.bits_to_tensor(k, w.dtype), runner.bits_to_tensor(v, w.dtype),
+                          sl)
+                out = kv.attention(ds, runner.bits_to_tensor(q, w.dtype), w.scale)
+            outs.append(out)
+            slots.append(sl)
+            plans.append(plan)
+        assert kv.read_error() == 0
+        res[fused] = (outs, slots, pool_bits(kv))
+    return res, plans
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(32, 8, 128, 0), (8, 8, 128, 1), (16, 2, 64, 1),
+                                            (64, 8, 128, 0), (8, 1, 64, 0)])
+def test_fused_append_attention_decode_steps(hq, hkv, d, dtype):
+    # decode steps through pkv_append_attention: the warp streaming a (request, KV head)'s
+    # last page writes the new row first.  Outputs, slot ids and every pool byte equal the
+    # separate kv_append + attention calls, and every row matches the oracle.
+    ctx = [0, 1, 15, 16, 17, 100, 255, 256, 1000, 3000]
+    w = custom(1800 + hq + d, hq, hkv, d, dtype, [(c, 0, 3) for c in ctx])
+    res, plans = _steps_both_ways(w)
+    (fo, fs, fp), (so, ss, sp) = res[True], res[False]
+    for i, plan in enumerate(plans):
+        assert torch.equal(fo[i].view(torch.int16), so[i].view(torch.int16)), i
+        assert torch.equal(fs[i], ss[i]), i
+        assert_close(gpu_as_f64(fo[i]), oracle_rows(w, plan), "fused step %d" % i)
+    assert all(np.array_equal(a, b) for a, b in zip(fp, sp))
+
+
+def test_fused_append_attention_other_steps_fall_back():
+    # steps with prefill chunks (and more than 256 requests) take the append kernel, then
+    # the attention step: same bits as the separate calls
+    specs = [(300, 40, 1), (0, 200, 0), (17, 0, 2)] + [(5, 0, 1)] * 260
+    w = custom(1900, 8, 2, 128, 0, specs, budget=512)
+    res, plans = _steps_both_ways(w)
+    assert any(p.max_q_len > 1 for p in plans) and plans[0].num_reqs > 256
+    for i, plan in enumerate(plans):
+        assert torch.equal(res[True][0][i].view(torch.int16), res[False][0][i].view(torch.int16))
+        assert torch.equal(res[True][1][i], res[False][1][i])
+    assert all(np.array_equal(a, b) for a, b in zip(res[True][2], res[False][2]))
+
+
+def test_fused_append_attention_bad_page_flagged():
+    w = custom(1950, 4, 2, 64, 0, [(20, 0, 1), (40, 0, 1)])
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    plan.block_table[1, 2] = w.num_pages + 5   # the page the second request appends into
+    runner.run_step_fused(kv, w, plan)
+    assert kv.read_error() & binding.DEVERR_PAGE_RANGE
+
+
 def test_decode_literal_skeleton_scale_one():
     # hotelren.com/news/6181127 §5.1 writes softmax(q @ K_all.T) with no scale: scale = 1.0
     w = custom(200, 4, 2, 64, 0, [(40, 0, 1), (3, 0, 1)])
