@@ -687,7 +687,8 @@ def main():
         r = time_decode(device, args.steps, args.warmup, dist_ctx, args.pool_pages)
         acct = r["acct"]
         value = acct["step"] * dist_ctx.world / (r["ms_step"] * 1e-3) / 1e9
-        kernel_bytes = acct["attention"]
+        # the decode kernel of this step also appends the new rows (pkv_append_attention)
+        kernel_bytes = acct["attention"] + acct["append"]
         achieved = kernel_bytes / (r["ms_kernel"] * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist_ctx.world,
