@@ -327,6 +327,59 @@ def test_ragged_step_with_idle_requests(kv_int8):
     assert_close(gpu_as_f64(out), ref, "ragged step")
 
 
+@pytest.mark.parametrize("kv_int8", [False, True])
+def test_decode_step_with_idle_requests(kv_int8):
+    # a decode step (every row q_len <= 1, so the self-planned decode grid) in which some
+    # requests do not advance: q_len 0 with cached keys, and q_len 0 with none.  They give
+    # zero-length segments to the in-kernel plan; every row matches the oracle, the fused
+    # and the separate calls give the same bits, and no page of an idle request changes.
+    specs = [(50, 0, 0), (33, 0, 1), (0, 0, 0), (16, 0, 1), (300, 0, 0), (127, 0, 1),
+             (31, 0, 0), (1000, 0, 1), (15, 0, 1)]
+    w = custom(660 + kv_int8, 8, 2, 128, 0, specs)
+    results = []
+    for fused in (True, False):
+        s = scheduler_for(w)
+        kv = runner.paged_kv_for(w, kv_int8=kv_int8)
+        runner.load_history(kv, w, s.history_plan())
+        step = s.next_step()
+        got = {int(r): j for j, r in enumerate(step.rids)}
+        rids, q_lens, ctx, tables = [], [], [], []
+        for r, spec in enumerate(specs):
+            rids.append(r)
+            if r in got:
+                j = got[r]
+                q_lens.append(int(step.q_lens[j]))
+                ctx.append(int(step.context_lens[j]))
+                tables.append([p for p in step.block_table[j].tolist() if p >= 0])
+            else:
+                q_lens.append(0)
+                ctx.append(spec[0])
+                tables.append(list(s.reqs[r].pages))
+        assert q_lens == [0, 1, 0, 1, 0, 1, 0, 1, 1]
+        plan = make_plan(rids, q_lens, ctx, tables)
+        idle_pages = [p for r in (0, 4, 6) for p in tables[r]]
+        before = [b[idle_pages].copy() for b in pool_bits(kv)]
+        sl = torch.full((plan.total_q_tokens,), -7, dtype=torch.int64, device="cuda")
+        if fused:
+            out = runner.run_step_fused(kv, w, plan, sl)
+        else:
+            q, k, v = runner.step_host_inputs(w, plan)
+            ds = kv.upload(plan)
+            kv.append(ds, runner.bits_to_tensor(k, w.dtype), runner.bits_to_tensor(v, w.dtype),
+                      sl)
+            out = kv.attention(ds, runner.bits_to_tensor(q, w.dtype), w.scale)
+        assert kv.read_error() == 0
+        assert all(np.array_equal(b[idle_pages], a) for b, a in zip(pool_bits(kv), before))
+        ref = oracle_rows_int8(w, plan) if kv_int8 else oracle_rows(w, plan)
+        assert out.shape[0] == 5
+        assert_close(gpu_as_f64(out), ref, "decode step with idle requests")
+        results.append((out, sl, pool_bits(kv)))
+    (fo, fs, fp), (so, ss, sp) = results
+    assert torch.equal(fo.view(torch.int16), so.view(torch.int16))
+    assert torch.equal(fs, ss)
+    assert all(np.array_equal(a, b) for a, b in zip(fp, sp))
+
+
 def test_long_contexts():
     # maximum-size rows: a decode row over 131,071 cached tokens (8,192 pages, about 900
     # splits per (row, KV head); with up to 45 decode rows possible in this step the combine
