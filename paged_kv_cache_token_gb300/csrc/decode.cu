@@ -423,6 +423,92 @@ __device__ __forceinline__ int claimed_chunk(unsigned long long* ctr, unsigned l
     return INT_MAX;
 }
 
+struct UnitMap {
+    int64_t S, C, D0;
+    int nw;
+    __device__ int64_t unit(int64_t p) const { return p < D0 ? p / S : nw + (p - D0) / C; }
+    __device__ int64_t start(int64_t u) const { return u < nw ? u * S : D0 + (u - nw) * C; }
+};
+__device__ __forceinline__ UnitMap unit_map(const int32_t* ctrl) {
+    UnitMap m;
+    m.nw = ctrl[4];
+    m.S = ctrl[5];
+    m.C = ctrl[6];
+    m.D0 = static_cast<int64_t>(m.nw) * m.S;
+    return m;
+}
+
+// Segments of more than kLongPieces pieces -- e.g. one long row spread over the whole grid --
+// are folded by the combine in chunks of kPieceChunk pieces on different CTAs.  A chunk's
+// state replaces its first piece (a thread reads and writes only its own elements of a
+// slot).  The CTA whose chunk arrives last at the segment's counter (zeroed by the decode
+// kernel) merges the chunk states in chunk order: nothing waits, and the result does not
+// depend on which CTA merges.  Up to kMaxLong such pairs are listed, in pair order, by the
+// decode kernel (the rest are folded whole by one CTA).
+constexpr int kPieceChunk = 32;
+constexpr int kLongPieces = 96;
+constexpr int kMaxLong = 512;
+// Lists the pairs with more than kLongPieces pieces: l_rh[k] the k-th in pair order,
+// l_off[k] its first chunk in the sequence of all listed pairs' chunks; hdr = {listed pairs,
+// their chunks}.  The whole CTA of NT threads calls it; lsum is 2 x NT / 32 ints of shared
+// memory.
+template <int NT, typename CountFn>
+__device__ __forceinline__ void list_long_pairs(CountFn count_of, int npairs, int32_t* l_rh,
+                                                int32_t* l_off, int32_t* hdr,
+                                                int (*lsum)[NT / 32]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = cdiv(npairs, NT);
+    const int p0 = min(npairs, tid * per), p1 = min(npairs, p0 + per);
+    int nb = 0, nc = 0;
+    for (int rh = p0; rh < p1; ++rh) {
+        const int cnt = count_of(rh);
+        if (cnt > kLongPieces) {
+            ++nb;
+            nc += cdiv(cnt, kPieceChunk);
+        }
+    }
+    int ib = nb, ic = nc;  // inclusive scans over the warp, then over the warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yb = __shfl_up_sync(kFull, ib, o), yc = __shfl_up_sync(kFull, ic, o);
+        if (lane >= o) {
+            ib += yb;
+            ic += yc;
+        }
+    }
+    if (lane == 31) {
+        lsum[0][warp] = ib;
+        lsum[1][warp] = ic;
+    }
+    __syncthreads();
+    int eb = ib - nb, ec = ic - nc, tb = 0, tc = 0;
+    for (int w = 0; w < NT / 32; ++w) {
+        if (w < warp) {
+            eb += lsum[0][w];
+            ec += lsum[1][w];
+        }
+        tb += lsum[0][w];
+        tc += lsum[1][w];
+    }
+    for (int rh = p0; rh < p1 && nb > 0 && eb <= kMaxLong; ++rh) {
+        const int cnt = count_of(rh);
+        if (cnt > kLongPieces) {
+            if (eb < kMaxLong) {
+                l_rh[eb] = rh;
+                l_off[eb] = ec;
+            } else {
+                hdr[1] = ec;  // where the listed pairs' chunks end
+            }
+            ++eb;
+            ec += cdiv(cnt, kPieceChunk);
+        }
+    }
+    if (tid == 0) {
+        hdr[0] = min(tb, kMaxLong);
+        if (tb <= kMaxLong) hdr[1] = tc;
+    }
+}
+
 // One work item as a warp sees it.
 struct DecItem {
     int idx;        // queue position; >= count when none
@@ -477,6 +563,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     __shared__ int s_keys[kSelfPlanMaxReqs];
     __shared__ int s_wsum[kDecWarps];
     __shared__ int s_bad;
+    __shared__ int s_lsum[2][kDecWarps];
     int sp_total = 0, sp_nw = 0, sp_static = 0, sp_chunk = 1, sp_chunks = 0, sp_unit = -1;
     int range_start = 0, range_end = 0;  // the unit this warp works through (T < 2^30)
     if (a.self_plan) {
@@ -743,11 +830,26 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
     pdl_trigger();  // the combine may be scheduled; it waits for this grid to finish
     if (a.self_plan && blockIdx.x == 0) {
         // what the combine needs: per request {token, first segment page, keys, pages per
-        // head}, the totals (every earlier kernel has completed: the workspace is free)
+        // head}, the totals, zeroed arrival counts (every earlier kernel has completed: the
+        // workspace is free)
         int4* rec = ws_at<int4>(a, a.lay.req_info);
         for (int r = threadIdx.x; r < a.num_reqs; r += kDecThreads)
             rec[r] = make_int4(s_tok[r], s_seg0[r], s_keys[r],
                                (s_seg0[r + 1] - s_seg0[r]) / Hkv);
+        int32_t* pair_ctr = ws_at<int32_t>(a, a.lay.pair_ctr);  // the combine's arrivals
+        for (int i = threadIdx.x; i < a.num_reqs * Hkv; i += kDecThreads) pair_ctr[i] = 0;
+        // the long pairs, for the combine
+        const UnitMap um{sp_static, sp_chunk, static_cast<int64_t>(sp_nw) * sp_static, sp_nw};
+        auto count_of = [&](int rh) {
+            const int r = rh / Hkv, g = rh % Hkv;
+            const int per = (s_seg0[r + 1] - s_seg0[r]) / Hkv;
+            if (per == 0) return 0;
+            const int64_t b = static_cast<int64_t>(s_seg0[r]) + static_cast<int64_t>(g) * per;
+            return static_cast<int>(um.unit(b + per - 1) - um.unit(b) + 1);
+        };
+        int32_t* l_rh = pair_ctr + a.num_reqs * Hkv;
+        list_long_pairs<kDecThreads>(count_of, (s_bad || sp_nw == 0) ? 0 : a.num_reqs * Hkv,
+                                     l_rh, l_rh + kMaxLong, ctrl + 12, s_lsum);
         if (threadIdx.x == 0) {
             if (s_bad) set_error(a.err, PKV_DEVERR_TOKENS);
             ctrl[1] = sp_total;
@@ -1252,7 +1354,8 @@ struct SlotPieces {
     }
 };
 
-template <typename T, int D, int G, int NG, typename SlotFn>
+// kL2: load through L2 only (states other CTAs of the same grid wrote)
+template <typename T, int D, int G, int NG, bool kL2 = false, typename SlotFn>
 __device__ __forceinline__ void combine_fold(const StepArgs& a, SlotFn slot_of, int count,
                                              bool to_out, int t, int g,
                                              float2 (*s_ml)[G * D / 4],
@@ -1276,8 +1379,14 @@ __device__ __forceinline__ void combine_fold(const StepArgs& a, SlotFn slot_of, 
             const int i = i0 + u * NG;
             if (i < count) {
                 const int64_t slot = slot_of(i);
-                ml[u] = part_ml[slot * G + j];
-                o[u] = *reinterpret_cast<const float4*>(part_o + (slot * G + j) * D + dim);
+                const float4* op = reinterpret_cast<const float4*>(part_o + (slot * G + j) * D + dim);
+                if constexpr (kL2) {
+                    ml[u] = __ldcg(part_ml + slot * G + j);
+                    o[u] = __ldcg(op);
+                } else {
+                    ml[u] = part_ml[slot * G + j];
+                    o[u] = *op;
+                }
             }
         }
 #pragma unroll
@@ -1384,16 +1493,116 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_kernel(StepArgs a) {
 // pages per warp) or nw S + (u - nw) C (chunks of C pages), so the segment meets units
 // u1 = unit(b) .. u2 = unit(e - 1).  One unit (u1 == u2) wrote the row itself.  Otherwise
 // the pieces are u1's first piece (slot 2 u1) when the unit starts exactly at b, else its
-// last (slot 2 u1 + 1), then the first piece of each later unit (slot 2 u).  NG thread
-// groups of a CTA share a pair's pieces, so even a segment that spans hundreds of units
-// (one dominant long row, or one cut into many chunks) is folded in a few rounds of loads.
-// Used for 16-bit pages, whose chunked tail gives many pairs dozens of pieces (measured
-// faster than the per-group form below for them).
+// last (slot 2 u1 + 1), then the first piece of each later unit (slot 2 u).
+struct PairPieces {
+    int count;        // pieces (<= 1: the decode kernel wrote the row)
+    int token, g;
+    SlotPieces slots;
+};
+__device__ __forceinline__ PairPieces pair_pieces(const int4* rec, const UnitMap& m, int Hkv,
+                                                  int rh) {
+    PairPieces pp{0, 0, 0, {0, 0, 0}};
+    const int r = rh / Hkv, g = rh % Hkv;
+    const int4 rr = rec[r];
+    const int per = rr.w;
+    if (per == 0) return pp;
+    const int64_t b = static_cast<int64_t>(rr.y) + static_cast<int64_t>(g) * per;
+    const int64_t u1 = m.unit(b), u2 = m.unit(b + per - 1);
+    pp.count = static_cast<int>(u2 - u1 + 1);
+    pp.token = rr.x;
+    pp.g = g;
+    pp.slots = SlotPieces{2 * u1 + (m.start(u1) == b ? 0 : 1), 2 * (u1 + 1), 2};
+    return pp;
+}
+
+struct SlotShift {   // pieces first, first + 1, ...
+    SlotPieces p;
+    int first;
+    __device__ int64_t operator()(int i) const { return p(first + i); }
+};
+struct SlotChunks {  // the first piece of every chunk
+    SlotPieces p;
+    __device__ int64_t operator()(int i) const { return p(i * kPieceChunk); }
+};
+struct LongPairs {          // the decode kernel's list, in shared memory
+    int rh[kMaxLong];       // listed long pairs, ascending
+    int off[kMaxLong];      // their first chunk in the grid's chunk sequence
+    int n, chunks, last;
+};
+// Copies the list (n > 0 entries) to shared memory; the whole CTA calls it.
+__device__ __forceinline__ void load_long_pairs(const StepArgs& a, const int32_t* ctrl,
+                                                LongPairs& L) {
+    const int32_t* l_rh = ws_at<const int32_t>(a, a.lay.pair_ctr) + a.num_reqs * a.num_kv_heads;
+    const int n = ctrl[12];
+    for (int k = threadIdx.x; k < n; k += blockDim.x) {
+        L.rh[k] = l_rh[k];
+        L.off[k] = l_rh[kMaxLong + k];
+    }
+    if (threadIdx.x == 0) {
+        L.n = n;
+        L.chunks = ctrl[13];
+    }
+    __syncthreads();
+}
+// whether pair rh is a listed long pair (folded by fold_long_pairs)
+__device__ __forceinline__ bool is_listed(const LongPairs& L, int rh) {
+    int lo = 0, hi = L.n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (L.rh[mid] < rh) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo < L.n && L.rh[lo] == rh;
+}
+// The CTA's first pair: chunk task k of the long pairs runs on CTA k mod grid, and the pairs
+// continue the sequence, so that they land on other CTAs while there are enough.
+__device__ __forceinline__ int first_after_chunks(bool any_long, const LongPairs& L) {
+    if (!any_long) return blockIdx.x;
+    const int b = static_cast<int>(blockIdx.x) - L.chunks % static_cast<int>(gridDim.x);
+    return b < 0 ? b + static_cast<int>(gridDim.x) : b;
+}
+template <typename T, int D, int G, int NG>
+__device__ __forceinline__ void fold_long_pairs(const StepArgs& a, const int4* rec,
+                                                const UnitMap& m, LongPairs& L,
+                                                float2 (*s_ml)[G * D / 4],
+                                                float4 (*s_acc)[G * D / 4]) {
+    const int Hkv = a.num_kv_heads;
+    int32_t* ctr = ws_at<int32_t>(a, a.lay.pair_ctr);
+    for (int v = blockIdx.x; v < L.chunks; v += gridDim.x) {  // uniform over the CTA
+        int lo = 0, hi = L.n - 1;  // the entry k with off[k] <= v < off[k + 1]
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (L.off[mid] <= v) lo = mid;
+            else hi = mid - 1;
+        }
+        const int rh = L.rh[lo], c = v - L.off[lo];
+        const PairPieces pp = pair_pieces(rec, m, Hkv, rh);
+        const int nch = cdiv(pp.count, kPieceChunk), first = c * kPieceChunk;
+        combine_fold<T, D, G, NG>(a, SlotShift{pp.slots, first},
+                                  min(kPieceChunk, pp.count - first), false, pp.token, pp.g,
+                                  s_ml, s_acc);
+        __threadfence();  // the chunk state, before the arrival that publishes it
+        __syncthreads();
+        if (threadIdx.x == 0) L.last = atomicAdd(ctr + rh, 1) == nch - 1 ? 1 : 0;
+        __syncthreads();
+        if (L.last) {
+            __threadfence();
+            combine_fold<T, D, G, NG, true>(a, SlotChunks{pp.slots}, nch, true, pp.token, pp.g,
+                                            s_ml, s_acc);
+        }
+        __syncthreads();  // L.last and the shared fold state, before the next chunk
+    }
+}
+
+// The combine of a self-planned step with 16-bit pages, whose chunked tail gives many pairs
+// dozens of pieces: NG thread groups of a CTA share a pair's pieces (measured faster than
+// the per-group form below for them), long pairs are spread over the grid.
 template <typename T, int D, int G, int NG>
 __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_kernel(StepArgs a) {
     constexpr int TPG = G * D / 4;
     __shared__ float2 s_ml[NG > 1 ? NG : 1][TPG];
     __shared__ float4 s_acc[NG > 1 ? NG : 1][TPG];
+    __shared__ LongPairs s_long;
     const int Hkv = a.num_kv_heads;
     int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
     const int4* rec = ws_at<const int4>(a, a.lay.req_info);  // {token, seg0, keys, pages}
@@ -1404,36 +1613,29 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_kernel(StepArgs
         atomicExch(reinterpret_cast<unsigned long long*>(ctrl + 10), 0ull);
     __syncthreads();
     pdl_trigger();
-    const int nreq = ctrl[2], nw = ctrl[4];
-    const int64_t S = ctrl[5], C = ctrl[6], D0 = static_cast<int64_t>(nw) * S;
-    auto unit = [&](int64_t p) -> int64_t { return p < D0 ? p / S : nw + (p - D0) / C; };
-    auto unit_start = [&](int64_t u) -> int64_t { return u < nw ? u * S : D0 + (u - nw) * C; };
-    for (int rh = blockIdx.x; rh < nreq * Hkv; rh += gridDim.x) {  // uniform over the CTA
-        const int r = rh / Hkv, g = rh % Hkv;
-        const int4 rr = rec[r];
-        const int per = rr.w;
-        if (per == 0) continue;
-        const int64_t b = static_cast<int64_t>(rr.y) + static_cast<int64_t>(g) * per;
-        const int64_t e = b + per;
-        const int64_t u1 = unit(b), u2 = unit(e - 1);
-        if (u1 == u2) continue;
-        const SlotPieces slots{2 * u1 + (unit_start(u1) == b ? 0 : 1), 2 * (u1 + 1), 2};
-        combine_fold<T, D, G, NG>(a, slots, static_cast<int>(u2 - u1 + 1), true, rr.x, g,
-                                  s_ml, s_acc);
+    const int npairs = ctrl[2] * Hkv;
+    const UnitMap m = unit_map(ctrl);
+    const bool any_long = ctrl[12] > 0;
+    if (any_long) {
+        load_long_pairs(a, ctrl, s_long);
+        fold_long_pairs<T, D, G, NG>(a, rec, m, s_long, s_ml, s_acc);
+    }
+    // the pairs, on the CTAs after those that took the long pairs' chunks
+    for (int rh = first_after_chunks(any_long, s_long); rh < npairs; rh += gridDim.x) {
+        const PairPieces pp = pair_pieces(rec, m, Hkv, rh);  // uniform over the CTA
+        if (pp.count <= 1 || (any_long && pp.count > kLongPieces && is_listed(s_long, rh)))
+            continue;
+        combine_fold<T, D, G, NG>(a, pp.slots, pp.count, true, pp.token, pp.g, s_ml, s_acc);
     }
 }
 
 // The same combine for steps whose pairs mostly have few pieces (INT8 pages, whose units are
 // static but for a remainder): the CTA's NG thread groups take NG pairs at a time (pairs
 // blockIdx.x + k gridDim.x, so pairs of neighbouring requests land in different CTAs); a
-// group folds a pair of at most kSmallPieces pieces on its own, in one round of loads, and
-// the pairs with more (a long segment) are then folded by all groups together.
+// group folds a pair of at most kSmallPieces pieces on its own, in one round of loads; the
+// pairs with more are then folded by all groups together, and the long ones are spread over
+// the grid.
 constexpr int kSmallPieces = 8;
-struct PairPieces {
-    int count;        // pieces (<= 1: the decode kernel wrote the row)
-    int token, g;
-    SlotPieces slots;
-};
 template <typename T, int D, int G, int NG>
 __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_solo_kernel(StepArgs a) {
     using Cv = F16<T>;
@@ -1441,6 +1643,7 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_solo_kernel(Ste
     __shared__ float2 s_ml[NG > 1 ? NG : 1][TPG];
     __shared__ float4 s_acc[NG > 1 ? NG : 1][TPG];
     __shared__ int s_big[NG], s_nbig;
+    __shared__ LongPairs s_long;
     const int Hkv = a.num_kv_heads;
     int32_t* ctrl = ws_at<int32_t>(a, a.lay.ctrl);
     const int4* rec = ws_at<const int4>(a, a.lay.req_info);  // {token, seg0, keys, pages}
@@ -1453,35 +1656,25 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_solo_kernel(Ste
         atomicExch(reinterpret_cast<unsigned long long*>(ctrl + 10), 0ull);
     __syncthreads();
     pdl_trigger();
-    const int nreq = ctrl[2], nw = ctrl[4];
-    const int64_t S = ctrl[5], C = ctrl[6], D0 = static_cast<int64_t>(nw) * S;
-    auto unit = [&](int64_t p) -> int64_t { return p < D0 ? p / S : nw + (p - D0) / C; };
-    auto unit_start = [&](int64_t u) -> int64_t { return u < nw ? u * S : D0 + (u - nw) * C; };
-    auto pieces_of = [&](int rh) {
-        PairPieces pp{0, 0, 0, {0, 0, 0}};
-        const int r = rh / Hkv, g = rh % Hkv;
-        const int4 rr = rec[r];
-        const int per = rr.w;
-        if (per == 0) return pp;
-        const int64_t b = static_cast<int64_t>(rr.y) + static_cast<int64_t>(g) * per;
-        const int64_t u1 = unit(b), u2 = unit(b + per - 1);
-        pp.count = static_cast<int>(u2 - u1 + 1);
-        pp.token = rr.x;
-        pp.g = g;
-        pp.slots = SlotPieces{2 * u1 + (unit_start(u1) == b ? 0 : 1), 2 * (u1 + 1), 2};
-        return pp;
-    };
+    const int npairs = ctrl[2] * Hkv;
+    const UnitMap m = unit_map(ctrl);
+    const bool any_long = ctrl[12] > 0;
+    if (any_long) {
+        load_long_pairs(a, ctrl, s_long);
+        fold_long_pairs<T, D, G, NG>(a, rec, m, s_long, s_ml, s_acc);
+    }
     const int grp = threadIdx.x / TPG, tin = threadIdx.x % TPG;
     const int j = tin / (D / 4), dim = (tin % (D / 4)) * 4;
-    const int npairs = nreq * Hkv;
+    const int first = first_after_chunks(any_long, s_long);
     for (int round = 0; static_cast<int64_t>(round) * gridDim.x * NG < npairs; ++round) {
         if (threadIdx.x == 0) s_nbig = 0;
         __syncthreads();
-        const int rh = blockIdx.x + (round * NG + grp) * gridDim.x;
+        const int rh = first + (round * NG + grp) * gridDim.x;
         if (rh < npairs) {
-            const PairPieces pp = pieces_of(rh);
+            const PairPieces pp = pair_pieces(rec, m, Hkv, rh);
             if (pp.count > kSmallPieces) {
-                if (tin == 0) s_big[atomicAdd(&s_nbig, 1)] = rh;
+                if (tin == 0 && !(any_long && pp.count > kLongPieces && is_listed(s_long, rh)))
+                    s_big[atomicAdd(&s_nbig, 1)] = rh;
             } else if (pp.count > 1) {
                 // this group alone: every piece's loads in flight together
                 float2 ml[kSmallPieces];
@@ -1519,7 +1712,7 @@ __global__ void __launch_bounds__(G * D / 4 * NG) combine_pieces_solo_kernel(Ste
         }
         __syncthreads();
         for (int k = 0; k < s_nbig; ++k) {  // uniform over the CTA
-            const PairPieces pp = pieces_of(s_big[k]);
+            const PairPieces pp = pair_pieces(rec, m, Hkv, s_big[k]);
             combine_fold<T, D, G, NG>(a, pp.slots, pp.count, true, pp.token, pp.g, s_ml, s_acc);
         }
     }
@@ -1573,6 +1766,9 @@ WorkspaceLayout workspace_layout(int num_reqs, int num_q_heads, int num_kv_heads
     L.tiles = off; off = up(off + static_cast<size_t>(L.max_tiles) * 16);
     L.part_ml = off; off = up(off + static_cast<size_t>(L.max_items) * G * 8);
     L.part_o = off; off = up(off + static_cast<size_t>(L.max_items) * G * head_dim * 4);
+    L.pair_ctr = off;  // then the long-pair list: kMaxLong pairs, kMaxLong chunk offsets
+    off = up(off + (L.self_plan ? (static_cast<size_t>(num_reqs) * num_kv_heads + 2 * kMaxLong) * 4
+                                : 0));
     L.total = off;
     return L;
 }
@@ -1621,15 +1817,19 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
     // self-planned steps: at most four thread groups and 512 threads per CTA, so two CTAs
     // fit an SM
     constexpr int kNg4 = std::max(1, std::min(4, 512 / kTpg));
+    // A step with few (request, KV head) pairs spreads every pair over many units, so the
+    // grids do not shrink with the pairs: the long pairs' chunks need many CTAs.  (A wider
+    // grid than the work needs costs time: a combine CTA fills an SM's registers, so the next
+    // step's kernels wait for it to exit.)
     if (a.self_plan && Q8) {
-        // one CTA per SM at most, each taking kNg4 pairs at a time
+        // CTAs of kNg4 pairs at a time, at most one per SM; at least 64 for the chunks of
+        // long pairs (INT8 units are static: few pairs share ~2,000 of them)
         const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
         e = launch_pdl(combine_pieces_solo_kernel<T, D, G, kNg4>,
-                       dim3(std::min(cdiv(pairs, kNg4), a.num_sms)), dim3(kTpg * kNg4), 0,
-                       stream, a);
+                       dim3(std::min(a.num_sms, std::max(cdiv(pairs, kNg4), 64))),
+                       dim3(kTpg * kNg4), 0, stream, a);
     } else if (a.self_plan) {
-        const int pairs = std::max(1, a.num_reqs * a.num_kv_heads);
-        e = launch_pdl(combine_pieces_kernel<T, D, G, kNg4>, dim3(std::min(pairs, 2 * a.num_sms)),
+        e = launch_pdl(combine_pieces_kernel<T, D, G, kNg4>, dim3(2 * a.num_sms),
                        dim3(kTpg * kNg4), 0, stream, a);
     } else if (max_splits <= kManySplits) {
         e = launch_pdl(combine_kernel<T, D, G, 1, kCombineRow>, dim3(cap_small), dim3(kTpg), 0,

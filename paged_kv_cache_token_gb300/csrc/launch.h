@@ -41,7 +41,9 @@ struct AppendArgs {
 //   page, keys, pages per head} of every request, ctrl[1] / [2] / [4] for the total pages,
 //   the requests and the warps sharing them, and two partial slots per decode warp)
 struct WorkspaceLayout {
-    size_t ctrl, req_info, rows, items, tiles, part_ml, part_o, total;
+    size_t ctrl, req_info, rows, items, tiles, part_ml, part_o;
+    size_t pair_ctr;  // self-planned steps: an arrival count per (request, KV head)
+    size_t total;
     int max_rows, max_items, max_tiles, target_items;
     int self_plan;  // every request advances by <= 1 token, at most kSelfPlanMaxReqs of them
 };

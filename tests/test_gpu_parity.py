@@ -391,11 +391,45 @@ def test_long_contexts():
     assert worst[0] < 2e-2
 
 
+_LONG_SPECS = {
+    "one_long_row": [(131071, 0, 1)],
+    "long_among_short": [(60000, 0, 1)] + [(16 + (37 * i) % 600, 0, 1) for i in range(63)],
+    "four_equal_rows": [(8191, 0, 1)] * 4,
+}
+
+
+@pytest.mark.parametrize("kv_int8,fused", [(False, True), (False, False), (True, False)])
+@pytest.mark.parametrize("case", sorted(_LONG_SPECS))
+def test_decode_step_long_pairs(case, kv_int8, fused):
+    # decode-only steps whose (request, KV head) pairs span many more work units than one
+    # CTA folds at once: their pieces are folded in chunks on different CTAs and merged by
+    # whichever arrives last.  Every row against the oracle; a second run of the same step
+    # gives the same bits (the merge order does not depend on the arrival order).
+    w = custom(700 + len(case) + 2 * kv_int8 + fused, 32, 8, 128, 0, _LONG_SPECS[case])
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w, kv_int8=kv_int8)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    assert plan.max_q_len == 1
+    if fused:
+        out = runner.run_step_fused(kv, w, plan)
+        again = runner.run_step_fused(kv, w, plan)   # re-appends the same rows
+    else:
+        out = runner.run_step(kv, w, plan)
+        q, _, _ = runner.step_host_inputs(w, plan)
+        again = kv.attention(kv.upload(plan), runner.bits_to_tensor(q, w.dtype), w.scale)
+    assert kv.read_error() == 0
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    ref = oracle_rows_int8(w, plan) if kv_int8 else oracle_rows(w, plan)
+    assert_close(gpu_as_f64(out), ref, "long pairs %s" % case)
+
+
 def test_long_row_two_pass_combine():
-    # three decode rows, two steps: 131,071 cached keys (about 820 splits of 10 pages: the
-    # combine merges 64-split chunks, then the chunk states), 3,000 keys (under 64 splits:
-    # finished by the chunk pass) and 100 keys (one split: written by the decode kernel).
-    # The long row's second token opens page 8,192.
+    # three decode rows, two self-planned steps: 131,071 cached keys (its 8 KV-head segments
+    # span thousands of work units: folded in chunks on many CTAs, then merged), 3,000 keys
+    # (a few dozen pieces per segment, folded by one CTA) and 100 keys (7 pages per segment:
+    # mostly inside one unit, written by the decode kernel).  The long row's second token
+    # opens page 8,192.
     worst, _, _ = run_all(custom(610, 32, 8, 128, 0, [(131071, 0, 2), (3000, 0, 2),
                                                       (100, 0, 2)]))
     assert worst[0] < 2e-2
