@@ -22,6 +22,7 @@ timing is max over ranks and ``value`` counts the bytes of all ranks (weak scali
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same workload.
 """
 import argparse
+import gc
 import json
 import math
 import os
@@ -188,7 +189,16 @@ def build_decode_state(device, pool_pages=70000):
     return w, plan, kv, (q, k, v)
 
 
+def settle():
+    """Collects garbage before a timed section.  The cyclic collector stays off while the
+    bench runs (main): a collection landing in a timed loop of one or two milliseconds adds
+    its whole pause to the steps (measured: the INT8 decode step read 0.084 instead of
+    0.063 ms once the earlier sections had left enough live objects)."""
+    gc.collect()
+
+
 def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
+    settle()
     from paged_kv_cache_token_gb300 import binding, runner
     w, plan, kv, (qh, kh, vh) = build_decode_state(device, pool_pages)
     dt = w.dtype
@@ -304,6 +314,7 @@ def time_decode(device, steps, warmup, dist_ctx, pool_pages=70000):
 def time_decode_int8(device, steps, pool_pages=70000):
     """The decode step over INT8 pages (same requests and shapes; per-channel scales): step
     time, decode-kernel time and their algorithmic bytes."""
+    settle()
     from paged_kv_cache_token_gb300 import binding, runner
     w = W.decode_only(num_pages=pool_pages)
     s = scheduler_for(w)
@@ -355,6 +366,7 @@ def time_decode_int8(device, steps, pool_pages=70000):
 def time_prefill(device, reps=5, kv_int8=False):
     """Attention-kernel time of the 8K one-shot prefill and of the 4 x 2048 chunks (over
     INT8 pages with ``kv_int8``)."""
+    settle()
     from paged_kv_cache_token_gb300 import binding, runner
     res = {}
     for label, chunk in (("one_shot_8192", None), ("chunks_4x2048", 2048)):
@@ -406,6 +418,7 @@ def time_mixed(device, reps=3):
     30,000-token prompt, token budget 2048): every step's append + attention, each step
     repeated `reps` times back to back between events (the repeats rewrite the same pages
     with the same values and recompute the same outputs)."""
+    settle()
     from paged_kv_cache_token_gb300 import runner
     w = W.mixed()
     s = scheduler_for(w)
@@ -448,6 +461,7 @@ def time_decode_loop(device, reps=5):
     per-step time as separate steps (metadata of every step already on the device, append +
     attention launched from the host), as one device-side loop (lengths advanced on the
     device) and as one CUDA graph replay of all 64 steps."""
+    settle()
     from paged_kv_cache_token_gb300 import binding, runner
     w = W.mha_skew()
     s = scheduler_for(w)
@@ -499,6 +513,7 @@ def time_decode_loop_layers(device, n_layers=4, reps=5):
     the whole sequence is one CUDA graph, so per-layer steps read their K/V from HBM.  Timed
     twice: every layer planning its own step (pkv_paged_attention_step), and one plan per
     step shared by the layers (pkv_plan_attention + pkv_paged_attention_run)."""
+    settle()
     from paged_kv_cache_token_gb300 import runner
     w = W.mha_skew()
     s = scheduler_for(w)
@@ -657,6 +672,7 @@ def main():
             build.build()
         dist_ctx.barrier()
         binding.load()
+        gc.disable()  # sections collect before their timed regions (settle)
         device = torch.device("cuda", dist_ctx.local if dist_ctx.world > 1 else 0)
         torch.cuda.set_device(device)
         hbm, bf16, bf16_sus, peak_src = peaks()
