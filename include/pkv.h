@@ -16,6 +16,16 @@
  *  - Pointers named d_* or documented "device" are CUDA device pointers; all other
  *    pointers are host pointers.  The caller owns every buffer; the library allocates
  *    nothing and keeps no per-call state.
+ *  - Pinned host memory (cudaHostAlloc / cudaMallocHost) is mapped into the device's
+ *    address space at the same address (unified addressing).  q, k_new, v_new, out,
+ *    slot_mapping_out and the step description's four arrays may point there: the kernels
+ *    read and write them with plain loads and stores, which reach host memory over the
+ *    CPU-GPU link (NVLink-C2C on GB300), so a step moves its inputs and output with no
+ *    separate copy.  Exceptions: a step with max_q_len >= 16 (requests with 16 or more
+ *    new tokens run on the tensor-core prefill kernel) reads q with tensor-memory-
+ *    accelerator copies, which need device memory -- a host q is refused there with
+ *    PKV_ERR_INVALID_ARG; the pools, the scales, the workspace and the error flag are
+ *    device memory always.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *    Work is enqueued asynchronously; only pkv_read_device_error synchronises.
  *  - Return value: PKV_OK (0) or a negative pkv_status.  On an error detected on the

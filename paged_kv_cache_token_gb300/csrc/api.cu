@@ -28,6 +28,19 @@ int num_sms_current_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Whether p is device memory (or managed memory, which the device maps as its own).  Pinned
+// host memory is mapped into the device's address space too (unified addressing), and the
+// kernels' plain loads and stores reach it over the CPU-GPU link -- but the tensor-memory
+// accelerator copies of the prefill kernels need device memory.
+bool device_memory(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // an unregistered host pointer: clear the sticky-free error
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
 // Checks shared by both calls.  Returns PKV_OK or the first problem found.
 int check_desc(const pkv_step_desc* d) {
     if (!d) return PKV_ERR_INVALID_ARG;
@@ -252,6 +265,9 @@ int attention_impl(const pkv_step_desc* desc, const void* q, const void* k_cache
     const pkv::WorkspaceLayout lay = layout_for(desc, sms, int8);
     if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_WORKSPACE;
+    // steps that can have prefill tiles read q with TMA: it must be device memory
+    if (phase != Phase::kPlanOnly && lay.max_tiles > 0 && !device_memory(q))
+        return PKV_ERR_INVALID_ARG;
 
     pkv::StepArgs a{};
     a.num_reqs = desc->num_reqs;

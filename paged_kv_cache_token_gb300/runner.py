@@ -284,6 +284,68 @@ class StepStaging:
         self.out_host.copy_(self.out, non_blocking=True)
 
 
+class HostStaging(StepStaging):
+    """A decode step's inputs and output kept in pinned host memory and used in place.
+
+    Pinned host memory is mapped into the device's address space at the same address, and
+    the decode kernels read Q, the new K/V and the step's four metadata arrays from it and
+    write the output rows into it: plain loads and stores over the CPU-GPU link (NVLink-C2C
+    on GB300).  One library call per step then moves the step's bytes both ways, with no
+    copy-engine transfer and no cross-stream event wait between the step's kernels and
+    its neighbours' (such a wait ends their programmatic overlap).  Decode steps only: with
+    max_q_len >= 16 the library reads Q with tensor-memory-accelerator copies and refuses
+    host memory.  ``upload`` and ``download`` do nothing; ``stage`` rewrites the buffer, so
+    call it only once the GPU is done with the previous step that used it.
+    """
+
+    def _ensure(self, nbytes: int, out_bytes: int) -> None:
+        if self._host is None or self._host.numel() < nbytes:
+            self._host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+            self._dev = self._host
+        if self._out_host is None or self._out_host.numel() < out_bytes:
+            self._out_host = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+            self._out_dev = self._out_host
+
+    def upload(self) -> None:
+        pass
+
+    def download(self) -> None:
+        pass
+
+
+class HostPipeline:
+    """Consecutive decode steps on one stream through two HostStaging buffers.
+
+    Step i uses buffer i % 2 (and, with ``kv_alt``, the second set of pools on odd steps).
+    ``launch`` is the one library call of the step plus an event; ``stage`` waits for the
+    event of the step that last used the buffer before rewriting it; ``result`` waits for
+    the step's event and returns the pinned output, valid until the buffer's next launch.
+    """
+
+    def __init__(self, kv: PagedKV, stream=None, kv_alt: Optional[PagedKV] = None):
+        self.stg = [HostStaging(kv), HostStaging(kv_alt if kv_alt is not None else kv)]
+        self.stream = stream or torch.cuda.current_stream(kv.device)
+        self.done = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+
+    def stage(self, slot: int, plan: StepPlan, q_bits: np.ndarray, k_bits: np.ndarray,
+              v_bits: np.ndarray) -> None:
+        if plan.max_q_len >= 16:
+            raise ValueError("HostPipeline runs decode steps (max_q_len < 16)")
+        if self.used[slot]:
+            self.done[slot].synchronize()
+        self.stg[slot].stage(plan, q_bits, k_bits, v_bits)
+
+    def launch(self, slot: int, scale: float) -> None:
+        self.stg[slot].run(scale, self.stream)
+        self.done[slot].record(self.stream)
+        self.used[slot] = True
+
+    def result(self, slot: int) -> torch.Tensor:
+        self.done[slot].synchronize()
+        return self.stg[slot].out_host
+
+
 class StepPipeline:
     """Consecutive steps through two stagings, with the copies on their own streams.
 

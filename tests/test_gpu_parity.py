@@ -380,6 +380,60 @@ def test_decode_step_with_idle_requests(kv_int8):
     assert all(np.array_equal(a, b) for a, b in zip(fp, sp))
 
 
+@pytest.mark.parametrize("kv_int8", [False, True])
+def test_host_resident_decode_steps(kv_int8):
+    # decode steps whose Q, new K/V, metadata and output stay in pinned host memory, read
+    # and written in place by the kernels: the same output bits and pool bytes as the
+    # copy-engine pipeline over device buffers, and every row against the oracle
+    ctx = [0, 1, 15, 16, 17, 100, 255, 256, 1000, 3000]
+    w = custom(2100 + kv_int8, 32, 8, 128, 0, [(c, 0, 3) for c in ctx])
+    res = {}
+    for host in (True, False):
+        s = scheduler_for(w)
+        kv = runner.paged_kv_for(w, kv_int8=kv_int8)
+        runner.load_history(kv, w, s.history_plan())
+        pipe = runner.HostPipeline(kv) if host else runner.StepPipeline(kv)
+        outs, plans = [], []
+        for i, plan in enumerate(s.all_steps()):
+            q, k, v = runner.step_host_inputs(w, plan)
+            pipe.stage(i % 2, plan, q, k, v)
+            pipe.launch(i % 2, w.scale)
+            outs.append(pipe.result(i % 2).clone())
+            plans.append(plan)
+        torch.cuda.synchronize()
+        assert kv.read_error() == 0
+        res[host] = (outs, pool_bits(kv))
+    (ho, hp), (do, dp) = res[True], res[False]
+    assert len(ho) == len(do) == 3
+    for i, plan in enumerate(plans):
+        assert torch.equal(ho[i].view(torch.int16), do[i].view(torch.int16)), i
+        ref = oracle_rows_int8(w, plan) if kv_int8 else oracle_rows(w, plan)
+        assert_close(gpu_as_f64(ho[i]), ref, "host-resident step %d" % i)
+    assert all(np.array_equal(a, b) for a, b in zip(hp, dp))
+
+
+def test_host_q_refused_on_prefill_steps():
+    # a step with a 40-token prefill reads Q with tensor-memory-accelerator copies: a Q in
+    # pinned host memory is refused on the host, before anything is launched
+    w = custom(2150, 8, 2, 128, 0, [(0, 40, 0), (20, 0, 1)])
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    plan = s.next_step()
+    assert plan.max_q_len >= 16
+    q, _, _ = runner.step_host_inputs(w, plan)
+    ds = kv.upload(plan)
+    out = torch.full((plan.total_q_tokens, w.num_q_heads, w.head_dim), 7.0,
+                     dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.PkvError) as e:
+        kv.attention_desc(ds.desc, runner.bits_to_tensor(q, w.dtype, "cpu", pin=True), out,
+                          w.scale, kv.workspace(ds.desc))
+    assert e.value.status == -1  # PKV_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+    with pytest.raises(ValueError):
+        runner.HostPipeline(kv).stage(0, plan, q, q, q)
+
+
 def test_long_contexts():
     # maximum-size rows: a decode row over 131,071 cached tokens (8,192 pages, about 900
     # splits per (row, KV head); with up to 45 decode rows possible in this step the combine
