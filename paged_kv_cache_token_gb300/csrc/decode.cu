@@ -816,6 +816,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         nxt = resolve(i1, ra, rb);
     }
     int cur_win = load_window(cur, 0), cur_win_base = 0;
+    // the window after cur_win, loaded 32 pages ahead of its use: the block table can be a
+    // round trip away (L2, or host memory over the CPU-GPU link)
+    int cur_pf = cur.np > 32 ? load_window(cur, 32) : 0;
     int nxt_win = load_window(nxt, 0);
     // Over an earlier plan only the work list (written by a plan that completed before this
     // grid launched) and the block table were read so far.  The preceding kernel may still
@@ -881,7 +884,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         if (ic < cur.np) {
             if (ic >= cur_win_base + 32) {
                 cur_win_base += 32;
-                cur_win = load_window(cur, cur_win_base);
+                cur_win = cur_pf;
+                cur_pf = cur.np > cur_win_base + 32 ? load_window(cur, cur_win_base + 32) : 0;
             }
             win = cur_win;
             lidx = ic - cur_win_base;
@@ -1278,6 +1282,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         app_cur = app_nxt;
         cur_win = nxt_win;
         cur_win_base = 0;
+        cur_pf = cur.np > 32 ? load_window(cur, 32) : 0;
         if constexpr (kPrefetchQ) {
 #pragma unroll
             for (int u = 0; u < NQ; ++u) q_cur[u] = q_nxt[u];
