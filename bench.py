@@ -798,7 +798,8 @@ def main():
                             "of cache in all, above L2), all layers' append + attention in one "
                             "CUDA graph" % (ml["layers"], ml["layers"] *
                                             ml["bytes_per_layer_step"] / 1e6),
-                **ml, "frac_of_hbm": ml["shared_plan"]["GBps"] / hbm}
+                **ml, "frac_of_hbm": max(ml["plan_per_layer"]["GBps"],
+                                         ml["shared_plan"]["GBps"]) / hbm}
         if not args.no_prefill and dist_ctx.rank == 0:
             mx = time_mixed(device)
             line["mixed_step"] = {

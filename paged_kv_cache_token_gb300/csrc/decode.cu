@@ -48,6 +48,7 @@ constexpr int kManySplits = 64;   // rows that may have more splits get a groupe
 constexpr int kChunkedCtas = 4096;  // largest grid of the two-pass combine
 constexpr int kDecMaxCtasPerSm = 3;  // decode CTAs an SM can hold (INT8 pages)
 constexpr int kMinChunkPages = 4;    // smallest dynamic chunk of a self-planned step
+constexpr int kStaticOnlyPagesPerWarp = 32;  // below this per warp: no 3/4 static split
 constexpr int kSlotsPerWarp = 6;     // partial slots a self-planned step may use per warp
 
 template <typename T>
@@ -615,8 +616,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
         // at most; the rest serve the chunks)
         sp_nw = min(min(nwarps, sp_total), a.lay.max_items / kSlotsPerWarp);
         if (sp_nw > 0) {
+            // small steps (few pages per warp) are all static, as INT8 steps are: there a
+            // piece's setup outweighs what the chunks even out
+            const bool all_static = Q8 || sp_total < kStaticOnlyPagesPerWarp * sp_nw;
             const SelfPlanUnits u = self_plan_units(sp_total, sp_nw, a.lay.max_items,
-                                                    Q8 ? 1 : 3, Q8 ? 1 : 4);
+                                                    all_static ? 1 : 3, all_static ? 1 : 4);
             sp_static = u.static_pages;
             sp_chunk = u.chunk_pages;
             sp_chunks = u.chunks;
