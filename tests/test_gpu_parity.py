@@ -478,6 +478,24 @@ def test_decode_step_long_pairs(case, kv_int8, fused):
     assert_close(gpu_as_f64(out), ref, "long pairs %s" % case)
 
 
+@pytest.mark.parametrize("hq,hkv,d,dtype,case", [(32, 32, 128, 1, "four_equal_rows"),
+                                                 (8, 1, 64, 0, "one_long_row"),
+                                                 (16, 2, 64, 1, "long_among_short")])
+def test_decode_step_long_pairs_head_shapes(hq, hkv, d, dtype, case):
+    # the long-pair combine with other group sizes and head dims (thread groups of 32 to
+    # 256 threads): fused decode steps against the oracle, repeated runs bit-identical
+    w = custom(760 + hq + d, hq, hkv, d, dtype, _LONG_SPECS[case])
+    s = scheduler_for(w)
+    kv = runner.paged_kv_for(w)
+    runner.load_history(kv, w, s.history_plan())
+    plan = s.next_step()
+    out = runner.run_step_fused(kv, w, plan)
+    again = runner.run_step_fused(kv, w, plan)
+    assert kv.read_error() == 0
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    assert_close(gpu_as_f64(out), oracle_rows(w, plan), "long pairs %s %d/%d" % (case, hq, hkv))
+
+
 def test_long_row_two_pass_combine():
     # three decode rows, two self-planned steps: 131,071 cached keys (its 8 KV-head segments
     # span thousands of work units: folded in chunks on many CTAs, then merged), 3,000 keys
