@@ -77,8 +77,12 @@ __device__ __forceinline__ long long sum_ceil(long long a, long long b, long lon
 
 // Lengths of request r, all four loads issued together (no dependent round trip).
 struct ReqLens { int q, c, t0; bool ok; };
+// Read before the kernel's dependency wait (the lengths are final before the step starts).
+// context_lens is the one step input a library kernel updates in place (advance_context,
+// between the steps of a device-side loop): it fences its write before letting this grid
+// launch, and the read goes to L2, past any line an SM's L1 kept from an earlier step.
 __device__ __forceinline__ ReqLens load_request(const StepArgs& a, int r) {
-    const int q = a.q_lens[r], c = a.context_lens[r];
+    const int q = a.q_lens[r], c = __ldcg(a.context_lens + r);
     const int o0 = a.q_offsets[r], o1 = a.q_offsets[r + 1];
     return ReqLens{q, c, o0, request_ok(a, q, c, o0, o1)};
 }

@@ -178,12 +178,15 @@ int launch_kv_append_int8(const AppendArgs& a, cudaStream_t stream) {
 }
 
 // context_lens[r] += q_lens[r]: the step's tokens are now cached.  Earlier kernels on the
-// stream (the attention step) read the lengths, so the update waits for them.
+// stream (the attention step) read the lengths, so the update waits for them.  The next
+// step's kernels read the lengths before their own dependency wait, so the update is
+// fenced to the device's point of coherence before they may launch.
 __global__ void __launch_bounds__(256) advance_context_kernel(const int32_t* q_lens,
                                                               int32_t* context_lens, int n) {
     pdl_wait();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r < n) context_lens[r] += q_lens[r];
+    __threadfence();
     pdl_trigger();
 }
 
