@@ -187,6 +187,21 @@ PKV_API int pkv_append_attention(const pkv_step_desc* desc, const void* k_new, c
                                  size_t workspace_bytes, int32_t* dev_err_flag, void* stream);
 
 /*
+ * pkv_append_attention_int8 -- pkv_kv_append_int8 followed by pkv_paged_attention_step_int8,
+ * in one call (INT8 pools; the arguments of those two calls).  Decode steps of at most 256
+ * requests run as one decode grid, as in pkv_append_attention: the warp that streams a
+ * (request, KV head)'s last page quantises the request's new K and V rows with the same
+ * arithmetic as pkv_kv_append_int8 (so the pool bytes and slot ids are identical) and writes
+ * them into that page before reading it.  Other steps run the two calls' kernels.
+ */
+PKV_API int pkv_append_attention_int8(const pkv_step_desc* desc, const void* k_new,
+                                      const void* v_new, const float* k_scale,
+                                      const float* v_scale, int8_t* k_cache, int8_t* v_cache,
+                                      int64_t* slot_mapping_out, const void* q, void* out,
+                                      float scale, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_err_flag, void* stream);
+
+/*
  * pkv_plan_attention, pkv_paged_attention_run -- the attention step in two halves, so that
  * one plan serves every layer of a model step.  The step's work list (decode rows, split-KV
  * items, prefill tiles) depends only on the lengths and the block table, which every layer

@@ -30,7 +30,7 @@ EXPORTED = ("pkv_kv_append", "pkv_advance_context", "pkv_attention_workspace_byt
             "pkv_attention_workspace_bytes_int8", "pkv_paged_attention_step_int8",
             "pkv_paged_attention_step_static_ws", "pkv_plan_attention",
             "pkv_paged_attention_run", "pkv_paged_attention_run_int8", "pkv_copy_pages",
-            "pkv_append_attention",
+            "pkv_append_attention", "pkv_append_attention_int8",
             "pkv_read_device_error", "pkv_set_kernel_events", "pkv_status_string",
             "pkv_version")
 
@@ -88,6 +88,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_append_attention.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V, V,
                                          ctypes.c_float, V, sz, V, V]
     lib.pkv_append_attention.restype = ctypes.c_int
+    lib.pkv_append_attention_int8.argtypes = [ctypes.POINTER(StepDesc), V, V, V, V, V, V, V,
+                                              V, V, ctypes.c_float, V, sz, V, V]
+    lib.pkv_append_attention_int8.restype = ctypes.c_int
     lib.pkv_copy_pages.argtypes = [ctypes.POINTER(StepDesc), V, V, ctypes.c_int32, V, V,
                                    ctypes.c_int, V, V]
     lib.pkv_copy_pages.restype = ctypes.c_int
@@ -195,6 +198,23 @@ def append_attention(desc: StepDesc, k_new, v_new, k_cache, v_cache, q, out, sca
                                      _stream(stream))
     if check and rc != OK:
         raise PkvError("pkv_append_attention", rc)
+    return rc
+
+
+def append_attention_int8(desc: StepDesc, k_new, v_new, k_scale, v_scale, k_cache, v_cache, q,
+                          out, scale: float, workspace, slot_mapping=None, err=None, stream=None,
+                          check: bool = True, workspace_bytes: Optional[int] = None) -> int:
+    """kv_append_int8 then the INT8 attention step in one call (one fused grid for decode
+    steps)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None \
+        else workspace_bytes
+    rc = load().pkv_append_attention_int8(ctypes.byref(desc), _ptr(k_new), _ptr(v_new),
+                                          _ptr(k_scale), _ptr(v_scale), _ptr(k_cache),
+                                          _ptr(v_cache), _ptr(slot_mapping), _ptr(q), _ptr(out),
+                                          float(scale), _ptr(workspace), nbytes, _ptr(err),
+                                          _stream(stream))
+    if check and rc != OK:
+        raise PkvError("pkv_append_attention_int8", rc)
     return rc
 
 

@@ -374,6 +374,36 @@ int pkv_append_attention(const pkv_step_desc* desc, const void* k_new, const voi
                           dev_err_flag, stream, nullptr, nullptr);
 }
 
+int pkv_append_attention_int8(const pkv_step_desc* desc, const void* k_new, const void* v_new,
+                              const float* k_scale, const float* v_scale, int8_t* k_cache,
+                              int8_t* v_cache, int64_t* slot_mapping_out, const void* q,
+                              void* out, float scale, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err_flag, void* stream) {
+    int rc = check_desc(desc);
+    if (rc != PKV_OK) return rc;
+    if (desc->total_q_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    if (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale))
+        return PKV_ERR_INVALID_ARG;
+    if (slot_mapping_out && (reinterpret_cast<uintptr_t>(slot_mapping_out) & 7u))
+        return PKV_ERR_INVALID_ARG;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    if (layout_for(desc, sms, true).self_plan) {
+        // one decode grid quantises, appends and attends
+        if (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache))
+            return PKV_ERR_INVALID_ARG;
+        const FusedAppend f{k_new, v_new, slot_mapping_out};
+        return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                              dev_err_flag, stream, k_scale, v_scale, Phase::kPlanAndRun, &f);
+    }
+    if ((rc = kv_append_impl(desc, k_new, v_new, k_cache, v_cache, slot_mapping_out,
+                             dev_err_flag, stream, k_scale, v_scale)) != PKV_OK)
+        return rc;
+    return attention_impl(desc, q, k_cache, v_cache, out, scale, workspace, workspace_bytes,
+                          dev_err_flag, stream, k_scale, v_scale);
+}
+
 int pkv_plan_attention(const pkv_step_desc* desc, void* workspace, size_t workspace_bytes,
                        int32_t* dev_err_flag, void* stream) {
     return attention_impl(desc, nullptr, nullptr, nullptr, nullptr, 1.f, workspace,

@@ -105,6 +105,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// One INT8 code of a KV element: the element divided by its channel's fixed scale (IEEE
+// division), rounded to the nearest integer (ties to even), clamped to [-127, 127], as the
+// code's two's-complement byte.  The quantiser of wmrh.cn/news/64708 §4.3, the same in
+// every kernel that writes INT8 pages.
+__device__ __forceinline__ uint32_t int8_code(float x, float s) {
+    const int c = max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
+    return static_cast<uint32_t>(c) & 0xFFu;
+}
+
 // ---------------------------------------------------------------- bulk async copy (TMA, 1-D)
 // Global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte aligned) that
 // signals completion on `bar` through the transaction count.

@@ -987,6 +987,58 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                 const uint8_t* sK = ring + stage * S::kStageBytes;   // [16 tokens][D] codes
                 const uint8_t* sV = sK + S::kPageBytes;               // [D][16 tokens] codes
                 const int nvalid = min(kPage, cur.nkv - (cur.pb + i) * kPage);
+                const bool patch = a.fused_append && i == cur.np - 1 && holds_last(cur);
+                if (patch) {
+                    // this step's row of the segment's last page, quantised as the INT8
+                    // append does: lane l's channels l DPL .. into the staged page (K: row
+                    // `slot`; V: column `slot` of the [D][16] block) and into the pool
+                    constexpr int DPL = D / 32;
+                    const int phys = __shfl_sync(kFull, cur_win, i - cur_win_base);
+                    const int slot = (cur.nkv - 1) % kPage;
+                    if (phys >= 0) {
+                        const int64_t src =
+                            (static_cast<int64_t>(cur.t) * Hkv + cur.g) * D + lane * DPL;
+                        const int chan = cur.g * D + lane * DPL;
+                        const uint16_t* ks = static_cast<const uint16_t*>(a.k_new) + src;
+                        const uint16_t* vs = static_cast<const uint16_t*>(a.v_new) + src;
+                        uint32_t kword = 0, vq[DPL];
+#pragma unroll
+                        for (int e = 0; e < DPL; e += 2) {
+                            const float2 kf =
+                                Cv::unpack(__ldg(reinterpret_cast<const uint32_t*>(ks + e)));
+                            const float2 vf =
+                                Cv::unpack(__ldg(reinterpret_cast<const uint32_t*>(vs + e)));
+                            kword |= int8_code(kf.x, __ldg(a.k_scale + chan + e)) << (8 * e);
+                            kword |= int8_code(kf.y, __ldg(a.k_scale + chan + e + 1))
+                                     << (8 * (e + 1));
+                            vq[e] = int8_code(vf.x, __ldg(a.v_scale + chan + e));
+                            vq[e + 1] = int8_code(vf.y, __ldg(a.v_scale + chan + e + 1));
+                        }
+                        const int64_t block =
+                            (static_cast<int64_t>(phys) * Hkv + cur.g) * kPage * D;
+                        uint8_t* kst = const_cast<uint8_t*>(sK) + slot * D + lane * DPL;
+                        uint8_t* kpo = static_cast<uint8_t*>(const_cast<void*>(a.k_cache)) +
+                                       block + slot * D + lane * DPL;
+                        if constexpr (DPL == 4) {
+                            *reinterpret_cast<uint32_t*>(kst) = kword;
+                            *reinterpret_cast<uint32_t*>(kpo) = kword;
+                        } else {
+                            *reinterpret_cast<uint16_t*>(kst) = static_cast<uint16_t>(kword);
+                            *reinterpret_cast<uint16_t*>(kpo) = static_cast<uint16_t>(kword);
+                        }
+                        uint8_t* vst = const_cast<uint8_t*>(sV) + slot;
+                        uint8_t* vpo = static_cast<uint8_t*>(const_cast<void*>(a.v_cache)) +
+                                       block + slot;
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) {
+                            vst[(lane * DPL + e) * kPage] = static_cast<uint8_t>(vq[e]);
+                            vpo[(lane * DPL + e) * kPage] = static_cast<uint8_t>(vq[e]);
+                        }
+                    }
+                    if (phys >= 0 && lane == 0 && cur.g == 0 && a.slot_mapping)
+                        a.slot_mapping[cur.t] = static_cast<int64_t>(phys) * kPage + slot;
+                    __syncwarp();
+                }
                 // key words of rows kr0, kr1 (D/4 bytes each; rows kr0 of lanes qg = 2p and
                 // 2p + 1 share banks, a 2-way conflict the shared-memory pipe absorbs)
                 uint32_t k0[KW], k1[KW];
@@ -1050,6 +1102,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(StepArgs a) {
                               minus_1152_h2(codes_lo_h2(x1)), minus_1152_h2(codes_hi_h2(x0)),
                               minus_1152_h2(codes_hi_h2(x1)), pb0, pb1);
                 }
+                if (patch) fence_proxy_async_smem();  // the patched stage is refilled by a copy
                 __syncwarp();
                 issue_one();  // refill the stage just freed
             }

@@ -104,10 +104,7 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendArgs a) {
     }
     const int ntok = min(kTokPerBlock, qlen - tok0);
     const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.max_pages;
-    auto quant = [](float x, float s) {
-        const int c = max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
-        return static_cast<uint32_t>(c) & 0xFFu;  // the code's two's-complement byte
-    };
+    auto quant = [](float x, float s) { return int8_code(x, s); };
     for (int w = warp; w < ntok * a.num_kv_heads; w += blockDim.x / 32) {
         const int i = tok0 + w / a.num_kv_heads, h = w % a.num_kv_heads;
         const int t = start + i;

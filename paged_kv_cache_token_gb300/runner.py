@@ -126,11 +126,12 @@ class PagedKV:
 
     def append_attention_desc(self, desc, k_new, v_new, q, out, scale: float, ws,
                               slot_mapping=None, stream=None) -> None:
-        """kv_append then the attention step (16-bit pools in one call, fused into one decode
-        grid for decode steps; INT8 pools as the two calls)."""
+        """kv_append then the attention step in one call (fused into one decode grid for
+        decode steps), for 16-bit and INT8 pools."""
         if self.kv_int8:
-            self.append_desc(desc, k_new, v_new, slot_mapping, stream)
-            self.attention_desc(desc, q, out, scale, ws, stream)
+            binding.append_attention_int8(desc, k_new, v_new, self.k_scale, self.v_scale,
+                                          self.k_cache, self.v_cache, q, out, scale, ws,
+                                          slot_mapping, self.err, stream)
         else:
             binding.append_attention(desc, k_new, v_new, self.k_cache, self.v_cache, q, out,
                                      scale, ws, slot_mapping, self.err, stream)

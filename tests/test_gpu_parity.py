@@ -150,13 +150,13 @@ def test_decode_batches(hq, hkv, d, dtype):
     run_all(w)
 
 
-def _steps_both_ways(w):
-    """Every step of w through pkv_append_attention and through the two separate calls, on
-    fresh pools: (outputs, slot ids, pool bits) of each, and the plans."""
+def _steps_both_ways(w, kv_int8=False):
+    """Every step of w through pkv_append_attention(_int8) and through the two separate
+    calls, on fresh pools: (outputs, slot ids, pool bits) of each, and the plans."""
     res = {}
     for fused in (True, False):
         s = scheduler_for(w)
-        kv = runner.paged_kv_for(w)
+        kv = runner.paged_kv_for(w, kv_int8=kv_int8)
         runner.load_history(kv, w, s.history_plan())
         outs, slots, plans = [], [], []
         for plan in s.all_steps():
@@ -191,6 +191,24 @@ def test_fused_append_attention_decode_steps(hq, hkv, d, dtype):
         assert torch.equal(fo[i].view(torch.int16), so[i].view(torch.int16)), i
         assert torch.equal(fs[i], ss[i]), i
         assert_close(gpu_as_f64(fo[i]), oracle_rows(w, plan), "fused step %d" % i)
+    assert all(np.array_equal(a, b) for a, b in zip(fp, sp))
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(32, 8, 128, 0), (8, 8, 128, 1), (16, 2, 64, 1),
+                                            (8, 1, 64, 0)])
+def test_fused_append_attention_int8_decode_steps(hq, hkv, d, dtype):
+    # decode steps through pkv_append_attention_int8: the warp streaming a (request, KV
+    # head)'s last page quantises the new row (the INT8 append's arithmetic) into it first.
+    # Outputs, slot ids and every pool byte equal the separate kv_append_int8 + attention
+    # calls, and every row matches the INT8 oracle.
+    ctx = [0, 1, 15, 16, 17, 100, 255, 256, 1000, 3000]
+    w = custom(1850 + hq + d, hq, hkv, d, dtype, [(c, 0, 3) for c in ctx])
+    res, plans = _steps_both_ways(w, kv_int8=True)
+    (fo, fs, fp), (so, ss, sp) = res[True], res[False]
+    for i, plan in enumerate(plans):
+        assert torch.equal(fo[i].view(torch.int16), so[i].view(torch.int16)), i
+        assert torch.equal(fs[i], ss[i]), i
+        assert_close(gpu_as_f64(fo[i]), oracle_rows_int8(w, plan), "fused INT8 step %d" % i)
     assert all(np.array_equal(a, b) for a, b in zip(fp, sp))
 
 
@@ -452,7 +470,8 @@ _LONG_SPECS = {
 }
 
 
-@pytest.mark.parametrize("kv_int8,fused", [(False, True), (False, False), (True, False)])
+@pytest.mark.parametrize("kv_int8,fused", [(False, True), (False, False), (True, True),
+                                           (True, False)])
 @pytest.mark.parametrize("case", sorted(_LONG_SPECS))
 def test_decode_step_long_pairs(case, kv_int8, fused):
     # decode-only steps whose (request, KV head) pairs span many more work units than one
