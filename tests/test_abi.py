@@ -177,3 +177,21 @@ def test_append_attention_argument_checks(lib):
               q_offsets=None, context_lens=None, block_table=None)
     assert lib.pkv_append_attention(ctypes.byref(e), None, None, None, None, None, None, None,
                                     1.0, None, 0, None, None) == 0
+
+
+def test_append_attention_int8_argument_checks(lib):
+    d = _desc()
+    t, odd = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1008)
+    call = lambda *a: lib.pkv_append_attention_int8(ctypes.byref(d), *a)
+    # args: k_new, v_new, k_scale, v_scale, k_cache, v_cache, slot_mapping, q, out, scale,
+    # workspace, bytes, err, stream -- refused on the host before any device query
+    assert call(None, t, t, t, t, t, None, t, t, 1.0, t, 1 << 30, None, None) == -1
+    assert call(t, odd, t, t, t, t, None, t, t, 1.0, t, 1 << 30, None, None) == -1
+    assert call(t, t, None, t, t, t, None, t, t, 1.0, t, 1 << 30, None, None) == -1   # no scales
+    assert call(t, t, t, odd, t, t, None, t, t, 1.0, t, 1 << 30, None, None) == -1
+    assert call(t, t, t, t, t, t, ctypes.c_void_p(0x1004), t, t, 1.0, t, 1 << 30, None,
+                None) == -1
+    e = _desc(num_reqs=0, total_q_tokens=0, max_q_len=0, max_context_len=0, q_lens=None,
+              q_offsets=None, context_lens=None, block_table=None)
+    assert lib.pkv_append_attention_int8(ctypes.byref(e), None, None, None, None, None, None,
+                                         None, None, None, 1.0, None, 0, None, None) == 0
