@@ -1895,7 +1895,19 @@ static int launch_decode_t(const StepArgs& a, cudaStream_t stream, cudaEvent_t e
                        dim3(std::min(a.num_sms, std::max(cdiv(pairs, kNg4), 64))),
                        dim3(kTpg * kNg4), 0, stream, a);
     } else if (a.self_plan) {
-        e = launch_pdl(combine_pieces_kernel<T, D, G, kNg4>, dim3(2 * a.num_sms),
+        // one wave: as many CTAs per SM as fit, at most two (a CTA of 512 threads fills an
+        // SM's registers, one of 128 threads -- G = 1 -- leaves room for more; measured: a
+        // second wave of the big CTAs cost the 64-request step 1.2 us, halving the small
+        // ones cost the MHA-skew steps 8-10%)
+        static int per_sm = 0;  // benign race: every thread computes the same value
+        if (per_sm == 0) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &n, combine_pieces_kernel<T, D, G, kNg4>, kTpg * kNg4, 0) != cudaSuccess)
+                return PKV_ERR_CUDA;
+            per_sm = std::max(1, std::min(2, n));
+        }
+        e = launch_pdl(combine_pieces_kernel<T, D, G, kNg4>, dim3(per_sm * a.num_sms),
                        dim3(kTpg * kNg4), 0, stream, a);
     } else if (max_splits <= kManySplits) {
         e = launch_pdl(combine_kernel<T, D, G, 1, kCombineRow>, dim3(cap_small), dim3(kTpg), 0,
